@@ -1,0 +1,160 @@
+"""Reference planner (numpy) -- the bit-exact target of the device planner.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the product path.
+
+Three outputs, all integer, all unique under the canonical orderings below.
+
+1. Degree buckets.  deg_i = row_ptr[i+1] - row_ptr[i].  With inclusive upper
+   bounds b_1 < ... < b_{B-2}: bucket 0 holds deg 0, bucket k (1 <= k <= B-2)
+   holds b_{k-1} < deg <= b_k (b_0 = 0), bucket B-1 holds deg > b_{B-2}.
+   ``bucket_rows`` lists rows grouped by bucket, ascending id inside a bucket;
+   ``bucket_ptr`` (B+1) is the exclusive scan of bucket sizes.
+
+2. Heavy-row chunks.  A row is heavy when deg > heavy_threshold.  Heavy rows in
+   ascending id; row r is cut into ceil(deg/C) chunks of C consecutive CSR
+   positions (the last one shorter).  ``chunks`` is (n_chunks, 3) int32 of
+   (row, e_begin, e_end); ``heavy_chunk_ptr`` (n_heavy+1) the scan of chunk
+   counts.
+
+3. Binary Sparse Block (BSB) tiles of 16-row windows, after the Fused3S
+   figure 1 caption (sciencestack.ai/paper/2505.08098, Figure 1: a row window
+   is "compacted, tiled, and stored in BSB format", TCB 16x8).  Window w holds
+   rows [16w, 16w+16).  U_w = sorted unique sources of its edges.  It gets
+   T_w = ceil(|U_w| / 8) tiles; tile t covers U_w[8t .. 8t+8), padded with -1.
+   ``win_tile_ptr`` (W+1) is the scan of T_w.  Each tile has a 128-bit
+   bitmap stored as four little-endian uint32 words: bit r*8 + c (word
+   (r*8+c)//32) is set iff the CSR holds an edge (16w + r <- tile_cols[8t+c]).
+   ``win_nnz`` counts CSR entries per window; ``win_flags`` bit 0 marks a
+   window with a repeated (row, source) pair, bit 1 a window that takes the
+   tile path.  A window takes the tile path when the tile path is enabled and
+   it has no repeated pair, 1 <= T_w <= max_tiles, no heavy row, and
+   1000 * nnz >= density_milli * 128 * T_w.  ``tile_windows`` lists them in
+   ascending order.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+WIN_ROWS = 16
+TILE_COLS = 8
+FLAG_DUP = 1
+FLAG_TILE = 2
+
+
+def degrees(row_ptr: np.ndarray) -> np.ndarray:
+    return np.diff(row_ptr.astype(np.int64))
+
+
+def degree_buckets(row_ptr: np.ndarray, bounds) -> dict:
+    deg = degrees(row_ptr)
+    bounds = np.asarray(bounds, dtype=np.int64)
+    nb = len(bounds) + 2
+    bucket = np.where(deg == 0, 0, 1 + np.searchsorted(bounds, deg, side="left"))
+    order = np.argsort(bucket, kind="stable")  # stable: ascending id inside a bucket
+    counts = np.bincount(bucket, minlength=nb)
+    ptr = np.zeros(nb + 1, np.int64)
+    np.cumsum(counts, out=ptr[1:])
+    return dict(bucket_of=bucket.astype(np.uint8), bucket_ptr=ptr.astype(np.int32),
+                bucket_rows=order.astype(np.int32))
+
+
+def heavy_chunks(row_ptr: np.ndarray, heavy_threshold: int, chunk_edges: int) -> dict:
+    deg = degrees(row_ptr)
+    heavy = np.flatnonzero(deg > heavy_threshold)
+    nch = (deg[heavy] + chunk_edges - 1) // chunk_edges
+    hptr = np.zeros(heavy.size + 1, np.int64)
+    np.cumsum(nch, out=hptr[1:])
+    rows = np.repeat(heavy, nch)
+    local = np.arange(int(hptr[-1])) - np.repeat(hptr[:-1], nch)
+    start = row_ptr[rows].astype(np.int64) + local * chunk_edges
+    end = np.minimum(start + chunk_edges, row_ptr[rows + 1].astype(np.int64))
+    chunks = np.stack([rows, start, end], axis=1).astype(np.int32).reshape(-1, 3)
+    return dict(heavy_rows=heavy.astype(np.int32), heavy_chunk_ptr=hptr.astype(np.int32),
+                chunks=chunks)
+
+
+def bsb(row_ptr: np.ndarray, col_idx: np.ndarray, num_nodes: int) -> dict:
+    n = int(num_nodes)
+    deg = degrees(row_ptr)
+    W = (n + WIN_ROWS - 1) // WIN_ROWS
+    rows = np.repeat(np.arange(n, dtype=np.int64), deg)
+    src = col_idx.astype(np.int64)
+    win = rows // WIN_ROWS
+    r_in = rows % WIN_ROWS
+
+    # sorted unique (window, source) pairs
+    key = win * n + src
+    order = np.argsort(key, kind="stable")
+    ks = key[order]
+    first = np.ones(ks.size, dtype=bool)
+    first[1:] = ks[1:] != ks[:-1]
+    ukey = ks[first]
+    uwin = ukey // n
+    usrc = ukey % n
+    ucount = np.bincount(uwin, minlength=W).astype(np.int64)
+    ntiles = (ucount + TILE_COLS - 1) // TILE_COLS
+    win_tile_ptr = np.zeros(W + 1, np.int64)
+    np.cumsum(ntiles, out=win_tile_ptr[1:])
+    T = int(win_tile_ptr[-1])
+    ustart = np.zeros(W + 1, np.int64)
+    np.cumsum(ucount, out=ustart[1:])
+    upos = np.arange(ukey.size, dtype=np.int64) - ustart[uwin]  # rank inside U_w
+
+    tile_cols = np.full(T * TILE_COLS, -1, np.int64)
+    tile_cols[win_tile_ptr[uwin] * TILE_COLS + upos] = usrc
+
+    # every edge -> (tile, column slot) -> bit
+    uid_sorted = np.cumsum(first) - 1
+    uid = np.empty_like(uid_sorted)
+    uid[order] = uid_sorted
+    pos = upos[uid]
+    tile = win_tile_ptr[win] + pos // TILE_COLS
+    bit = r_in * TILE_COLS + pos % TILE_COLS
+    words = np.zeros((T, 4), np.uint32)
+    np.bitwise_or.at(words, (tile, bit // 32), (np.uint32(1) << (bit % 32).astype(np.uint32)))
+
+    # repeated (row, source) pairs
+    rkey = np.sort(rows * n + src)
+    dup_at = np.flatnonzero(rkey[1:] == rkey[:-1])
+    win_dup = np.zeros(W, bool)
+    win_dup[(rkey[dup_at] // n) // WIN_ROWS] = True
+
+    win_nnz = np.bincount(win, minlength=W).astype(np.int64)
+    return dict(win_tile_ptr=win_tile_ptr.astype(np.int32),
+                tile_cols=tile_cols.astype(np.int32),
+                tile_bits=words,
+                win_nnz=win_nnz.astype(np.int32),
+                win_dup=win_dup)
+
+
+def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold: int,
+                   max_tiles: int, density_milli: int) -> dict:
+    W = b["win_nnz"].shape[0]
+    flags = np.where(b["win_dup"], FLAG_DUP, 0).astype(np.uint8)
+    if enabled:
+        deg = degrees(row_ptr)
+        n = deg.shape[0]
+        pad = np.zeros(W * WIN_ROWS, np.int64)
+        pad[:n] = deg
+        maxdeg = pad.reshape(W, WIN_ROWS).max(axis=1)
+        nt = np.diff(b["win_tile_ptr"].astype(np.int64))
+        nnz = b["win_nnz"].astype(np.int64)
+        ok = (~b["win_dup"]) & (nt >= 1) & (nt <= max_tiles) & (maxdeg <= heavy_threshold) \
+            & (1000 * nnz >= int(density_milli) * 128 * nt)
+        flags = flags | np.where(ok, FLAG_TILE, 0).astype(np.uint8)
+    tile_windows = np.flatnonzero(flags & FLAG_TILE).astype(np.int32)
+    return dict(win_flags=flags, tile_windows=tile_windows)
+
+
+def full_plan(row_ptr, col_idx, num_nodes, bounds=(32, 256, 2048), heavy_threshold=512,
+              chunk_edges=256, with_bsb=True, tile_enabled=False, max_tiles=32,
+              density_milli=150) -> dict:
+    out = {}
+    out.update(degree_buckets(row_ptr, bounds))
+    out.update(heavy_chunks(row_ptr, heavy_threshold, chunk_edges))
+    if with_bsb:
+        b = bsb(row_ptr, col_idx, num_nodes)
+        out.update(b)
+        out.update(tile_selection(row_ptr, b, tile_enabled, heavy_threshold, max_tiles, density_milli))
+    return out

@@ -1,0 +1,137 @@
+"""The numpy reference planner against brute-force loops and invariants (CPU)."""
+import numpy as np
+import pytest
+
+import graphgen
+from oracle import planner
+
+
+def _graphs():
+    yield "random", graphgen.random_csr(70, 30, seed=1, zero_frac=0.2)
+    yield "unsorted", graphgen.random_csr(53, 40, seed=2, zero_frac=0.1, sorted_rows=False)
+    yield "multigraph", graphgen.random_csr(45, 25, seed=3, zero_frac=0.2, multigraph=True)
+    yield "tiny", graphgen.tiny_poisson(num_nodes=37, seed=4)
+    yield "dense", graphgen.batched_dense(num_graphs=5, seed=5)
+    yield "one_row", graphgen.random_csr(1, 1, seed=6, zero_frac=0.0)
+
+
+def brute_bsb(row_ptr, col, n):
+    """Window-by-window restatement with Python loops (tiny graphs only)."""
+    W = (n + 15) // 16
+    tile_ptr, cols, bits, nnz, dup = [0], [], [], [], []
+    for w in range(W):
+        rows = range(16 * w, min(16 * w + 16, n))
+        srcs = sorted({int(col[e]) for r in rows for e in range(row_ptr[r], row_ptr[r + 1])})
+        nt = (len(srcs) + 7) // 8
+        tile_ptr.append(tile_ptr[-1] + nt)
+        padded = srcs + [-1] * (8 * nt - len(srcs))
+        cols += padded
+        for t in range(nt):
+            word = [0, 0, 0, 0]
+            for r in rows:
+                present = {int(col[e]) for e in range(row_ptr[r], row_ptr[r + 1])}
+                for c in range(8):
+                    s = padded[8 * t + c]
+                    if s >= 0 and s in present:
+                        b = (r - 16 * w) * 8 + c
+                        word[b // 32] |= 1 << (b % 32)
+            bits.append(word)
+        nnz.append(sum(int(row_ptr[r + 1] - row_ptr[r]) for r in rows))
+        d = False
+        for r in rows:
+            s = [int(col[e]) for e in range(row_ptr[r], row_ptr[r + 1])]
+            d |= len(s) != len(set(s))
+        dup.append(d)
+    return (np.array(tile_ptr), np.array(cols, dtype=np.int64), np.array(bits, dtype=np.uint64).reshape(-1, 4),
+            np.array(nnz), np.array(dup, bool))
+
+
+@pytest.mark.parametrize("name,g", list(_graphs()), ids=[n for n, _ in _graphs()])
+def test_bsb_matches_brute_force(name, g):
+    b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    tp, cols, bits, nnz, dup = brute_bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    assert np.array_equal(b["win_tile_ptr"], tp)
+    assert np.array_equal(b["tile_cols"], cols)
+    assert np.array_equal(b["tile_bits"].astype(np.uint64), bits.reshape(-1, 4))
+    assert np.array_equal(b["win_nnz"], nnz)
+    assert np.array_equal(b["win_dup"], dup)
+
+
+@pytest.mark.parametrize("name,g", list(_graphs()), ids=[n for n, _ in _graphs()])
+def test_bsb_decodes_to_csr(name, g):
+    b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    n = g.num_nodes
+    got = set()
+    bits = b["tile_bits"]
+    popc = 0
+    for w in range(b["win_tile_ptr"].size - 1):
+        t0, t1 = b["win_tile_ptr"][w], b["win_tile_ptr"][w + 1]
+        cw = b["tile_cols"][8 * t0:8 * t1]
+        real = cw[cw >= 0]
+        assert np.all(np.diff(real) > 0)  # strictly increasing
+        assert np.all(cw[real.size:] == -1)  # padding only at the end
+        assert t1 - t0 == (real.size + 7) // 8  # minimal tile count
+        for t in range(t0, t1):
+            for bit in range(128):
+                if (int(bits[t, bit // 32]) >> (bit % 32)) & 1:
+                    r, c = divmod(bit, 8)
+                    assert b["tile_cols"][8 * t + c] >= 0
+                    got.add((16 * w + r, int(b["tile_cols"][8 * t + c])))
+                    popc += 1
+    want = {(i, int(s)) for i in range(n) for s in g.col_idx[g.row_ptr[i]:g.row_ptr[i + 1]]}
+    assert got == want
+    if name != "multigraph":
+        assert popc == g.num_edges
+
+
+def test_degree_buckets_brute_force():
+    g = graphgen.powerlaw(num_nodes=3000, max_degree=2500, seed=9)
+    bounds = (3, 10, 100)
+    b = planner.degree_buckets(g.row_ptr, bounds)
+    deg = g.degrees()
+    lists = [[], [], [], [], []]
+    for i, d in enumerate(deg):
+        if d == 0:
+            k = 0
+        elif d <= 3:
+            k = 1
+        elif d <= 10:
+            k = 2
+        elif d <= 100:
+            k = 3
+        else:
+            k = 4
+        lists[k].append(i)
+    flat = [i for lst in lists for i in lst]
+    assert np.array_equal(b["bucket_rows"], flat)
+    assert np.array_equal(b["bucket_ptr"], np.cumsum([0] + [len(x) for x in lists]))
+
+
+def test_heavy_chunks_cover_rows():
+    g = graphgen.powerlaw(num_nodes=3000, max_degree=2500, seed=10)
+    T, C = 40, 16
+    h = planner.heavy_chunks(g.row_ptr, T, C)
+    deg = g.degrees()
+    assert np.array_equal(h["heavy_rows"], np.flatnonzero(deg > T))
+    ch = h["chunks"]
+    for k, r in enumerate(h["heavy_rows"]):
+        mine = ch[h["heavy_chunk_ptr"][k]:h["heavy_chunk_ptr"][k + 1]]
+        assert np.all(mine[:, 0] == r)
+        assert mine[0, 1] == g.row_ptr[r] and mine[-1, 2] == g.row_ptr[r + 1]
+        assert np.all(mine[1:, 1] == mine[:-1, 2])
+        assert np.all(mine[:, 2] - mine[:, 1] <= C) and np.all(mine[:, 2] > mine[:, 1])
+        assert np.all(mine[:-1, 2] - mine[:-1, 1] == C)
+
+
+def test_tile_selection_brute_force():
+    g = graphgen.batched_dense(num_graphs=12, seed=11)
+    b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=40, max_tiles=6, density_milli=200)
+    deg = g.degrees()
+    W = b["win_nnz"].size
+    for w in range(W):
+        nt = b["win_tile_ptr"][w + 1] - b["win_tile_ptr"][w]
+        md = deg[16 * w:16 * w + 16].max()
+        ok = (not b["win_dup"][w]) and 1 <= nt <= 6 and md <= 40 and b["win_nnz"][w] / (128.0 * nt) >= 0.2
+        assert bool(sel["win_flags"][w] & planner.FLAG_TILE) == ok
+    assert np.array_equal(sel["tile_windows"], np.flatnonzero(sel["win_flags"] & planner.FLAG_TILE))
