@@ -1,0 +1,390 @@
+"""Throughput benchmark of the fused sparse graph attention forward pass.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl g3s|reference]
+                    [--workload lognormal_local] [--size full|small]
+
+One step = one g3s_forward over the whole graph (fused kernel, plus the merge
+of heavy-row partials), inputs resident in HBM.  The default workload is the
+large HBM-bound graph: N = 2,000,000 nodes, log-normal(3.6, 0.8) in-degree
+(~100.7M edges), 60% of sources within +-4096 of the destination, 4 heads x
+32, bf16, standard softmax.  Its inputs (~2.5 GB touched per step) are far
+larger than L2, so no explicit flush runs between steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
+replica of the workload on its own GPU (independent problems, no collective
+on the data path: weak scaling); time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on the same workload, a bounded sample of rows per step, on the
+host cores of rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import graphgen  # noqa: E402
+
+METRIC = "edges/s of fused sparse graph attention; % of HBM or tensor-pipe roofline"
+UNIT = "edges/s"
+ELT = {"f32": 4, "f16": 2, "bf16": 2}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
+
+
+def kernel_sources_hash() -> str:
+    csrc = os.path.join(ROOT, "sparse_graph_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per forward from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % workload)
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_sources_sha256") != kernel_sources_hash():
+        return None
+    try:
+        return int(kv["dram_bytes_per_forward"])
+    except (KeyError, ValueError):
+        return None
+
+
+def byte_counts(g, w, out_dtype):
+    """Algorithmic bytes of one forward.
+
+    gathered:    CSR + Q once per row + K and V once per edge (+ E in, Eout out) + O
+    compulsory:  every array touched once
+    """
+    e, eo = ELT[w.dtype], ELT[out_dtype]
+    N, E, HD = g.num_nodes, g.num_edges, w.heads * w.head_dim
+    csr = 4 * (N + 1) + 4 * E
+    node = N * HD * e
+    out = N * HD * eo
+    edge_feat = (E * HD * (e + eo)) if w.variant == "rtmscore" else 0
+    gathered = csr + node + 2 * E * HD * e + edge_feat + out
+    compulsory = csr + 3 * node + out + edge_feat
+    return gathered, compulsory
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="g3s_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.NAMES, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_rate(g, w, t, target_s: float, rows_start: int = 0):
+    """Time the fp64 oracle on a contiguous block of rows sized for ~target_s.
+
+    Returns (edges/s, seconds, rows, edges, threads)."""
+    import oracle
+
+    deg = g.degrees()
+    args = (g.row_ptr, g.col_idx, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, t["Q"], t["K"], t["V"],
+            t.get("E"))
+    # calibration on a small block
+    n_cal = min(g.num_nodes, 2000)
+    rows = np.arange(rows_start, rows_start + n_cal) % g.num_nodes
+    t0 = time.perf_counter()
+    oracle.forward(*args, rows=rows)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rate = deg[rows].sum() / dt
+    want_edges = rate * target_s
+    cum = np.cumsum(deg)
+    n_rows = int(min(g.num_nodes, max(1, np.searchsorted(cum, want_edges) + 1)))
+    rows = np.arange(rows_start, rows_start + n_rows) % g.num_nodes
+    t0 = time.perf_counter()
+    oracle.forward(*args, rows=rows)
+    dt = time.perf_counter() - t0
+    edges = int(deg[rows].sum())
+    return edges / dt, dt, n_rows, edges, oracle.threads()
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["g3s", "reference"], default="g3s")
+    ap.add_argument("--workload", default="lognormal_local", choices=list(graphgen.WORKLOADS))
+    ap.add_argument("--size", default="full", choices=["full", "small"])
+    ap.add_argument("--nodes", type=int, default=None, help="override the workload's node count (profiling)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    g, vals, w = graphgen.make_workload(args.workload, args.size)
+    t = {k: graphgen.to_dtype(v, w.dtype) for k, v in vals.items()}
+    per_step = max(0.2, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    start = 0
+    for _ in range(args.warmup):
+        _, _, n, _, _ = oracle_rate(g, w, t, per_step, start)
+        start = (start + n) % g.num_nodes
+    total_edges, total_s, threads = 0, 0.0, 1
+    for _ in range(args.steps):
+        _, dt, n, edges, threads = oracle_rate(g, w, t, per_step, start)
+        start = (start + n) % g.num_nodes
+        total_edges += edges
+        total_s += dt
+    value = total_edges / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "num_nodes": g.num_nodes, "num_edges": g.num_edges, "heads": w.heads,
+                   "head_dim": w.head_dim, "input_dtype": w.dtype, "variant": w.variant},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "per step a contiguous block of rows (~%.1f s of fp64 oracle work), "
+                                   "%d edges over %d steps" % (per_step, total_edges, args.steps)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+
+    import sparse_graph_attention_gb300 as g3s
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    over = {} if args.nodes is None else {"num_nodes": args.nodes}
+    g, vals, w = graphgen.make_workload(args.workload, args.size, **over)
+    t = {k: graphgen.to_dtype(v, w.dtype) for k, v in vals.items()}
+    rp = torch.from_numpy(g.row_ptr).to(dev)
+    ci = torch.from_numpy(g.col_idx).to(dev)
+    dQ, dK, dV = (t[k].to(dev) for k in "QKV")
+    dE = t["E"].to(dev) if w.variant == "rtmscore" else None
+    stream = torch.cuda.current_stream(dev)
+
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant)
+    torch.cuda.synchronize(dev)
+    plan_ms = 1000.0 * (time.perf_counter() - t0)
+    st = plan.stats()
+    launches = 1 + (1 if st["chunks"] > 0 else 0) + (1 if st["tile_windows"] > 0 else 0)
+
+    odt = g3s.torch_dtype(plan.out_dtype)
+    O = torch.empty(dQ.shape, dtype=odt, device=dev)
+    Eout = torch.empty(dE.shape, dtype=odt, device=dev) if dE is not None else None
+
+    def step():
+        if w.variant == "rtmscore":
+            plan.forward(dQ, dK, dV, dE, O, Eout)
+        else:
+            plan.forward(dQ, dK, dV, None, O)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K forwards, inputs resident ----------------------
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.3)  # let the sampler start before the work does
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist:
+        x = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        total_ms = float(x.item())
+    ms_per_step = total_ms / args.steps
+    edges_all = g.num_edges * args.steps * world
+    value = edges_all / (total_ms / 1000.0)
+
+    # ---- roofline of the forward (fused kernel + heavy-row merge) --------
+    gathered, compulsory = byte_counts(g, w, plan.out_dtype)
+    fwd_s = statistics.mean(per_launch_ms) / 1000.0
+    peak, peak_src = measured_hbm_peak()
+    achieved = gathered / fwd_s / 1e9
+    traffic = recorded_traffic(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_source": peak_src,
+                "kernel": "g3s_forward (fused CUDA-core kernel + heavy-row merge)",
+                "bytes_model": "gathered: CSR + Q + K,V per edge (+E, Eout) + O; L2 reuse of local sources lets "
+                               "frac exceed 1",
+                "compulsory_gbs": compulsory / fwd_s / 1e9,
+                "compulsory_frac": compulsory / fwd_s / 1e9 / peak}
+    if traffic is not None:
+        roofline["dram_gbs"] = traffic / fwd_s / 1e9
+        roofline["dram_frac"] = traffic / fwd_s / 1e9 / peak
+
+    # ---- end to end through the C ABI on host buffers --------------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: t[k].pin_memory() for k in t}
+        Oh = torch.empty(pin["Q"].shape, dtype=odt).pin_memory()
+        Eoh = torch.empty(pin["E"].shape, dtype=odt).pin_memory() if w.variant == "rtmscore" else None
+        staging = torch.empty(plan.staging_size(), dtype=torch.uint8, device=dev)
+
+        def host_step():
+            plan.forward_host(pin["Q"], pin["K"], pin["V"], Oh, pin.get("E"), Eoh, staging=staging)
+
+        for _ in range(2):
+            host_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        n_e2e = max(1, min(args.steps, 50))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            host_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b)
+        if dist:
+            x = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            e2e_ms = float(x.item())
+        hd = w.heads * w.head_dim
+        nb, nbo = g.num_nodes * hd * ELT[w.dtype], g.num_nodes * hd * ELT[plan.out_dtype]
+        eb, ebo = g.num_edges * hd * ELT[w.dtype], g.num_edges * hd * ELT[plan.out_dtype]
+        h2d = 3 * nb + (eb if w.variant == "rtmscore" else 0)
+        d2h = nbo + (ebo if w.variant == "rtmscore" else 0)
+        e2e = {"value": g.num_edges * n_e2e * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, dt, n_rows, edges, threads = oracle_rate(g, w, t, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "rows 0..%d (%d edges, %.1f s) of the same workload, fp64 oracle" % (n_rows - 1, edges, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "num_nodes": g.num_nodes,
+                       "num_edges": g.num_edges, "heads": w.heads, "head_dim": w.head_dim, "variant": w.variant,
+                       "out_dtype": plan.out_dtype, "accumulation": "f32",
+                       "l2": "no flush: inputs larger than L2 (%.2f GB touched per step)" % (compulsory / 1e9),
+                       "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+            "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms,
+            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tile_windows": st["tile_windows"]},
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * g3s.h -- C ABI of libg3s, fused sparse graph attention ("3S") on GB300.
+ *
+ * For every destination row i of a CSR graph (rows = destinations, columns =
+ * sources) and every head h, one pass computes
+ *   SDDMM    l_ij = <q_i, k_j> / sqrt(d)              over the in-edges of i
+ *   softmax  a_ij = exp(l_ij - max_j l_ij) / sum_j exp(l_ij - max_j l_ij)
+ *   SpMM     o_i  = sum_j a_ij v_j                    (o_i = 0 when i has no in-edge)
+ * This is the three-step pattern named in the Fused3S abstract
+ * (sciencestack.ai/paper/2505.08098, Abstract: "SDDMM, softmax normalization,
+ * and SpMM") and the per-node gather of the Triton article
+ * (stondelli.it/articles/gattn-triton, "Using the CSC index for fast edge
+ * lookup").
+ *
+ * The RTMScore edge-modulated variant (same article, "Background" list and
+ * "Fusing the full graph attention", the eager torch_attn listing) replaces
+ * the logit and the softmax by
+ *   t_ij = clamp(q_i * k_j / sqrt(d), -5, 5)   (elementwise; optional)
+ *   u_ij = t_ij * e_ij                          (elementwise, stored as Eout)
+ *   s_ij = exp(clamp(sum_f u_ij, -5, 5)),  a_ij = s_ij / (sum_j s_ij + eps)
+ *
+ * Memory model.  Every array belongs to the caller: this library allocates no
+ * device or host memory after g3s_plan_create returns (the plan's small host
+ * struct is the only allocation it ever makes).  Device pointers must stay
+ * valid while a plan or a call uses them.  All work is enqueued on the given
+ * stream; g3s_plan_create synchronises that stream (once, or twice with
+ * validation on) to read back the plan's sizes, g3s_forward never does.
+ *
+ * Errors.  Every entry point returns a g3s_status; no exception or abort
+ * crosses the ABI.  g3s_last_error() gives a human-readable detail of the
+ * last failure on the calling thread.
+ *
+ * Layouts (row-major, contiguous, little-endian):
+ *   row_ptr  int32 [N+1]      row_ptr[0] = 0, non-decreasing, row_ptr[N] = E
+ *   col_idx  int32 [E]        sources of row i at col_idx[row_ptr[i] .. row_ptr[i+1])
+ *   Q, K, V      [N][H][d]    element type = the plan's dtype
+ *   O            [N][H][d]    element type = the plan's out_dtype (fp32 by default)
+ *   Eproj        [E][H][d]    the plan's dtype, indexed by CSR position (RTMScore only)
+ *   Eout         [E][H][d]    the plan's out_dtype, indexed by CSR position
+ * Limits: E < 2^31; d in {16, 32, 64, 128}; H*d*sizeof(dtype) a power of two
+ * between 16 B and 4 KiB; every value pointer 16-byte aligned.
+ */
+#ifndef G3S_H
+#define G3S_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *g3s_stream_t;
+
+typedef enum g3s_status {
+    G3S_OK = 0,
+    G3S_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, plan mismatch */
+    G3S_ERR_UNSUPPORTED = 2, /* shape or dtype without a compiled kernel */
+    G3S_ERR_BAD_GRAPH = 3,   /* CSR failed validation (see g3s_last_error) */
+    G3S_ERR_WORKSPACE = 4,   /* workspace missing, misaligned or too small */
+    G3S_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    G3S_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} g3s_status;
+
+typedef enum g3s_dtype { G3S_F32 = 0, G3S_F16 = 1, G3S_BF16 = 2 } g3s_dtype;
+
+typedef enum g3s_variant {
+    G3S_STANDARD = 0, /* softmax(<q,k>/sqrt d) */
+    G3S_RTMSCORE = 1  /* exp(clip(sum clamp(q*k/sqrt d)*e)) / (sum + eps), with Eout */
+} g3s_variant;
+
+#define G3S_NUM_BUCKETS 5
+
+/*
+ * Planner options.  Fill with g3s_plan_options_init, then override.
+ *  bucket_bounds   inclusive upper degree bounds of buckets 1..3 (bucket 0 is
+ *                  degree 0, bucket 4 is above bucket_bounds[2]); default 32, 256, 2048
+ *  heavy_threshold rows with more in-edges are cut into chunks processed by
+ *                  several warps and merged (default 512)
+ *  chunk_edges     CSR positions per chunk of a heavy row (default 256)
+ *  bsb             build the 16x8 BSB tiles: 1 on, 0 off, -1 when the tile path
+ *                  is eligible (default -1)
+ *  tile_path       route dense row windows to the tensor-core kernel: 1 on,
+ *                  0 off, -1 automatic (default -1: on where compiled)
+ *  tile_density_milli  a window takes the tile path when
+ *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 150)
+ *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default 32)
+ *  bsb_smem_edges  windows with more CSR entries than this are compacted by
+ *                  the global-bitmap planner kernel instead of the shared-
+ *                  memory sort (default 2048; a testing knob)
+ *  rtm_elementwise_clamp  1: clamp q*k/sqrt(d) elementwise before *e, the
+ *                  order of the article's code (default); 0: skip that clamp
+ *  rtm_epsilon     the variant's denominator epsilon (default 1e-6)
+ *  validate_graph  1: check the CSR on the device before planning (default)
+ *  out_dtype       element type of O and Eout: G3S_F32 (default) or the input
+ *                  dtype.  fp32 keeps the fp32 accumulation; a 16-bit store adds
+ *                  up to one half-ulp of rounding (2^-8 relative for bf16)
+ */
+typedef struct g3s_plan_options {
+    int32_t bucket_bounds[G3S_NUM_BUCKETS - 2];
+    int32_t heavy_threshold;
+    int32_t chunk_edges;
+    int32_t bsb;
+    int32_t tile_path;
+    int32_t tile_density_milli;
+    int32_t tile_max_tiles;
+    int32_t bsb_smem_edges;
+    int32_t rtm_elementwise_clamp;
+    float rtm_epsilon;
+    int32_t validate_graph;
+    int32_t out_dtype;
+} g3s_plan_options;
+
+typedef struct g3s_plan_stats {
+    int64_t num_nodes, num_edges;
+    int32_t heads, head_dim, dtype, variant, out_dtype, reserved0;
+    int64_t bucket_count[G3S_NUM_BUCKETS];
+    int64_t heavy_rows, chunks;
+    int32_t has_bsb, tile_path;
+    int64_t windows, tiles, tile_windows, dup_windows, large_windows;
+    int64_t tile_window_nnz; /* CSR entries handled by the tile path */
+    size_t workspace_used;
+} g3s_plan_stats;
+
+/* Planner arrays readable with g3s_plan_export (all int32 unless noted). */
+typedef enum g3s_plan_array {
+    G3S_ARR_BUCKET_PTR = 0,      /* [G3S_NUM_BUCKETS+1] scan of bucket sizes */
+    G3S_ARR_BUCKET_ROWS = 1,     /* [N] rows by bucket, ascending id inside */
+    G3S_ARR_HEAVY_ROWS = 2,      /* [heavy_rows] ascending */
+    G3S_ARR_HEAVY_CHUNK_PTR = 3, /* [heavy_rows+1] */
+    G3S_ARR_CHUNKS = 4,          /* [chunks][3] (row, e_begin, e_end) */
+    G3S_ARR_WIN_TILE_PTR = 5,    /* [W+1], W = ceil(N/16) */
+    G3S_ARR_TILE_COLS = 6,       /* [tiles][8], -1 padded */
+    G3S_ARR_TILE_BITS = 7,       /* uint32 [tiles][4], bit r*8+c of a 128-bit word */
+    G3S_ARR_WIN_NNZ = 8,         /* [W] CSR entries per window */
+    G3S_ARR_WIN_FLAGS = 9,       /* uint8 [W]: bit0 repeated edge, bit1 tile path */
+    G3S_ARR_TILE_WINDOWS = 10    /* [tile_windows] ascending */
+} g3s_plan_array;
+
+typedef struct g3s_plan g3s_plan; /* opaque */
+
+/* Library version string, e.g. "g3s 0.1 sm_103a". Never NULL. */
+const char *g3s_version(void);
+
+/* Name of a status code. Never NULL. */
+const char *g3s_status_string(g3s_status status);
+
+/* Detail of the last failing call on this thread ("" when none). Never NULL. */
+const char *g3s_last_error(void);
+
+/* Fill *opts with the defaults listed above. */
+void g3s_plan_options_init(g3s_plan_options *opts);
+
+/*
+ * Upper bound of the workspace bytes a plan for these sizes needs, for any
+ * graph with N nodes and E edges.  opts may be NULL (defaults).
+ * INVALID_ARG for negative sizes or a NULL *bytes; UNSUPPORTED for shapes
+ * without a kernel.
+ */
+g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int heads, int head_dim,
+                                   g3s_dtype dtype, g3s_variant variant,
+                                   const g3s_plan_options *opts, size_t *bytes);
+
+/*
+ * Build a plan for one graph on the current CUDA device (the degree
+ * buckets, heavy-row chunks and BSB tiles, all on the device).
+ *   row_ptr_d, col_idx_d  device CSR arrays; must outlive the plan
+ *   workspace_d           device memory of workspace_bytes, 256-byte aligned,
+ *                         owned by the caller, must outlive the plan
+ *   stream                all planner kernels run here; synchronised before return
+ *   out                   receives the plan; free with g3s_plan_destroy
+ * Returns BAD_GRAPH when validation finds row_ptr[0] != 0, a decreasing
+ * row_ptr, row_ptr[N] != E or a source outside [0, N).  With validation off
+ * a malformed CSR is undefined behaviour.
+ */
+g3s_status g3s_plan_create(const int32_t *row_ptr_d, const int32_t *col_idx_d, int64_t num_nodes,
+                           int64_t num_edges, int heads, int head_dim, g3s_dtype dtype,
+                           g3s_variant variant, const g3s_plan_options *opts, void *workspace_d,
+                           size_t workspace_bytes, g3s_stream_t stream, g3s_plan **out);
+
+/* Sizes and counts of a plan. */
+g3s_status g3s_plan_get_stats(const g3s_plan *plan, g3s_plan_stats *stats);
+
+/*
+ * Copy one planner array to host memory.  bytes_needed (may be NULL)
+ * receives its size; host_dst may be NULL to query only.  Otherwise bytes
+ * must be at least that size.  Synchronous (blocks on the plan's stream).
+ * UNSUPPORTED for BSB arrays of a plan built without BSB.
+ */
+g3s_status g3s_plan_export(const g3s_plan *plan, g3s_plan_array which, void *host_dst, size_t bytes,
+                           size_t *bytes_needed);
+
+/*
+ * One fused forward pass over the whole graph, enqueued on `stream`.
+ *   Q, K, V  device [N][H][d] inputs
+ *   Eproj    device [E][H][d] edge projections; RTMScore only, else NULL
+ *   O        device [N][H][d] output in out_dtype (fully overwritten)
+ *   Eout     device [E][H][d] updated edge features in out_dtype (RTMScore;
+ *            NULL skips the store)
+ * Uses the plan's workspace for heavy-row partials, so calls that share a
+ * plan must not overlap on the device.  Asynchronous: returns after the
+ * launches are enqueued.  INVALID_ARG for NULL / misaligned pointers or an
+ * Eproj that does not match the variant; CUDA when a launch fails.
+ */
+g3s_status g3s_forward(const g3s_plan *plan, const void *Q, const void *K, const void *V,
+                       const void *Eproj, void *O, void *Eout, g3s_stream_t stream);
+
+/*
+ * Bytes of device staging g3s_forward_host needs for this plan: room for
+ * Q, K, V, O (and Eproj, Eout for RTMScore), each 256-byte aligned.
+ */
+g3s_status g3s_host_staging_size(const g3s_plan *plan, size_t *bytes);
+
+/*
+ * g3s_forward on HOST buffers: copies Q, K, V (and Eproj) host->device into
+ * the caller's device staging area, runs the forward pass, and copies O (and
+ * Eout when non-NULL) device->host, all enqueued on `stream` (one
+ * cudaMemcpyAsync per array).  Host buffers should be pinned for the copies
+ * to be asynchronous; the caller synchronises the stream before reading O.
+ */
+g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K_h, const void *V_h,
+                            const void *Eproj_h, void *O_h, void *Eout_h, void *staging_d,
+                            size_t staging_bytes, g3s_stream_t stream);
+
+/* Release the plan's host struct (the caller still owns the workspace). NULL is a no-op. */
+void g3s_plan_destroy(g3s_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* G3S_H */

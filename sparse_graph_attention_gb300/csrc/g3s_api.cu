@@ -1,0 +1,458 @@
+// C ABI of libg3s: argument checks, workspace layout, plan lifetime and the
+// forward orchestration.  All compute runs in the kernels of g3s_core.cu,
+// g3s_planner.cu (and the tile kernel); this file only validates and launches.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+
+#include "g3s_internal.h"
+
+using namespace g3s;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+g3s_status fail(g3s_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+g3s_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(G3S_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CUDA_OR_FAIL(x, where)                                     \
+    do {                                                           \
+        cudaError_t e_ = (x);                                      \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where);        \
+    } while (0)
+
+constexpr size_t kAlign = 256;
+
+int dtype_size(int dt) { return dt == G3S_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Carver {
+    char* base;
+    size_t off = 0;
+    template <class T>
+    T* take(long long count) {
+        off = (off + kAlign - 1) & ~(kAlign - 1);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += (size_t)(count > 0 ? count : 0) * sizeof(T);
+        return p;
+    }
+};
+
+void default_options(g3s_plan_options* o) {
+    memset(o, 0, sizeof *o);
+    o->bucket_bounds[0] = 32;
+    o->bucket_bounds[1] = 256;
+    o->bucket_bounds[2] = 2048;
+    o->heavy_threshold = 512;
+    o->chunk_edges = 256;
+    o->bsb = -1;
+    o->tile_path = -1;
+    o->tile_density_milli = 150;
+    o->tile_max_tiles = 32;
+    o->bsb_smem_edges = 2048;
+    o->rtm_elementwise_clamp = 1;
+    o->rtm_epsilon = 1e-6f;
+    o->validate_graph = 1;
+    o->out_dtype = G3S_F32;
+}
+
+// The tensor-core tile path is not part of this build yet.
+bool tile_path_compiled(int /*dtype*/, int /*variant*/, int /*head_dim*/) { return false; }
+
+g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype, int variant,
+                       const g3s_plan_options& o, PlanShape* s) {
+    if (N < 0 || E < 0) return fail(G3S_ERR_INVALID_ARG, "negative size (N=%lld, E=%lld)", (long long)N, (long long)E);
+    if (N > 0x7fffffffLL - 64) return fail(G3S_ERR_INVALID_ARG, "N=%lld does not fit int32 indices", (long long)N);
+    if (E > 0x7fffffffLL) return fail(G3S_ERR_INVALID_ARG, "E=%lld does not fit int32 CSR offsets", (long long)E);
+    if (dtype < G3S_F32 || dtype > G3S_BF16) return fail(G3S_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (variant != G3S_STANDARD && variant != G3S_RTMSCORE) return fail(G3S_ERR_INVALID_ARG, "unknown variant %d", variant);
+    if (heads < 1) return fail(G3S_ERR_INVALID_ARG, "heads must be >= 1 (got %d)", heads);
+    if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128)
+        return fail(G3S_ERR_UNSUPPORTED, "head_dim %d not in {16, 32, 64, 128}", head_dim);
+    const long long row_bytes = (long long)heads * head_dim * dtype_size(dtype);
+    const long long row_vecs = row_bytes / 16;
+    if (!core_supported(dtype, (int)(row_vecs > 4096 ? 4096 : row_vecs)))
+        return fail(G3S_ERR_UNSUPPORTED, "H*d*sizeof(dtype) = %lld bytes is not a power of two in [16, 4096]", row_bytes);
+    for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) {
+        if (o.bucket_bounds[k] < 1 || (k > 0 && o.bucket_bounds[k] <= o.bucket_bounds[k - 1]))
+            return fail(G3S_ERR_INVALID_ARG, "bucket_bounds must be positive and increasing");
+    }
+    if (o.heavy_threshold < 1) return fail(G3S_ERR_INVALID_ARG, "heavy_threshold must be >= 1");
+    if (o.chunk_edges < 1) return fail(G3S_ERR_INVALID_ARG, "chunk_edges must be >= 1");
+    if (o.bsb < -1 || o.bsb > 1 || o.tile_path < -1 || o.tile_path > 1)
+        return fail(G3S_ERR_INVALID_ARG, "bsb and tile_path take -1, 0 or 1");
+    if (o.tile_density_milli < 0 || o.tile_max_tiles < 1)
+        return fail(G3S_ERR_INVALID_ARG, "tile_density_milli >= 0 and tile_max_tiles >= 1 required");
+    if (o.bsb_smem_edges < 1 || o.bsb_smem_edges > 16384)
+        return fail(G3S_ERR_INVALID_ARG, "bsb_smem_edges must be in [1, 16384]");
+    if (!(o.rtm_epsilon >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "rtm_epsilon must be >= 0");
+    if (o.out_dtype != G3S_F32 && o.out_dtype != dtype)
+        return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
+
+    const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
+    if (o.tile_path == 1 && !tile_ok)
+        return fail(G3S_ERR_UNSUPPORTED, "tile path requested but not available for this dtype/variant/head_dim");
+    s->N = N;
+    s->E = E;
+    s->H = heads;
+    s->D = head_dim;
+    s->heavy_threshold = o.heavy_threshold;
+    s->chunk_edges = o.chunk_edges;
+    for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
+    s->bsb_smem_edges = o.bsb_smem_edges;
+    s->tile_density_milli = o.tile_density_milli;
+    s->tile_max_tiles = o.tile_max_tiles;
+    s->tile_enabled = tile_ok && o.tile_path != 0;
+    s->build_bsb = o.bsb == 1 || (o.bsb == -1 && s->tile_enabled);
+    if (s->tile_enabled && !s->build_bsb)
+        return fail(G3S_ERR_INVALID_ARG, "the tile path needs the BSB tiles (bsb = 0 with tile_path on)");
+    const long long T = o.heavy_threshold;
+    s->max_heavy = N < E / (T + 1) ? N : E / (T + 1);
+    s->max_chunks = E / o.chunk_edges + s->max_heavy;
+    s->W = (N + kWinRows - 1) / kWinRows;
+    s->max_tiles = s->build_bsb ? (E + 7 * s->W) / kTileCols : 0;
+    s->bitmap_words = s->build_bsb ? (N + 31) / 32 : 0;
+    const long long scan_n = N > s->W ? N : s->W;
+    s->scan_blocks = (scan_n + 1023) / 1024 + 2;
+    return G3S_OK;
+}
+
+size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
+    Carver c{static_cast<char*>(base)};
+    a->counts = c.take<PlanCounts>(1);
+    a->bucket_of = c.take<uint8_t>(s.N);
+    a->bucket_ptr = c.take<int32_t>(G3S_NUM_BUCKETS + 1);
+    a->bucket_rows = c.take<int32_t>(s.N);
+    a->heavy_rows = c.take<int32_t>(s.max_heavy);
+    a->heavy_chunk_ptr = c.take<int32_t>(s.max_heavy + 1);
+    a->heavy_index = c.take<int32_t>(s.N);
+    a->chunks = c.take<int32_t>(3 * s.max_chunks);
+    a->part_acc = c.take<float>(s.max_chunks * s.H * s.D);
+    a->part_ml = c.take<float>(s.max_chunks * s.H * 2);
+    a->scan_blocks = c.take<int32_t>(s.scan_blocks);
+    if (s.build_bsb) {
+        a->win_tile_ptr = c.take<int32_t>(s.W + 1);
+        a->win_ucount = c.take<int32_t>(s.W);
+        a->win_nnz = c.take<int32_t>(s.W);
+        a->win_flags = c.take<uint8_t>(s.W);
+        a->tile_windows = c.take<int32_t>(s.W);
+        a->large_windows = c.take<int32_t>(s.W);
+        a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
+        a->tile_bits = c.take<uint32_t>(s.max_tiles * 4);
+        a->bitmap_scratch = c.take<uint32_t>((long long)kLargeCtas * 3 * s.bitmap_words);
+    } else {
+        a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
+        a->win_flags = nullptr;
+        a->tile_bits = a->bitmap_scratch = nullptr;
+    }
+    return (c.off + kAlign - 1) & ~(kAlign - 1);
+}
+
+}  // namespace
+
+struct g3s_plan {
+    PlanShape shape;
+    PlanArrays arr;
+    PlanCounts counts;  // host copy
+    g3s_plan_options opts;
+    int dtype, variant, device;
+    const int32_t* row_ptr;
+    const int32_t* col_idx;
+    size_t ws_used;
+};
+
+extern "C" {
+
+const char* g3s_version(void) { return "g3s 0.1 (sm_103a)"; }
+
+const char* g3s_status_string(g3s_status s) {
+    switch (s) {
+        case G3S_OK: return "G3S_OK";
+        case G3S_ERR_INVALID_ARG: return "G3S_ERR_INVALID_ARG";
+        case G3S_ERR_UNSUPPORTED: return "G3S_ERR_UNSUPPORTED";
+        case G3S_ERR_BAD_GRAPH: return "G3S_ERR_BAD_GRAPH";
+        case G3S_ERR_WORKSPACE: return "G3S_ERR_WORKSPACE";
+        case G3S_ERR_CUDA: return "G3S_ERR_CUDA";
+        case G3S_ERR_TIMEOUT: return "G3S_ERR_TIMEOUT";
+    }
+    return "G3S_ERR_UNKNOWN";
+}
+
+const char* g3s_last_error(void) { return t_last_error.c_str(); }
+
+void g3s_plan_options_init(g3s_plan_options* opts) {
+    if (opts) default_options(opts);
+}
+
+g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int heads, int head_dim, g3s_dtype dtype,
+                                   g3s_variant variant, const g3s_plan_options* opts, size_t* bytes) {
+    if (!bytes) return fail(G3S_ERR_INVALID_ARG, "bytes is NULL");
+    g3s_plan_options o;
+    if (opts)
+        o = *opts;
+    else
+        default_options(&o);
+    PlanShape s;
+    g3s_status st = check_shape(num_nodes, num_edges, heads, head_dim, dtype, variant, o, &s);
+    if (st != G3S_OK) return st;
+    PlanArrays a;
+    *bytes = carve(s, &a, nullptr);
+    return G3S_OK;
+}
+
+g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, int64_t num_nodes, int64_t num_edges,
+                           int heads, int head_dim, g3s_dtype dtype, g3s_variant variant,
+                           const g3s_plan_options* opts, void* workspace_d, size_t workspace_bytes,
+                           g3s_stream_t stream_, g3s_plan** out) {
+    if (!out) return fail(G3S_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    g3s_plan_options o;
+    if (opts)
+        o = *opts;
+    else
+        default_options(&o);
+    PlanShape s;
+    g3s_status st = check_shape(num_nodes, num_edges, heads, head_dim, dtype, variant, o, &s);
+    if (st != G3S_OK) return st;
+    if (!row_ptr_d) return fail(G3S_ERR_INVALID_ARG, "row_ptr is NULL");
+    if (num_edges > 0 && !col_idx_d) return fail(G3S_ERR_INVALID_ARG, "col_idx is NULL with E > 0");
+    if ((reinterpret_cast<uintptr_t>(row_ptr_d) & 3u) || (reinterpret_cast<uintptr_t>(col_idx_d) & 3u))
+        return fail(G3S_ERR_INVALID_ARG, "row_ptr / col_idx must be 4-byte aligned");
+    PlanArrays a;
+    const size_t need = carve(s, &a, nullptr);
+    if (!workspace_d) return fail(G3S_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if (reinterpret_cast<uintptr_t>(workspace_d) % kAlign)
+        return fail(G3S_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+    if (workspace_bytes < need)
+        return fail(G3S_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+    carve(s, &a, workspace_d);
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    CUDA_OR_FAIL(cudaGetDevice(&dev), "cudaGetDevice");
+    PlanCounts hc;
+    CUDA_OR_FAIL(cudaMemsetAsync(a.counts, 0, sizeof(PlanCounts), stream), "cudaMemsetAsync(counts)");
+    if (s.build_bsb && s.bitmap_words > 0)
+        CUDA_OR_FAIL(cudaMemsetAsync(a.bitmap_scratch, 0, (size_t)kLargeCtas * 3 * s.bitmap_words * sizeof(uint32_t), stream),
+                     "cudaMemsetAsync(bitmaps)");
+    if (o.validate_graph) {
+        CUDA_OR_FAIL(plan_validate(row_ptr_d, col_idx_d, s, a, stream), "CSR validation launch");
+        CUDA_OR_FAIL(cudaMemcpyAsync(&hc, a.counts, sizeof hc, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync(counts)");
+        CUDA_OR_FAIL(cudaStreamSynchronize(stream), "cudaStreamSynchronize(validation)");
+        if (hc.status) {
+            return fail(G3S_ERR_BAD_GRAPH, "CSR validation failed:%s%s%s%s",
+                        (hc.status & kErrRowPtr0) ? " row_ptr[0] != 0;" : "",
+                        (hc.status & kErrRowPtrOrder) ? " row_ptr decreases;" : "",
+                        (hc.status & kErrRowPtrEnd) ? " row_ptr[N] != E;" : "",
+                        (hc.status & kErrColRange) ? " a source index is outside [0, N);" : "");
+        }
+    }
+    CUDA_OR_FAIL(plan_build(row_ptr_d, col_idx_d, s, a, stream), "planner launch");
+    CUDA_OR_FAIL(cudaMemcpyAsync(&hc, a.counts, sizeof hc, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync(counts)");
+    CUDA_OR_FAIL(cudaStreamSynchronize(stream), "cudaStreamSynchronize(planner)");
+
+    g3s_plan* p = new (std::nothrow) g3s_plan;
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "out of host memory for the plan struct");
+    p->shape = s;
+    p->arr = a;
+    p->counts = hc;
+    p->opts = o;
+    p->dtype = dtype;
+    p->variant = variant;
+    p->device = dev;
+    p->row_ptr = row_ptr_d;
+    p->col_idx = col_idx_d;
+    p->ws_used = need;
+    *out = p;
+    return G3S_OK;
+}
+
+g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
+    if (!p || !st) return fail(G3S_ERR_INVALID_ARG, "NULL plan or stats");
+    memset(st, 0, sizeof *st);
+    st->num_nodes = p->shape.N;
+    st->num_edges = p->shape.E;
+    st->heads = p->shape.H;
+    st->head_dim = p->shape.D;
+    st->dtype = p->dtype;
+    st->variant = p->variant;
+    st->out_dtype = p->opts.out_dtype;
+    for (int b = 0; b < G3S_NUM_BUCKETS; ++b) st->bucket_count[b] = p->counts.bucket_count[b];
+    st->heavy_rows = p->counts.n_heavy;
+    st->chunks = p->counts.n_chunks;
+    st->has_bsb = p->shape.build_bsb ? 1 : 0;
+    st->tile_path = p->shape.tile_enabled ? 1 : 0;
+    st->windows = p->shape.build_bsb ? p->shape.W : 0;
+    st->tiles = p->counts.n_tiles;
+    st->tile_windows = p->counts.n_tile_windows;
+    st->dup_windows = p->counts.n_dup_windows;
+    st->large_windows = p->counts.n_large_windows;
+    st->tile_window_nnz = p->counts.tile_window_nnz;
+    st->workspace_used = p->ws_used;
+    return G3S_OK;
+}
+
+g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_dst, size_t bytes, size_t* bytes_needed) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    const void* src = nullptr;
+    size_t n = 0;
+    const PlanShape& s = p->shape;
+    const PlanCounts& c = p->counts;
+    const bool bsb_arr = which >= G3S_ARR_WIN_TILE_PTR;
+    if (bsb_arr && !s.build_bsb) return fail(G3S_ERR_UNSUPPORTED, "plan was built without BSB tiles");
+    switch (which) {
+        case G3S_ARR_BUCKET_PTR: src = p->arr.bucket_ptr; n = 4 * (G3S_NUM_BUCKETS + 1); break;
+        case G3S_ARR_BUCKET_ROWS: src = p->arr.bucket_rows; n = 4 * (size_t)s.N; break;
+        case G3S_ARR_HEAVY_ROWS: src = p->arr.heavy_rows; n = 4 * (size_t)c.n_heavy; break;
+        case G3S_ARR_HEAVY_CHUNK_PTR: src = p->arr.heavy_chunk_ptr; n = 4 * ((size_t)c.n_heavy + 1); break;
+        case G3S_ARR_CHUNKS: src = p->arr.chunks; n = 12 * (size_t)c.n_chunks; break;
+        case G3S_ARR_WIN_TILE_PTR: src = p->arr.win_tile_ptr; n = 4 * ((size_t)s.W + 1); break;
+        case G3S_ARR_TILE_COLS: src = p->arr.tile_cols; n = 4 * kTileCols * (size_t)c.n_tiles; break;
+        case G3S_ARR_TILE_BITS: src = p->arr.tile_bits; n = 16 * (size_t)c.n_tiles; break;
+        case G3S_ARR_WIN_NNZ: src = p->arr.win_nnz; n = 4 * (size_t)s.W; break;
+        case G3S_ARR_WIN_FLAGS: src = p->arr.win_flags; n = (size_t)s.W; break;
+        case G3S_ARR_TILE_WINDOWS: src = p->arr.tile_windows; n = 4 * (size_t)c.n_tile_windows; break;
+        default: return fail(G3S_ERR_INVALID_ARG, "unknown plan array %d", (int)which);
+    }
+    if (bytes_needed) *bytes_needed = n;
+    if (!host_dst) return G3S_OK;
+    if (bytes < n) return fail(G3S_ERR_INVALID_ARG, "destination has %zu bytes, %zu needed", bytes, n);
+    if (n == 0) return G3S_OK;
+    CUDA_OR_FAIL(cudaDeviceSynchronize(), "cudaDeviceSynchronize(export)");
+    CUDA_OR_FAIL(cudaMemcpy(host_dst, src, n, cudaMemcpyDeviceToHost), "cudaMemcpy(export)");
+    return G3S_OK;
+}
+
+g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const void* V, const void* Eproj, void* O,
+                       void* Eout, g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    const PlanShape& s = p->shape;
+    const bool rtm = p->variant == G3S_RTMSCORE;
+    if (s.N > 0 && (!Q || !K || !V || !O)) return fail(G3S_ERR_INVALID_ARG, "Q, K, V and O must be non-NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(Eproj) || !aligned16(Eout))
+        return fail(G3S_ERR_INVALID_ARG, "value pointers must be 16-byte aligned");
+    if (rtm) {
+        if (s.E > 0 && !Eproj) return fail(G3S_ERR_INVALID_ARG, "RTMScore plan needs Eproj");
+    } else if (Eproj || Eout) {
+        return fail(G3S_ERR_INVALID_ARG, "Eproj / Eout are only valid for an RTMScore plan");
+    }
+    int dev = -1;
+    CUDA_OR_FAIL(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != p->device) return fail(G3S_ERR_INVALID_ARG, "plan was built on device %d, current is %d", p->device, dev);
+    if (s.N == 0) return G3S_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    const int esz = dtype_size(p->dtype);
+    CoreParams cp;
+    cp.row_ptr = p->row_ptr;
+    cp.col_idx = p->col_idx;
+    cp.Q = Q;
+    cp.K = K;
+    cp.V = V;
+    cp.E = Eproj;
+    cp.O = O;
+    cp.Eout = rtm ? Eout : nullptr;
+    cp.chunks = p->arr.chunks;
+    cp.part_acc = p->arr.part_acc;
+    cp.part_ml = p->arr.part_ml;
+    cp.win_flags = p->counts.n_tile_windows > 0 ? p->arr.win_flags : nullptr;
+    cp.N = s.N;
+    cp.n_chunks = p->counts.n_chunks;
+    cp.H = s.H;
+    cp.D = s.D;
+    cp.heavy_threshold = s.heavy_threshold;
+    cp.row_vecs = s.H * s.D * esz / 16;
+    cp.lph = s.D * esz / 16;
+    const float inv_sqrt_d = 1.0f / sqrtf((float)s.D);
+    cp.qscale = rtm ? inv_sqrt_d : inv_sqrt_d * 1.4426950408889634f;
+    cp.eps = p->opts.rtm_epsilon;
+    cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
+    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream), "fused kernel launch");
+    if (p->counts.n_chunks > 0) {
+        MergeParams mp;
+        mp.heavy_rows = p->arr.heavy_rows;
+        mp.heavy_chunk_ptr = p->arr.heavy_chunk_ptr;
+        mp.part_acc = p->arr.part_acc;
+        mp.part_ml = p->arr.part_ml;
+        mp.O = O;
+        mp.n_heavy = p->counts.n_heavy;
+        mp.H = s.H;
+        mp.D = s.D;
+        mp.eps = p->opts.rtm_epsilon;
+        CUDA_OR_FAIL(merge_launch(p->opts.out_dtype, rtm, mp, stream), "merge kernel launch");
+    }
+    return G3S_OK;
+}
+
+g3s_status g3s_host_staging_size(const g3s_plan* p, size_t* bytes) {
+    if (!p || !bytes) return fail(G3S_ERR_INVALID_ARG, "NULL plan or bytes");
+    const size_t hd = (size_t)p->shape.H * p->shape.D;
+    const size_t node = (size_t)p->shape.N * hd * dtype_size(p->dtype);
+    const size_t node_out = (size_t)p->shape.N * hd * dtype_size(p->opts.out_dtype);
+    const size_t edge = (size_t)p->shape.E * hd * dtype_size(p->dtype);
+    const size_t edge_out = (size_t)p->shape.E * hd * dtype_size(p->opts.out_dtype);
+    auto up = [](size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); };
+    size_t n = 3 * up(node) + up(node_out);
+    if (p->variant == G3S_RTMSCORE) n += up(edge) + up(edge_out);
+    *bytes = n;
+    return G3S_OK;
+}
+
+g3s_status g3s_forward_host(const g3s_plan* p, const void* Qh, const void* Kh, const void* Vh, const void* Eh, void* Oh,
+                            void* Eouth, void* staging, size_t staging_bytes, g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    size_t need = 0;
+    g3s_host_staging_size(p, &need);
+    if (!staging || staging_bytes < need || reinterpret_cast<uintptr_t>(staging) % kAlign)
+        return fail(G3S_ERR_WORKSPACE, "staging needs %zu bytes, %zu-byte aligned", need, kAlign);
+    const bool rtm = p->variant == G3S_RTMSCORE;
+    const size_t hd = (size_t)p->shape.H * p->shape.D;
+    const size_t node = (size_t)p->shape.N * hd * dtype_size(p->dtype);
+    const size_t node_out = (size_t)p->shape.N * hd * dtype_size(p->opts.out_dtype);
+    const size_t edge = (size_t)p->shape.E * hd * dtype_size(p->dtype);
+    const size_t edge_out = (size_t)p->shape.E * hd * dtype_size(p->opts.out_dtype);
+    if (p->shape.N > 0 && (!Qh || !Kh || !Vh || !Oh)) return fail(G3S_ERR_INVALID_ARG, "host Q, K, V, O must be non-NULL");
+    if (rtm && p->shape.E > 0 && !Eh) return fail(G3S_ERR_INVALID_ARG, "RTMScore plan needs host Eproj");
+    if (!rtm && (Eh || Eouth)) return fail(G3S_ERR_INVALID_ARG, "Eproj / Eout are only valid for an RTMScore plan");
+    auto up = [](size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); };
+    char* b = static_cast<char*>(staging);
+    void* dQ = b;
+    void* dK = b + up(node);
+    void* dV = b + 2 * up(node);
+    void* dO = b + 3 * up(node);
+    void* dE = rtm ? b + 3 * up(node) + up(node_out) : nullptr;
+    void* dEo = rtm ? b + 3 * up(node) + up(node_out) + up(edge) : nullptr;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (node) {
+        CUDA_OR_FAIL(cudaMemcpyAsync(dQ, Qh, node, cudaMemcpyHostToDevice, stream), "H2D Q");
+        CUDA_OR_FAIL(cudaMemcpyAsync(dK, Kh, node, cudaMemcpyHostToDevice, stream), "H2D K");
+        CUDA_OR_FAIL(cudaMemcpyAsync(dV, Vh, node, cudaMemcpyHostToDevice, stream), "H2D V");
+    }
+    if (rtm && edge) CUDA_OR_FAIL(cudaMemcpyAsync(dE, Eh, edge, cudaMemcpyHostToDevice, stream), "H2D Eproj");
+    g3s_status st = g3s_forward(p, dQ, dK, dV, rtm ? dE : nullptr, dO, (rtm && Eouth) ? dEo : nullptr, stream_);
+    if (st != G3S_OK) return st;
+    if (node_out) CUDA_OR_FAIL(cudaMemcpyAsync(Oh, dO, node_out, cudaMemcpyDeviceToHost, stream), "D2H O");
+    if (rtm && Eouth && edge_out)
+        CUDA_OR_FAIL(cudaMemcpyAsync(Eouth, dEo, edge_out, cudaMemcpyDeviceToHost, stream), "D2H Eout");
+    return G3S_OK;
+}
+
+void g3s_plan_destroy(g3s_plan* p) { delete p; }
+
+}  // extern "C"

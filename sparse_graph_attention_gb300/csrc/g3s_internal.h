@@ -1,0 +1,133 @@
+// Internal declarations shared by the libg3s translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/g3s.h"
+
+namespace g3s {
+
+constexpr int kWinRows = 16;   // rows per BSB row window
+constexpr int kTileCols = 8;   // columns per BSB tile (16x8 tiles)
+constexpr int kFlagDup = 1;    // window holds a repeated (row, source) pair
+constexpr int kFlagTile = 2;   // window takes the tensor-core tile path
+constexpr int kWarpsPerCta = 8;
+
+// Error bits written by the CSR validation kernel.
+enum : int32_t {
+    kErrRowPtr0 = 1,      // row_ptr[0] != 0
+    kErrRowPtrOrder = 2,  // row_ptr decreasing somewhere
+    kErrRowPtrEnd = 4,    // row_ptr[N] != E
+    kErrColRange = 8,     // a source outside [0, N)
+};
+
+// Small device-resident counters filled by the planner and read back once.
+struct PlanCounts {
+    int32_t status;
+    int32_t bucket_count[G3S_NUM_BUCKETS];
+    int32_t n_heavy;
+    int32_t n_chunks;
+    int32_t n_tiles;
+    int32_t n_tile_windows;
+    int32_t n_dup_windows;
+    int32_t n_large_windows;
+    int32_t pad0;
+    long long tile_window_nnz;
+};
+
+// Device views the planner writes into (all inside the caller's workspace).
+struct PlanArrays {
+    uint8_t* bucket_of;        // [N]
+    int32_t* bucket_ptr;       // [NB+1]
+    int32_t* bucket_rows;      // [N]
+    int32_t* heavy_rows;       // [max_heavy]
+    int32_t* heavy_chunk_ptr;  // [max_heavy+1]
+    int32_t* heavy_index;      // [N] scratch: heavy ordinal of a heavy row
+    int32_t* chunks;           // [max_chunks][3]
+    float* part_acc;           // [max_chunks][H*d]
+    float* part_ml;            // [max_chunks][H][2]
+    // BSB
+    int32_t* win_tile_ptr;     // [W+1]
+    int32_t* win_ucount;       // [W] unique sources per window (scratch)
+    int32_t* win_nnz;          // [W]
+    uint8_t* win_flags;        // [W]
+    int32_t* tile_windows;     // [W]
+    int32_t* large_windows;    // [W]
+    int32_t* tile_cols;        // [max_tiles][8]
+    uint32_t* tile_bits;       // [max_tiles][4]
+    uint32_t* bitmap_scratch;  // [kLargeCtas][3][words]
+    // scan scratch
+    int32_t* scan_blocks;      // [scan_block_capacity]
+    PlanCounts* counts;
+};
+
+constexpr int kLargeCtas = 32;  // CTAs of the global-bitmap window compaction
+
+struct PlanShape {
+    int64_t N, E;
+    int H, D;
+    int heavy_threshold, chunk_edges;
+    int bounds[G3S_NUM_BUCKETS - 2];
+    int bsb_smem_edges;
+    int tile_density_milli, tile_max_tiles;
+    bool build_bsb, tile_enabled;
+    int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
+    int64_t scan_blocks;
+};
+
+// ---- planner (g3s_planner.cu) --------------------------------------------
+cudaError_t plan_validate(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s,
+                          const PlanArrays& a, cudaStream_t st);
+cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s,
+                       const PlanArrays& a, cudaStream_t st);
+
+// ---- CUDA-core fused kernel (g3s_core.cu) ---------------------------------
+struct CoreParams {
+    const int32_t* row_ptr;
+    const int32_t* col_idx;
+    const void* Q;
+    const void* K;
+    const void* V;
+    const void* E;
+    void* O;
+    void* Eout;
+    const int32_t* chunks;
+    float* part_acc;
+    float* part_ml;
+    const uint8_t* win_flags;  // nullptr when no window takes the tile path
+    long long N;
+    long long n_chunks;
+    int H, D;
+    int heavy_threshold;
+    int row_vecs;  // H*D*sizeof(T)/16
+    int lph;       // 16-byte vectors per head = D*sizeof(T)/16
+    float qscale;  // standard: log2(e)/sqrt(d); RTMScore: 1/sqrt(d)
+    float eps;
+    int elementwise_clamp;
+};
+
+struct MergeParams {
+    const int32_t* heavy_rows;
+    const int32_t* heavy_chunk_ptr;
+    const float* part_acc;
+    const float* part_ml;
+    void* O;
+    int n_heavy;
+    int H, D;
+    float eps;
+};
+
+// dtype / out_dtype: 0 f32, 1 f16, 2 bf16; out_dtype is f32 or the input dtype.
+// Launchers return cudaErrorInvalidValue for shapes without a kernel.
+bool core_supported(int dtype, int row_vecs);
+cudaError_t core_launch(int dtype, int out_dtype, bool rtm, const CoreParams& p, cudaStream_t st);
+cudaError_t merge_launch(int out_dtype, bool rtm, const MergeParams& p, cudaStream_t st);
+cudaError_t core_launch_f32(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_f16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_bf16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
+cudaError_t merge_launch_f32(bool rtm, const MergeParams& p, cudaStream_t st);
+cudaError_t merge_launch_f16(bool rtm, const MergeParams& p, cudaStream_t st);
+cudaError_t merge_launch_bf16(bool rtm, const MergeParams& p, cudaStream_t st);
+
+}  // namespace g3s
