@@ -227,6 +227,45 @@ g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K
 /* Release the plan's host struct (the caller still owns the workspace). NULL is a no-op. */
 void g3s_plan_destroy(g3s_plan *plan);
 
+/*
+ * Bytes of device scratch built into the library for g3s_forward_noalloc.
+ */
+#define G3S_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * g3s_forward_noalloc -- plan and forward in one call, with no allocation.
+ *
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory: an inference engine that hands out device
+ * memory only when it is built, a process whose GPU memory is already held
+ * by another framework's caching allocator, or a service under a fixed
+ * memory budget.  Such callers cannot provide the workspace g3s_plan_create
+ * needs, and a cudaMalloc may also synchronise the device at a bad time.
+ *
+ * Same arguments and result as g3s_plan_create (default options, no BSB
+ * tiles) followed by g3s_forward: O (and Eout) come out in fp32, the
+ * caller passes the CSR, inputs and outputs only.  The planner arrays and
+ * heavy-row partial results live in a static device array of
+ * G3S_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading this library
+ * holds until the process exits.  A graph whose plan needs more -- the size
+ * g3s_plan_workspace_size reports with bsb = 0, about 9 bytes per node plus
+ * 6*(H*d + 2*H + 3) bytes per 256 edges -- is rejected with
+ * G3S_ERR_WORKSPACE before any device work.
+ *
+ * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call
+ * on a device looks up the scratch's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Every call on a device shares the one scratch array and leaves its
+ * contents behind (the counters it needs are cleared at the start of each
+ * call), so calls that overlap on the GPU, from any stream or thread, race:
+ * serialise them.  Synchronises `stream` twice (validation and planner
+ * sizes) before enqueueing the forward kernels, which run asynchronously.
+ */
+g3s_status g3s_forward_noalloc(const int32_t *row_ptr_d, const int32_t *col_idx_d, int64_t num_nodes,
+                               int64_t num_edges, int heads, int head_dim, g3s_dtype dtype,
+                               g3s_variant variant, const void *Q, const void *K, const void *V,
+                               const void *Eproj, void *O, void *Eout, g3s_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -86,7 +86,9 @@ _lib = None
 
 EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_options_init",
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
-            "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy"]
+            "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
+            "g3s_forward_noalloc"]
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def load_library(path: str = LIB_PATH):
@@ -117,6 +119,8 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_forward_host.argtypes = [P, P, P, P, P, P, P, P, SZ, P]
         lib.g3s_plan_destroy.argtypes = [P]
         lib.g3s_plan_destroy.restype = None
+        lib.g3s_forward_noalloc.argtypes = [P, P, I64, I64, I, I, I, I, P, P, P, P, P, P, P]
+        lib.g3s_forward_noalloc.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -343,5 +347,30 @@ class Plan:
         return staging
 
 
-__all__ = ["Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
+def forward_noalloc(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant, Q, K, V, E=None, O=None,
+                    Eout=None, stream=None):
+    """``g3s_forward_noalloc``: plan + forward in one call using the library's
+    static device scratch (for callers that cannot allocate device memory).
+    Returns O (fp32), and Eout when given."""
+    torch = _torch()
+    lib = load_library()
+    dev = row_ptr.device
+    n, ne = int(num_nodes), int(col_idx.numel())
+    tdt = torch_dtype(dtype)
+    nn, nedge = n * heads * head_dim, ne * heads * head_dim
+    if O is None:
+        O = torch.empty((n, heads, head_dim), dtype=torch.float32, device=dev)
+    args = [_dev_ptr(row_ptr, "row_ptr", torch.int32, n + 1, dev),
+            _dev_ptr(col_idx, "col_idx", torch.int32, device=dev) if ne else None]
+    vals = [_dev_ptr(Q, "Q", tdt, nn, dev), _dev_ptr(K, "K", tdt, nn, dev), _dev_ptr(V, "V", tdt, nn, dev),
+            _dev_ptr(E, "E", tdt, nedge, dev) if E is not None else None,
+            _dev_ptr(O, "O", torch.float32, nn, dev),
+            _dev_ptr(Eout, "Eout", torch.float32, nedge, dev) if Eout is not None else None]
+    with torch.cuda.device(dev):
+        _check(lib.g3s_forward_noalloc(args[0], args[1], n, ne, int(heads), int(head_dim), DTYPES[dtype],
+                                       VARIANTS[variant], *vals, _stream_handle(stream)))
+    return (O, Eout) if Eout is not None else O
+
+
+__all__ = ["forward_noalloc","Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
            "DTYPES", "VARIANTS", "ARRAYS", "EXPORTED", "LIB_PATH"]

@@ -13,8 +13,11 @@
 using namespace g3s;
 
 namespace {
-
 thread_local std::string t_last_error;
+}  // namespace
+
+namespace g3s {
+namespace api {
 
 g3s_status fail(g3s_status st, const char* fmt, ...) {
     char buf[512];
@@ -35,8 +38,6 @@ g3s_status cuda_fail(cudaError_t e, const char* where) {
         cudaError_t e_ = (x);                                      \
         if (e_ != cudaSuccess) return cuda_fail(e_, where);        \
     } while (0)
-
-constexpr size_t kAlign = 256;
 
 int dtype_size(int dt) { return dt == G3S_F32 ? 4 : 2; }
 
@@ -164,7 +165,10 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     return (c.off + kAlign - 1) & ~(kAlign - 1);
 }
 
-}  // namespace
+}  // namespace api
+}  // namespace g3s
+
+using namespace g3s::api;
 
 struct g3s_plan {
     PlanShape shape;

@@ -130,4 +130,17 @@ cudaError_t merge_launch_f32(bool rtm, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool rtm, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool rtm, const MergeParams& p, cudaStream_t st);
 
+// ---- host helpers shared by the ABI translation units (g3s_api.cu) ---------
+namespace api {
+constexpr size_t kAlign = 256;
+g3s_status fail(g3s_status st, const char* fmt, ...);
+g3s_status cuda_fail(cudaError_t e, const char* where);
+int dtype_size(int dt);
+bool aligned16(const void* p);
+void default_options(g3s_plan_options* o);
+g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype, int variant,
+                       const g3s_plan_options& o, PlanShape* s);
+size_t carve(const PlanShape& s, PlanArrays* a, void* base);
+}  // namespace api
+
 }  // namespace g3s

@@ -119,3 +119,16 @@ def test_calls_without_plan_fail_cleanly(lib):
                                ctypes.byref(out)) == 4
     assert lib.g3s_plan_create(None, P(16), 10, 20, 1, 16, 0, 0, ctypes.byref(o), P(4096), 1 << 30, None,
                                ctypes.byref(out)) == 1
+
+
+def test_noalloc_rejects_graphs_beyond_its_scratch(lib):
+    """The static-scratch entry point refuses, before touching the GPU, a graph
+    whose plan would not fit in its built-in scratch."""
+    P = ctypes.c_void_p
+    n, e = 2_000_000, 100_000_000
+    assert g3s.workspace_size(n, e, 4, 32, "bf16", bsb=0) > g3s.NOALLOC_SCRATCH_BYTES
+    st = lib.g3s_forward_noalloc(P(256), P(256), n, e, 4, 32, 2, 0, P(256), P(256), P(256), None, P(256), None,
+                                 None)
+    assert st == 4
+    assert b"static scratch" in lib.g3s_last_error()
+    assert g3s.workspace_size(200_000, 2_850_000, 1, 64, "f16", bsb=0) <= g3s.NOALLOC_SCRATCH_BYTES
