@@ -137,6 +137,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
 size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     Carver c{static_cast<char*>(base)};
     a->counts = c.take<PlanCounts>(1);
+    a->work_counter = c.take<unsigned long long>(1);
     a->bucket_of = c.take<uint8_t>(s.N);
     a->bucket_ptr = c.take<int32_t>(G3S_NUM_BUCKETS + 1);
     a->bucket_rows = c.take<int32_t>(s.N);
@@ -376,6 +377,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.part_acc = p->arr.part_acc;
     cp.part_ml = p->arr.part_ml;
     cp.win_flags = p->counts.n_tile_windows > 0 ? p->arr.win_flags : nullptr;
+    cp.work_counter = p->arr.work_counter;
     cp.N = s.N;
     cp.n_chunks = p->counts.n_chunks;
     cp.H = s.H;

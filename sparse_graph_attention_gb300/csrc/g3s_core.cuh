@@ -1,8 +1,8 @@
 // CUDA-core fused 3S kernel: SDDMM -> softmax -> SpMM in one pass per
 // destination row, plus the merge of heavy-row partial results.
 //
-// Mapping.  One warp owns one work item: a whole destination row, or one
-// chunk of a heavy row.  A node's features for all heads, H*d values, are
+// Mapping.  A warp processes one work item at a time: a whole destination
+// row, or one chunk of a heavy row.  A node's features for all heads, H*d values, are
 // read as 16-byte vectors ("row_vecs" of them).  When a row is narrower than
 // 32 vectors the warp splits into G = 32/row_vecs lane groups and every group
 // gathers a different in-edge, so one warp load instruction covers G edges;
@@ -135,49 +135,53 @@ struct Store<__half, 8> {
     }
 };
 
+// 2^x with the hardware approximation (relative error about 2^-22; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Lazy rescale: the running max used as the exponent's reference only moves
+// up when a logit exceeds it by more than this (log2 units), so most batches
+// skip the rescale; weights stay below 2^kRescaleSlack.
+constexpr float kRescaleSlack = 8.0f;
+constexpr int kItemsPerGrab = 2;  // work items a warp takes per atomic grab
+
+// Per-lane constants of the lane mapping.
+struct Lanes {
+    int lane, rv, gsize, G, g, sub, lph;
+    __device__ Lanes(int lane_, int rv_, int lph_) : lane(lane_), rv(rv_), lph(lph_) {
+        gsize = rv < 32 ? rv : 32;
+        G = 32 / gsize;
+        g = lane / gsize;
+        sub = lane - g * gsize;
+    }
+};
+
 // ---------------------------------------------------------------------------
-// The fused kernel.  T: input element type; OutT: type of O and Eout (fp32
-// or T); NV: 16-byte vectors per lane per edge; RTM: edge-modulated variant.
+// One work item: destination `row`, CSR positions [e0, e1).  chunk >= 0 means
+// this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
+// otherwise normalise and write O.
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT, int NV, bool RTM>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParams p) {
+__device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
+                                             const int e1, const long long chunk) {
     using VT = Vec<T>;
-    constexpr int VE = VT::N;                   // elements per 16-byte vector
-    constexpr int U = NV >= 4 ? 1 : 4 / NV;     // edges per lane group per step
-    const int lane = threadIdx.x & 31;
-    const long long w = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-
-    int row;
-    long long e0, e1;
-    bool is_chunk;
-    if (w < p.n_chunks) {
-        const int32_t* c = p.chunks + 3 * w;
-        row = c[0];
-        e0 = c[1];
-        e1 = c[2];
-        is_chunk = true;
-    } else {
-        const long long r = w - p.n_chunks;
-        if (r >= p.N) return;
-        row = (int)r;
-        e0 = p.row_ptr[row];
-        e1 = p.row_ptr[row + 1];
-        if (e1 - e0 > p.heavy_threshold) return;  // done by chunks + merge
-        if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) return;  // tile path
-        is_chunk = false;
-    }
-
-    const int rv = p.row_vecs;
-    const int gsize = rv < 32 ? rv : 32;
-    const int G = 32 / gsize;
-    const int g = lane / gsize;
-    const int sub = lane - g * gsize;
-    const int lph = p.lph;
+    constexpr int VE = VT::N;                // elements per 16-byte vector
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;  // edges per lane group per step
+    const int rv = L.rv, g = L.g, sub = L.sub, lph = L.lph;
+    const int S = L.G * U;                   // edges per step (power of two, <= 64)
 
     const uint4* Q4 = static_cast<const uint4*>(p.Q);
-    const uint4* K4 = static_cast<const uint4*>(p.K);
-    const uint4* V4 = static_cast<const uint4*>(p.V);
-    const uint4* E4 = static_cast<const uint4*>(p.E);
+    const uint4* K4 = static_cast<const uint4*>(p.K) + sub;
+    const uint4* V4 = static_cast<const uint4*>(p.V) + sub;
+    const uint4* E4 = static_cast<const uint4*>(p.E) + sub;
+
+    // source indices of the first 64 edges, one per lane in two registers
+    int cbase = e0;
+    int idx_lo = (e0 + L.lane < e1) ? __ldg(p.col_idx + e0 + L.lane) : 0;
+    int idx_hi = (e0 + 32 + L.lane < e1) ? __ldg(p.col_idx + e0 + 32 + L.lane) : 0;
 
     float q[NV][VE];
 #pragma unroll
@@ -196,28 +200,50 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
         for (int k = 0; k < VE; ++k) acc[j][k] = 0.f;
     }
 
-    const long long step = (long long)G * U;
-    for (long long base = e0; base < e1; base += step) {
-        const long long eb = base + (long long)g * U;
+    for (int base = e0; base < e1; base += S) {
+        if (base - cbase >= 64) {  // warp-uniform: next 64 indices
+            cbase += 64;
+            idx_lo = (cbase + L.lane < e1) ? __ldg(p.col_idx + cbase + L.lane) : 0;
+            idx_hi = (cbase + 32 + L.lane < e1) ? __ldg(p.col_idx + cbase + 32 + L.lane) : 0;
+        }
+        const int off = base - cbase;   // 0, S, 2S, ... < 64
+        const int last = e1 - 1 - cbase;  // window position of the row's last edge
+        // Slots past the row's end re-read its last edge (a valid, cached
+        // address) and get weight 0, so the loads need no branch.
         int src[U];
+        bool ok[U];
+        if (S <= 32) {
+            const int v = (off & 32) ? idx_hi : idx_lo;  // warp-uniform choice
 #pragma unroll
-        for (int u = 0; u < U; ++u) src[u] = (eb + u < e1) ? __ldg(p.col_idx + eb + u) : -1;
+            for (int u = 0; u < U; ++u) {
+                const int pos = off + g * U + u;
+                ok[u] = pos <= last;
+                src[u] = __shfl_sync(kFull, v, (ok[u] ? pos : last) & 31);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                int pos = off + g * U + u;
+                ok[u] = pos <= last;
+                pos = ok[u] ? pos : last;
+                const int a = __shfl_sync(kFull, idx_lo, pos & 31);
+                const int b = __shfl_sync(kFull, idx_hi, pos & 31);
+                src[u] = pos < 32 ? a : b;
+            }
+        }
 
         uint4 kr[U][NV], vr[U][NV];
         uint4 er[RTM ? U : 1][RTM ? NV : 1];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const long long o = (long long)src[u] * rv;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                if (src[u] >= 0) {
-                    const long long o = (long long)src[u] * rv + sub + 32 * j;
-                    kr[u][j] = ldg16(K4 + o);
-                    vr[u][j] = ldg16(V4 + o);
-                    if constexpr (RTM) er[u][j] = ldg16(E4 + (eb + u) * rv + sub + 32 * j);
-                } else {
-                    kr[u][j] = make_uint4(0, 0, 0, 0);
-                    vr[u][j] = make_uint4(0, 0, 0, 0);
-                    if constexpr (RTM) er[u][j] = make_uint4(0, 0, 0, 0);
+                kr[u][j] = ldg16(K4 + o + 32 * j);
+                vr[u][j] = ldg16(V4 + o + 32 * j);
+                if constexpr (RTM) {
+                    const int e = ok[u] ? base + g * U + u : e1 - 1;
+                    er[u][j] = ldg16(E4 + (long long)e * rv + 32 * j);
                 }
             }
         }
@@ -240,13 +266,16 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
                         uo[k] = t * ef[k];
                         s += uo[k];
                     }
-                    if (p.Eout != nullptr && src[u] >= 0)
-                        Store<OutT, VE>::run(p.Eout, ((eb + u) * rv + sub + 32 * j) * VE, uo);
+                    if (p.Eout != nullptr && ok[u])
+                        Store<OutT, VE>::run(p.Eout, ((long long)(base + g * U + u) * rv + sub + 32 * j) * VE, uo);
                 } else {
+                    float2 s2 = make_float2(0.f, 0.f);  // packed fp32 FMA (two lanes of work per instruction)
 #pragma unroll
-                    for (int k = 0; k < VE; ++k) s = fmaf(q[j][k], kf[k], s);
+                    for (int k = 0; k < VE; k += 2)
+                        s2 = __ffma2_rn(make_float2(q[j][k], q[j][k + 1]), make_float2(kf[k], kf[k + 1]), s2);
+                    s = s2.x + s2.y;
                 }
-                for (int off = 1; off < lph; off <<= 1) s += __shfl_xor_sync(kFull, s, off);
+                for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
                 lg[u][j] = s;
             }
         }
@@ -256,7 +285,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
             if constexpr (RTM) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const float sc = src[u] >= 0 ? exp2f(clamp5(lg[u][j]) * kLog2e) : 0.f;
+                    const float sc = ok[u] ? ex2(clamp5(lg[u][j]) * kLog2e) : 0.f;
                     float vf[VE];
                     VT::to_float(vr[u][j], vf);
                     l[j] += sc;
@@ -267,27 +296,34 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
                 float mx = m[j];
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (src[u] >= 0) mx = fmaxf(mx, lg[u][j]);
-                const float corr = exp2f(m[j] - mx);
-                l[j] *= corr;
+                    if (ok[u]) mx = fmaxf(mx, lg[u][j]);
+                if (mx > m[j] + kRescaleSlack) {  // move the reference max
+                    const float corr = ex2(m[j] - mx);
+                    l[j] *= corr;
 #pragma unroll
-                for (int k = 0; k < VE; ++k) acc[j][k] *= corr;
-                m[j] = mx;
+                    for (int k = 0; k < VE; ++k) acc[j][k] *= corr;
+                    m[j] = mx;
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const float pw = src[u] >= 0 ? exp2f(lg[u][j] - mx) : 0.f;
+                    const float pw = ok[u] ? ex2(lg[u][j] - m[j]) : 0.f;
                     float vf[VE];
                     VT::to_float(vr[u][j], vf);
                     l[j] += pw;
+                    const float2 pw2 = make_float2(pw, pw);
 #pragma unroll
-                    for (int k = 0; k < VE; ++k) acc[j][k] = fmaf(pw, vf[k], acc[j][k]);
+                    for (int k = 0; k < VE; k += 2) {
+                        const float2 a2 = __ffma2_rn(pw2, make_float2(vf[k], vf[k + 1]), make_float2(acc[j][k], acc[j][k + 1]));
+                        acc[j][k] = a2.x;
+                        acc[j][k + 1] = a2.y;
+                    }
                 }
             }
         }
     }
 
     // merge the lane groups (fixed butterfly order)
-    for (int off = gsize; off < 32; off <<= 1) {
+    for (int off = L.gsize; off < 32; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             if constexpr (RTM) {
@@ -298,7 +334,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
                 const float mo = __shfl_xor_sync(kFull, m[j], off);
                 const float lo = __shfl_xor_sync(kFull, l[j], off);
                 const float mx = fmaxf(m[j], mo);
-                const float ca = exp2f(m[j] - mx), cb = exp2f(mo - mx);
+                const float ca = ex2(m[j] - mx), cb = ex2(mo - mx);
                 l[j] = l[j] * ca + lo * cb;
 #pragma unroll
                 for (int k = 0; k < VE; ++k) {
@@ -311,9 +347,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
     }
     if (g != 0) return;
 
-    if (is_chunk) {
+    if (chunk >= 0) {
         const long long HD = (long long)rv * VE;
-        float* pa = p.part_acc + w * HD;
+        float* pa = p.part_acc + chunk * HD;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int v = sub + 32 * j;
@@ -321,7 +357,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
 #pragma unroll
             for (int k = 0; k < VE; k += 4) dst[k / 4] = make_float4(acc[j][k], acc[j][k + 1], acc[j][k + 2], acc[j][k + 3]);
             if (v % lph == 0) {
-                float* ml = p.part_ml + (w * p.H + v / lph) * 2;
+                float* ml = p.part_ml + (chunk * p.H + v / lph) * 2;
                 ml[0] = m[j];
                 ml[1] = l[j];
             }
@@ -338,6 +374,43 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) core_kernel(const CoreParam
 #pragma unroll
             for (int k = 0; k < VE; ++k) o[k] = acc[j][k] * inv;
             Store<OutT, VE>::run(p.O, ((long long)row * rv + sub + 32 * j) * VE, o);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The fused kernel.  T: input element type; OutT: type of O and Eout (fp32
+// or T); NV: 16-byte vectors per lane per edge; RTM: edge-modulated variant.
+//
+// Persistent: the grid fills the GPU once and every warp takes work items
+// (heavy-row chunks first, then rows in ascending id) kItemsPerGrab at a
+// time from an atomic counter, so a warp that drew a short row is never idle
+// behind a long one, and the rows in flight stay a narrow band of ids (the
+// L2 keeps serving the sources near them).  Each item's result depends only
+// on its own data, so the dynamic order does not change any output.
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT, int NV, bool RTM>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? 4 : 1) core_kernel(const CoreParams p) {
+    const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
+    const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
+    const unsigned long long total = n_chunks + (unsigned long long)p.N;
+    for (;;) {
+        unsigned long long first = 0;
+        if (L.lane == 0) first = atomicAdd(p.work_counter, (unsigned long long)kItemsPerGrab);
+        first = __shfl_sync(kFull, first, 0);
+        if (first >= total) break;
+        const unsigned long long last = first + kItemsPerGrab < total ? first + kItemsPerGrab : total;
+        for (unsigned long long it = first; it < last; ++it) {
+            if (it < n_chunks) {
+                const int32_t* c = p.chunks + 3 * it;
+                process_item<T, OutT, NV, RTM>(p, L, c[0], c[1], c[2], (long long)it);
+            } else {
+                const int row = (int)(it - n_chunks);
+                const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
+                if (e1 - e0 > p.heavy_threshold) continue;  // done by chunks + merge
+                if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) continue;  // tile path
+                process_item<T, OutT, NV, RTM>(p, L, row, e0, e1, -1);
+            }
         }
     }
 }
@@ -371,7 +444,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
             float a = 0.f, s = 0.f;
             for (int c = c0; c < c1; ++c) {
                 const float* ml = p.part_ml + ((long long)c * p.H + h) * 2;
-                const float f = exp2f(ml[0] - mx);
+                const float f = ex2(ml[0] - mx);
                 s += ml[1] * f;
                 a += p.part_acc[(long long)c * HD + x] * f;
             }
@@ -382,22 +455,42 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
-template <typename T, typename OutT, bool RTM>
-cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
+template <typename T, typename OutT, int NV, bool RTM>
+cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
     const long long items = p.n_chunks + p.N;
     if (items <= 0) return cudaSuccess;
-    const long long blocks = (items + kWarpsPerCta - 1) / kWarpsPerCta;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // one resident wave of CTAs (cached per instantiation and device)
+    static int cached_dev = -1, cached_ctas = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != cached_dev) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, RTM>, kWarpsPerCta * 32, 0);
+        if (e != cudaSuccess) return e;
+        cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
+        cached_dev = dev;
+    }
+    const long long need = (items + (long long)kWarpsPerCta * kItemsPerGrab - 1) / ((long long)kWarpsPerCta * kItemsPerGrab);
+    const int ctas = (int)(need < cached_ctas ? need : cached_ctas);
+    e = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return e;
+    core_kernel<T, OutT, NV, RTM><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, typename OutT, bool RTM>
+cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
     const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
-    dim3 grid((unsigned)blocks), block(kWarpsPerCta * 32);
     switch (nv) {
-        case 1: core_kernel<T, OutT, 1, RTM><<<grid, block, 0, st>>>(p); break;
-        case 2: core_kernel<T, OutT, 2, RTM><<<grid, block, 0, st>>>(p); break;
-        case 4: core_kernel<T, OutT, 4, RTM><<<grid, block, 0, st>>>(p); break;
-        case 8: core_kernel<T, OutT, 8, RTM><<<grid, block, 0, st>>>(p); break;
+        case 1: return launch_core_nv<T, OutT, 1, RTM>(p, st);
+        case 2: return launch_core_nv<T, OutT, 2, RTM>(p, st);
+        case 4: return launch_core_nv<T, OutT, 4, RTM>(p, st);
+        case 8: return launch_core_nv<T, OutT, 8, RTM>(p, st);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template <typename OutT>

@@ -60,6 +60,7 @@ struct PlanArrays {
     // scan scratch
     int32_t* scan_blocks;      // [scan_block_capacity]
     PlanCounts* counts;
+    unsigned long long* work_counter;  // the fused kernel's work queue head
 };
 
 constexpr int kLargeCtas = 32;  // CTAs of the global-bitmap window compaction
@@ -96,6 +97,7 @@ struct CoreParams {
     float* part_acc;
     float* part_ml;
     const uint8_t* win_flags;  // nullptr when no window takes the tile path
+    unsigned long long* work_counter;  // device scratch word, zeroed before every launch
     long long N;
     long long n_chunks;
     int H, D;

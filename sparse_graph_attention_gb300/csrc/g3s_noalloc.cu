@@ -128,6 +128,7 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     cp.part_acc = a.part_acc;
     cp.part_ml = a.part_ml;
     cp.win_flags = nullptr;
+    cp.work_counter = a.work_counter;
     cp.N = s.N;
     cp.n_chunks = hc.n_chunks;
     cp.H = s.H;
