@@ -83,10 +83,13 @@ typedef enum g3s_variant {
  *  bsb             build the 16x8 BSB tiles: 1 on, 0 off, -1 when the tile path
  *                  is eligible (default -1)
  *  tile_path       route dense row windows to the tensor-core kernel: 1 on,
- *                  0 off, -1 automatic (default -1: on where compiled)
+ *                  0 off, -1 automatic (default -1: on where compiled, which
+ *                  is the standard form with fp16/bf16 inputs and d = 64,
+ *                  unless bsb = 0)
  *  tile_density_milli  a window takes the tile path when
  *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 150)
- *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default 32)
+ *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
+ *                  maximum with the tile path on: 32)
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
  *                  the global-bitmap planner kernel instead of the shared-
  *                  memory sort (default 2048; a testing knob)
@@ -223,6 +226,15 @@ g3s_status g3s_host_staging_size(const g3s_plan *plan, size_t *bytes);
 g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K_h, const void *V_h,
                             const void *Eproj_h, void *O_h, void *Eout_h, void *staging_d,
                             size_t staging_bytes, g3s_stream_t stream);
+
+/*
+ * Synchronise `stream` and report whether a kernel of an earlier g3s_forward
+ * on this plan gave up a bounded device-side wait (the tensor-core tile
+ * kernel waits on its MMAs for at most about one second).  Returns
+ * G3S_ERR_TIMEOUT once per such event (the flag is then cleared): the
+ * outputs of that forward are incomplete.  G3S_OK otherwise.
+ */
+g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
 
 /* Release the plan's host struct (the caller still owns the workspace). NULL is a no-op. */
 void g3s_plan_destroy(g3s_plan *plan);

@@ -87,7 +87,7 @@ _lib = None
 EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_options_init",
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
             "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
-            "g3s_forward_noalloc"]
+            "g3s_forward_noalloc", "g3s_forward_check"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -121,6 +121,8 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_plan_destroy.restype = None
         lib.g3s_forward_noalloc.argtypes = [P, P, I64, I64, I, I, I, I, P, P, P, P, P, P, P]
         lib.g3s_forward_noalloc.restype = I
+        lib.g3s_forward_check.argtypes = [P, P]
+        lib.g3s_forward_check.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -318,6 +320,11 @@ class Plan:
         with torch.cuda.device(self.device):
             _check(self._lib.g3s_forward(self.handle, q, k, v, e, o, eo, _stream_handle(stream)))
         return (O, Eout) if want_eout else O
+
+    def check(self, stream=None):
+        """``g3s_forward_check``: synchronise and raise G3SError(G3S_ERR_TIMEOUT)
+        if a forward kernel gave up a bounded device wait."""
+        _check(self._lib.g3s_forward_check(self.handle, _stream_handle(stream)))
 
     def staging_size(self) -> int:
         n = ctypes.c_size_t()

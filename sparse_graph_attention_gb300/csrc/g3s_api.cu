@@ -73,8 +73,7 @@ void default_options(g3s_plan_options* o) {
     o->out_dtype = G3S_F32;
 }
 
-// The tensor-core tile path is not part of this build yet.
-bool tile_path_compiled(int /*dtype*/, int /*variant*/, int /*head_dim*/) { return false; }
+bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
 
 g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype, int variant,
                        const g3s_plan_options& o, PlanShape* s) {
@@ -119,7 +118,10 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->bsb_smem_edges = o.bsb_smem_edges;
     s->tile_density_milli = o.tile_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
-    s->tile_enabled = tile_ok && o.tile_path != 0;
+    // automatic: on where compiled, unless the caller turned the BSB tiles off
+    s->tile_enabled = tile_ok && (o.tile_path == 1 || (o.tile_path == -1 && o.bsb != 0));
+    if (s->tile_enabled && o.tile_max_tiles > kTileMaxTilesPerWindow)
+        return fail(G3S_ERR_INVALID_ARG, "tile_max_tiles must be <= %d with the tile path on", kTileMaxTilesPerWindow);
     s->build_bsb = o.bsb == 1 || (o.bsb == -1 && s->tile_enabled);
     if (s->tile_enabled && !s->build_bsb)
         return fail(G3S_ERR_INVALID_ARG, "the tile path needs the BSB tiles (bsb = 0 with tile_path on)");
@@ -138,6 +140,7 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     Carver c{static_cast<char*>(base)};
     a->counts = c.take<PlanCounts>(1);
     a->work_counter = c.take<unsigned long long>(1);
+    a->fwd_status = c.take<int32_t>(1);
     a->bucket_of = c.take<uint8_t>(s.N);
     a->bucket_ptr = c.take<int32_t>(G3S_NUM_BUCKETS + 1);
     a->bucket_rows = c.take<int32_t>(s.N);
@@ -253,6 +256,7 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
     CUDA_OR_FAIL(cudaGetDevice(&dev), "cudaGetDevice");
     PlanCounts hc;
     CUDA_OR_FAIL(cudaMemsetAsync(a.counts, 0, sizeof(PlanCounts), stream), "cudaMemsetAsync(counts)");
+    CUDA_OR_FAIL(cudaMemsetAsync(a.fwd_status, 0, sizeof(int32_t), stream), "cudaMemsetAsync(status)");
     if (s.build_bsb && s.bitmap_words > 0)
         CUDA_OR_FAIL(cudaMemsetAsync(a.bitmap_scratch, 0, (size_t)kLargeCtas * 3 * s.bitmap_words * sizeof(uint32_t), stream),
                      "cudaMemsetAsync(bitmaps)");
@@ -389,6 +393,23 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.qscale = rtm ? inv_sqrt_d : inv_sqrt_d * 1.4426950408889634f;
     cp.eps = p->opts.rtm_epsilon;
     cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
+    if (p->counts.n_tile_windows > 0) {
+        TileParams tp;
+        tp.Q = Q;
+        tp.K = K;
+        tp.V = V;
+        tp.O = O;
+        tp.N = s.N;
+        tp.H = s.H;
+        tp.tile_windows = p->arr.tile_windows;
+        tp.n_tile_windows = p->counts.n_tile_windows;
+        tp.win_tile_ptr = p->arr.win_tile_ptr;
+        tp.tile_cols = p->arr.tile_cols;
+        tp.tile_bits = p->arr.tile_bits;
+        tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;
+        tp.status = p->arr.fwd_status;
+        CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
+    }
     CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream), "fused kernel launch");
     if (p->counts.n_chunks > 0) {
         MergeParams mp;
@@ -456,6 +477,20 @@ g3s_status g3s_forward_host(const g3s_plan* p, const void* Qh, const void* Kh, c
     if (node_out) CUDA_OR_FAIL(cudaMemcpyAsync(Oh, dO, node_out, cudaMemcpyDeviceToHost, stream), "D2H O");
     if (rtm && Eouth && edge_out)
         CUDA_OR_FAIL(cudaMemcpyAsync(Eouth, dEo, edge_out, cudaMemcpyDeviceToHost, stream), "D2H Eout");
+    return G3S_OK;
+}
+
+g3s_status g3s_forward_check(const g3s_plan* p, g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int32_t st = 0;
+    CUDA_OR_FAIL(cudaMemcpyAsync(&st, p->arr.fwd_status, sizeof st, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync(status)");
+    CUDA_OR_FAIL(cudaStreamSynchronize(stream), "cudaStreamSynchronize(check)");
+    if (st & kErrTimeout) {
+        CUDA_OR_FAIL(cudaMemsetAsync(p->arr.fwd_status, 0, sizeof(int32_t), stream), "cudaMemsetAsync(status)");
+        CUDA_OR_FAIL(cudaStreamSynchronize(stream), "cudaStreamSynchronize(check)");
+        return fail(G3S_ERR_TIMEOUT, "a forward kernel's bounded device wait gave up; its outputs are incomplete");
+    }
     return G3S_OK;
 }
 

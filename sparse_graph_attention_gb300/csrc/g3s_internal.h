@@ -20,7 +20,10 @@ enum : int32_t {
     kErrRowPtrOrder = 2,  // row_ptr decreasing somewhere
     kErrRowPtrEnd = 4,    // row_ptr[N] != E
     kErrColRange = 8,     // a source outside [0, N)
+    kErrTimeout = 16,     // a bounded device-side wait gave up (forward status word)
 };
+
+constexpr int kTileMaxTilesPerWindow = 32;  // tile-path windows have at most this many 16x8 tiles
 
 // Small device-resident counters filled by the planner and read back once.
 struct PlanCounts {
@@ -61,6 +64,7 @@ struct PlanArrays {
     int32_t* scan_blocks;      // [scan_block_capacity]
     PlanCounts* counts;
     unsigned long long* work_counter;  // the fused kernel's work queue head
+    int32_t* fwd_status;               // error bits set by forward kernels (kErrTimeout)
 };
 
 constexpr int kLargeCtas = 32;  // CTAs of the global-bitmap window compaction
@@ -131,6 +135,25 @@ cudaError_t core_launch_bf16(bool out_f32, bool rtm, const CoreParams& p, cudaSt
 cudaError_t merge_launch_f32(bool rtm, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool rtm, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool rtm, const MergeParams& p, cudaStream_t st);
+
+// ---- tensor-core tile kernel (g3s_tile.cu) -------------------------------
+struct TileParams {
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* O;
+    long long N;
+    int H;
+    const int32_t* tile_windows;
+    long long n_tile_windows;
+    const int32_t* win_tile_ptr;
+    const int32_t* tile_cols;
+    const uint32_t* tile_bits;
+    float scale_log2;  // log2(e)/sqrt(d)
+    int32_t* status;   // kErrTimeout is OR-ed in when a wait gives up
+};
+bool tile_supported(int dtype, int variant, int head_dim);
+cudaError_t tile_launch(int dtype, int out_dtype, const TileParams& p, cudaStream_t st);
 
 // ---- host helpers shared by the ABI translation units (g3s_api.cu) ---------
 namespace api {

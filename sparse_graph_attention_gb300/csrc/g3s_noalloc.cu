@@ -104,6 +104,7 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     // the planner (counters start at zero; every other array is fully written before it is read)
     PlanCounts hc;
     NOALLOC_CUDA(cudaMemsetAsync(a.counts, 0, sizeof(PlanCounts), stream), "cudaMemsetAsync(counts)");
+    NOALLOC_CUDA(cudaMemsetAsync(a.fwd_status, 0, sizeof(int32_t), stream), "cudaMemsetAsync(status)");
     NOALLOC_CUDA(plan_validate(row_ptr_d, col_idx_d, s, a, stream), "CSR validation launch");
     NOALLOC_CUDA(cudaMemcpyAsync(&hc, a.counts, sizeof hc, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync(counts)");
     NOALLOC_CUDA(cudaStreamSynchronize(stream), "cudaStreamSynchronize(validation)");

@@ -1,0 +1,457 @@
+// Tensor-core tile path: fused SDDMM -> masked softmax -> SpMM over the BSB
+// tiles of dense row windows, with tcgen05.mma accumulating in TMEM.
+//
+// Source: the Fused3S design (sciencestack.ai/paper/2505.08098): a 16-row
+// window is compacted to its unique source columns and tiled into 16x8 tiles
+// with bitmaps (Figure 1); one thread block owns a window's Q and O rows
+// (node-parallel, Figure 2); SDDMM, softmax and SpMM stay on chip with an
+// online softmax (TL;DR).  Its warp-level MMA layout is not reused: on sm_103a
+// one thread issues tcgen05.mma for the whole CTA and the accumulators live
+// in tensor memory.
+//
+// Mapping.  A CTA (4 warps, 128 threads) takes one group of up to 8 tile
+// windows and one head.  The 8 x 16 window rows stack into the 128 rows of
+// the MMA; the group's tiles are concatenated (window by window) and walked
+// 64 columns (8 tiles) at a time:
+//   1. cp.async gathers the K and V rows of the 64 columns (head h, d = 64)
+//      into 128-byte-swizzled shared memory (Q rows once per CTA);
+//   2. S = Q K^T (M=128, N=64, K=64) into TMEM columns [0, 64);
+//   3. thread i reads row i of S, masks entries outside its own window's
+//      tiles or absent from the bitmap, updates its running max / sum and
+//      writes P = 2^(s - m) in the input type to shared memory;
+//   4. O_chunk = P V (M=128, N=64, K=64; V read as an MN-major operand) into
+//      TMEM columns [64, 128), added by each thread to its fp32 row of O.
+// Rows are normalised and stored at the end.  Every wait on an mbarrier is
+// bounded (about one second of %globaltimer); on expiry the CTA sets the
+// plan's status word, frees its TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "g3s_internal.h"
+
+namespace g3s {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kD = 64;               // head_dim of this kernel
+constexpr int kNC = 64;              // columns per chunk (8 tiles)
+constexpr int kGroupWindows = 8;     // windows per CTA: 8 x 16 rows = 128 MMA rows
+constexpr int kMaxGroupTiles = kGroupWindows * kTileMaxTilesPerWindow;
+constexpr uint32_t kTmemCols = 128;  // S chunk [0, 64) + O chunk [64, 128)
+constexpr float kNegBig = -1e30f;
+constexpr float kRescaleSlack = 8.0f;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+struct TileSmem {
+    uint8_t q[128 * 128];  // Q rows, 128B-swizzled, K-major A operand
+    uint8_t k[kNC * 128];  // K rows of the chunk (K-major B operand of S)
+    uint8_t v[kNC * 128];  // V rows of the chunk (MN-major B operand of O)
+    uint8_t p[128 * 128];  // P rows (K-major A operand of O)
+    int cols[kNC];
+    uint32_t bits[8][4];
+    int tile_g[kMaxGroupTiles];      // global tile index of each group tile
+    int8_t tile_j[kMaxGroupTiles];   // window slot of each group tile
+    int win[kGroupWindows];
+    unsigned long long mbar;
+    uint32_t tmem_base;
+    int nw, tt;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* m, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(m)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* m, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// bounded wait: false when the phase did not complete within kWaitLimitNs
+__device__ bool mbar_wait_bounded(unsigned long long* m, uint32_t parity) {
+    if (mbar_try_wait(m, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(m, parity)) return true;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16 or bf16 in, fp32 accumulate)
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(unsigned long long* mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(mbar))
+                 : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"  // same statement: the outputs exist only after the wait
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.  Start address and the
+// two byte offsets are stored in 16-byte units; bits 46-47 hold the
+// descriptor version (1), bits 61-63 the swizzle mode (2 = 128 B).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1),
+// A/B type (bits 7-9 and 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0),
+// B major (bit 16: 0 K, 1 MN), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <typename T>
+struct Pack2;
+template <>
+struct Pack2<__nv_bfloat16> {
+    // round two floats to bf16, return the packed pair and the rounded values
+    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        float2 f = __bfloat1622float2(h);
+        ra = f.x;
+        rb = f.y;
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+template <>
+struct Pack2<__half> {
+    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
+        __half2 h = __floats2half2_rn(a, b);
+        float2 f = __half22float2(h);
+        ra = f.x;
+        rb = f.y;
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+template <typename OutT>
+__device__ __forceinline__ void store_row(void* O, long long off, const float (&o)[kD], float inv);
+template <>
+__device__ __forceinline__ void store_row<float>(void* O, long long off, const float (&o)[kD], float inv) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(O) + off);
+#pragma unroll
+    for (int i = 0; i < kD / 4; ++i) d[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+}
+template <>
+__device__ __forceinline__ void store_row<__nv_bfloat16>(void* O, long long off, const float (&o)[kD], float inv) {
+    uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(O) + off);
+#pragma unroll
+    for (int i = 0; i < kD / 8; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(o[8 * i + 2 * k] * inv, o[8 * i + 2 * k + 1] * inv);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+template <>
+__device__ __forceinline__ void store_row<__half>(void* O, long long off, const float (&o)[kD], float inv) {
+    uint4* d = reinterpret_cast<uint4*>(static_cast<__half*>(O) + off);
+#pragma unroll
+    for (int i = 0; i < kD / 8; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __half2 h = __floats2half2_rn(o[8 * i + 2 * k] * inv, o[8 * i + 2 * k + 1] * inv);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT>
+__global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int group = blockIdx.x, h = blockIdx.y;
+    const T* Q = static_cast<const T*>(p.Q);
+    const T* K = static_cast<const T*>(p.K);
+    const T* V = static_cast<const T*>(p.V);
+    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+    constexpr uint32_t kIdescS = idesc_f16(kBf16, false, 128, kNC);
+    constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kD);
+
+    // ---- set-up: TMEM, mbarrier, the group's windows and tiles ---------------
+    if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (tid == 0) mbar_init(&sm.mbar, 1);
+    if (tid < kGroupWindows) {
+        const long long idx = (long long)group * kGroupWindows + tid;
+        sm.win[tid] = idx < p.n_tile_windows ? p.tile_windows[idx] : -1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int nw = 0, tt = 0;
+        for (int j = 0; j < kGroupWindows && sm.win[j] >= 0; ++j) {
+            const int w = sm.win[j];
+            for (int t = p.win_tile_ptr[w]; t < p.win_tile_ptr[w + 1] && tt < kMaxGroupTiles; ++t) {
+                sm.tile_g[tt] = t;
+                sm.tile_j[tt] = (int8_t)j;
+                ++tt;
+            }
+            ++nw;
+        }
+        sm.nw = nw;
+        sm.tt = tt;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const uint32_t tmem_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    const int tt = sm.tt;
+
+    // ---- this thread's row ------------------------------------------------------
+    const int j = tid >> 4, r = tid & 15;
+    long long node = -1;
+    if (j < sm.nw) {
+        const long long n = (long long)sm.win[j] * kWinRows + r;
+        if (n < p.N) node = n;
+    }
+    {
+        const T* qrow = node >= 0 ? Q + (node * p.H + h) * kD : Q;
+        const uint32_t qdst = smem_u32(sm.q) + tid * 128;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) cp_async16(qdst + ((x ^ (tid & 7)) << 4), qrow + x * 8, node >= 0 ? 16u : 0u);
+    }
+
+    float o[kD];
+#pragma unroll
+    for (int i = 0; i < kD; ++i) o[i] = 0.f;
+    float m = kNegBig, l = 0.f;
+    uint32_t phase = 0;
+    bool failed = false;
+    const float scale = p.scale_log2;
+    const int nchunks = (tt + 7) / 8;
+
+    for (int ch = 0; ch < nchunks; ++ch) {
+        // chunk metadata
+        if (tid < kNC) {
+            const int t = ch * 8 + (tid >> 3);
+            sm.cols[tid] = t < tt ? p.tile_cols[(long long)sm.tile_g[t] * kTileCols + (tid & 7)] : -1;
+        } else if (tid < kNC + 32) {
+            const int s = (tid - kNC) >> 2, wd = (tid - kNC) & 3;
+            const int t = ch * 8 + s;
+            sm.bits[s][wd] = t < tt ? p.tile_bits[(long long)sm.tile_g[t] * 4 + wd] : 0u;
+        }
+        __syncthreads();
+        // gather the chunk's K and V rows (64 rows x 8 pieces of 16 B each)
+#pragma unroll
+        for (int it = 0; it < (kNC * 8) / kThreads; ++it) {
+            const int piece = tid + kThreads * it;
+            const int c = piece >> 3, x = piece & 7;
+            const int col = sm.cols[c];
+            const long long off = col >= 0 ? ((long long)col * p.H + h) * kD + x * 8 : 0;
+            const uint32_t d = (uint32_t)(c * 128 + ((x ^ (c & 7)) << 4));
+            cp_async16(smem_u32(sm.k) + d, K + off, col >= 0 ? 16u : 0u);
+            cp_async16(smem_u32(sm.v) + d, V + off, col >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // S = Q K^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks)
+                mma_f16(tmem, sdesc_sw128(smem_u32(sm.q) + ks * 32, 16, 1024), sdesc_sw128(smem_u32(sm.k) + ks * 32, 16, 1024),
+                        kIdescS, ks > 0 ? 1u : 0u);
+            mma_commit(&sm.mbar);
+        }
+        bool ok = mbar_wait_bounded(&sm.mbar, phase);
+        phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        tc_fence_after();
+
+        // masked online softmax of this row
+        float s[kNC];
+#pragma unroll
+        for (int q4 = 0; q4 < kNC / 16; ++q4) {
+            float v16[16];
+            tmem_ld16(tmem_row + q4 * 16, v16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s[q4 * 16 + i] = v16[i];
+        }
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int slot = 0; slot < 8; ++slot) {
+            const int t = ch * 8 + slot;
+            uint32_t mask8 = 0;
+            if (node >= 0 && t < tt && sm.tile_j[t] == j) mask8 = (sm.bits[slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float x = ((mask8 >> c) & 1u) ? s[slot * 8 + c] * scale : -INFINITY;
+                s[slot * 8 + c] = x;
+                cmax = fmaxf(cmax, x);
+            }
+        }
+        if (cmax > m + kRescaleSlack) {
+            const float corr = ex2(m - cmax);
+            l *= corr;
+#pragma unroll
+            for (int i = 0; i < kD; ++i) o[i] *= corr;
+            m = cmax;
+        }
+        {
+            const uint32_t pdst = smem_u32(sm.p) + tid * 128;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float ra, rb;
+                    w[k] = Pack2<T>::pack(ex2(s[x * 8 + 2 * k] - m), ex2(s[x * 8 + 2 * k + 1] - m), ra, rb);
+                    l += ra + rb;
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pdst + ((x ^ (tid & 7)) << 4)), "r"(w[0]),
+                             "r"(w[1]), "r"(w[2]), "r"(w[3])
+                             : "memory");
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // O_chunk = P V
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < kNC / 16; ++ks)
+                mma_f16(tmem + kNC, sdesc_sw128(smem_u32(sm.p) + ks * 32, 16, 1024),
+                        sdesc_sw128(smem_u32(sm.v) + ks * 16 * 128, kNC * 128, 1024), kIdescO, ks > 0 ? 1u : 0u);
+            mma_commit(&sm.mbar);
+        }
+        ok = mbar_wait_bounded(&sm.mbar, phase);
+        phase ^= 1u;
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < kD / 16; ++q4) {
+            float v16[16];
+            tmem_ld16(tmem_row + kNC + q4 * 16, v16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[q4 * 16 + i] += v16[i];
+        }
+        tc_fence_before();
+        __syncthreads();  // TMEM and shared buffers are reused by the next chunk
+    }
+    cp_async_wait_all();
+
+    if (!failed && node >= 0) store_row<OutT>(p.O, (node * p.H + h) * kD, o, l > 0.f ? 1.0f / l : 0.f);
+    if (failed && tid == 0) atomicOr(p.status, kErrTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, typename OutT>
+cudaError_t launch(const TileParams& p, cudaStream_t st) {
+    if (p.n_tile_windows <= 0) return cudaSuccess;
+    const size_t smem = sizeof(TileSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long groups = (p.n_tile_windows + kGroupWindows - 1) / kGroupWindows;
+    dim3 grid((unsigned)groups, (unsigned)p.H);
+    tile_kernel<T, OutT><<<grid, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tile_supported(int dtype, int variant, int head_dim) {
+    return (dtype == G3S_F16 || dtype == G3S_BF16) && variant == G3S_STANDARD && head_dim == kD;
+}
+
+cudaError_t tile_launch(int dtype, int out_dtype, const TileParams& p, cudaStream_t st) {
+    if (dtype == G3S_BF16) {
+        if (out_dtype == G3S_F32) return launch<__nv_bfloat16, float>(p, st);
+        if (out_dtype == G3S_BF16) return launch<__nv_bfloat16, __nv_bfloat16>(p, st);
+    } else if (dtype == G3S_F16) {
+        if (out_dtype == G3S_F32) return launch<__half, float>(p, st);
+        if (out_dtype == G3S_F16) return launch<__half, __half>(p, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace g3s

@@ -1,0 +1,115 @@
+"""GPU parity of the tensor-core tile path (tcgen05 + TMEM over BSB tiles)."""
+import numpy as np
+import pytest
+import torch
+
+import graphgen
+import oracle
+import sparse_graph_attention_gb300 as g3s
+
+from gpu_helpers import assert_close, assert_close_stored16, cast_values, device, ensure_built, run_case, upload_graph
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for the gpu tests")
+    ensure_built()
+
+
+def _run(g, H, dtype, plan_kw, seed=7):
+    vals = graphgen.make_values(g.num_nodes, g.num_edges, H, 64, False, seed=seed)
+    plan, O, errs = run_case(g, vals, H, 64, dtype, "standard", plan_kw=plan_kw)
+    plan.check()  # no bounded device wait gave up
+    return plan, O, vals
+
+
+def test_tile_small_batched_dense():
+    g = graphgen.batched_dense(num_graphs=24, seed=3)
+    plan, _, _ = _run(g, 8, "bf16", dict(tile_path=1))
+    st = plan.stats()
+    assert st["tile_path"] == 1 and st["tile_windows"] > 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tile_matches_core_path(dtype):
+    ensure_built()
+    g = graphgen.batched_dense(num_graphs=40, seed=5)
+    vals = graphgen.make_values(g.num_nodes, g.num_edges, 4, 64, False, seed=9)
+    t = {k: v.to(device()) for k, v in cast_values(vals, dtype).items()}
+    rp, ci = upload_graph(g)
+    tile = g3s.Plan(rp, ci, g.num_nodes, 4, 64, dtype, tile_path=1, tile_density_milli=0)
+    core = g3s.Plan(rp, ci, g.num_nodes, 4, 64, dtype, tile_path=0)
+    assert tile.stats()["tile_windows"] == (g.num_nodes + 15) // 16  # every window dense enough
+    assert core.stats()["tile_windows"] == 0
+    Ot = tile.forward(t["Q"], t["K"], t["V"])
+    Oc = core.forward(t["Q"], t["K"], t["V"])
+    tile.check()
+    want = oracle.forward(g.row_ptr, g.col_idx, g.num_nodes, 4, 64, dtype, "standard",
+                          *(cast_values(vals, dtype)[k] for k in "QKV"))
+    assert_close(Ot, want, dtype, "O tile path")
+    assert_close(Oc, want, dtype, "O core path")
+
+
+def test_tile_mixed_with_core_rows():
+    """Some windows dense (tile path), others sparse or holding heavy rows (core path)."""
+    a = graphgen.batched_dense(num_graphs=30, seed=11)       # dense windows
+    b = graphgen.powerlaw(num_nodes=2003, max_degree=1500, seed=12)  # sparse windows, heavy rows
+    off = a.num_nodes
+    rp = np.concatenate([a.row_ptr, a.row_ptr[-1] + b.row_ptr[1:]]).astype(np.int32)
+    col = np.concatenate([a.col_idx, b.col_idx + off]).astype(np.int32)
+    g = graphgen.Graph(rp, col)
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=150, heavy_threshold=60, chunk_edges=25))
+    st = plan.stats()
+    assert 0 < st["tile_windows"] < st["windows"] and st["chunks"] > 0
+
+
+def test_tile_many_chunks_per_window():
+    """Windows of 16 rows with up to 256 unique sources: 32 tiles, 4 chunks each."""
+    rng = np.random.default_rng(13)
+    n = 16 * 24 + 5
+    cols = []
+    deg = np.zeros(n, np.int64)
+    for i in range(n):
+        w = i // 16
+        pool = (np.arange(256) * 3 + w * 17) % n  # 256 distinct sources per window
+        s = np.sort(rng.choice(pool, size=rng.integers(60, 120), replace=False))
+        cols.append(s)
+        deg[i] = s.size
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
+    plan, _, _ = _run(g, 2, "f16", dict(tile_path=1, tile_density_milli=0, heavy_threshold=512))
+    st = plan.stats()
+    assert st["tile_windows"] == (n + 15) // 16
+    assert st["tiles"] > 20 * st["tile_windows"]
+
+
+def test_tile_multigraph_windows_stay_on_core():
+    g = graphgen.random_csr(200, 30, seed=17, multigraph=True)
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=0))
+    flags = plan.export("win_flags")
+    assert np.any(flags & 1)  # the multigraph has windows with repeated edges
+    assert not np.any(((flags & 1) != 0) & ((flags & 2) != 0))  # none of them takes the tile path
+
+
+def test_tile_sixteen_bit_output():
+    g = graphgen.batched_dense(num_graphs=16, seed=19)
+    plan, O, _ = _run(g, 8, "bf16", dict(tile_path=1, out_dtype="bf16"))
+    assert O.dtype == torch.bfloat16 and plan.stats()["tile_windows"] > 0
+
+
+def test_tile_rows_with_no_edges():
+    rng = np.random.default_rng(23)
+    n = 64
+    deg = rng.integers(5, 20, n)
+    deg[[3, 17, 18, 40]] = 0
+    cols = [np.sort(rng.choice(n, size=d, replace=False)) for d in deg]
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
+    plan, O, _ = _run(g, 1, "bf16", dict(tile_path=1, tile_density_milli=0))
+    assert plan.stats()["tile_windows"] == 4
+    assert torch.count_nonzero(O[[3, 17, 18, 40]]).item() == 0
