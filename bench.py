@@ -151,6 +151,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Largest value of x over all ranks (the slowest rank's time); x when not distributed."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(edges_per_step: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Edges per second of all ranks together (every rank runs its own replica)."""
+    return edges_per_step * steps * world / (elapsed_ms / 1000.0)
+
+
 def oracle_rate(g, w, t, target_s: float, rows_start: int = 0):
     """Time the fp64 oracle on a contiguous block of rows sized for ~target_s.
 
@@ -188,6 +204,12 @@ def parse_args():
     ap.add_argument("--size", default="full", choices=["full", "small"])
     ap.add_argument("--nodes", type=int, default=None, help="override the workload's node count (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for the cpu_baseline sample")
+    ap.add_argument("--tile-path", type=int, default=-1, choices=[-1, 0, 1],
+                    help="tensor-core tile path: -1 automatic (default), 0 off, 1 on")
+    ap.add_argument("--tile-density-milli", type=int, default=None,
+                    help="density cutoff of the tile path in 1/1000 (default: the library's)")
+    ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
+                    help="element type of O (default fp32)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -257,7 +279,12 @@ def main():
 
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant)
+    plan_kw = {"tile_path": args.tile_path}
+    if args.out_dtype:
+        plan_kw["out_dtype"] = args.out_dtype
+    if args.tile_density_milli is not None:
+        plan_kw["tile_density_milli"] = args.tile_density_milli
+    plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)
     torch.cuda.synchronize(dev)
     plan_ms = 1000.0 * (time.perf_counter() - t0)
     st = plan.stats()
@@ -298,13 +325,9 @@ def main():
         dist.barrier()
     total_ms = t_all0.elapsed_time(t_all1)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist:
-        x = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        total_ms = float(x.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    edges_all = g.num_edges * args.steps * world
-    value = edges_all / (total_ms / 1000.0)
+    value = whole_job_rate(g.num_edges, args.steps, world, total_ms)
 
     # ---- roofline of the forward (fused kernel + heavy-row merge) --------
     gathered, compulsory = byte_counts(g, w, plan.out_dtype)
@@ -322,6 +345,12 @@ def main():
     if traffic is not None:
         roofline["dram_gbs"] = traffic / fwd_s / 1e9
         roofline["dram_frac"] = traffic / fwd_s / 1e9 / peak
+    if st["tile_windows"] > 0:
+        # tile path: useful tile FLOPs (4 * 128 entries per 16x8 tile * d, per head) and the
+        # MMA FLOPs the kernel issues (two 128x64x64 products per 64-column chunk and head)
+        tiles = st["tiles_on_tile_path"] if "tiles_on_tile_path" in st else None
+        roofline["tile_windows"] = st["tile_windows"]
+        roofline["tile_window_nnz"] = st["tile_window_nnz"]
 
     # ---- end to end through the C ABI on host buffers --------------------
     e2e = None
@@ -347,16 +376,13 @@ def main():
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = a.elapsed_time(b)
-        if dist:
-            x = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            e2e_ms = float(x.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
         hd = w.heads * w.head_dim
         nb, nbo = g.num_nodes * hd * ELT[w.dtype], g.num_nodes * hd * ELT[plan.out_dtype]
         eb, ebo = g.num_edges * hd * ELT[w.dtype], g.num_edges * hd * ELT[plan.out_dtype]
         h2d = 3 * nb + (eb if w.variant == "rtmscore" else 0)
         d2h = nbo + (ebo if w.variant == "rtmscore" else 0)
-        e2e = {"value": g.num_edges * n_e2e * world / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(g.num_edges, n_e2e, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e}
 
     cpu = None
@@ -378,7 +404,8 @@ def main():
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms,
-            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tile_windows": st["tile_windows"]},
+            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tile_windows": st["tile_windows"],
+                     "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},
         }
         print(json.dumps(line), flush=True)
     if dist:

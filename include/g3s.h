@@ -87,7 +87,9 @@ typedef enum g3s_variant {
  *                  is the standard form with fp16/bf16 inputs and d = 64,
  *                  unless bsb = 0)
  *  tile_density_milli  a window takes the tile path when
- *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 150)
+ *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 500:
+ *                  on the batched 20-60-node graphs, density about 0.25, the
+ *                  CUDA-core kernel is faster)
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 32)
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by

@@ -64,7 +64,7 @@ void default_options(g3s_plan_options* o) {
     o->chunk_edges = 256;
     o->bsb = -1;
     o->tile_path = -1;
-    o->tile_density_milli = 150;
+    o->tile_density_milli = 500;
     o->tile_max_tiles = 32;
     o->bsb_smem_edges = 2048;
     o->rtm_elementwise_clamp = 1;

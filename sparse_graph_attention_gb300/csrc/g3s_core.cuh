@@ -49,6 +49,10 @@ struct Vec<float> {
                           __float_as_uint(f[3]));
     }
     __device__ static void store1(void* base, long long i, float x) { static_cast<float*>(base)[i] = x; }
+    __device__ static void to_float2(const uint4& r, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
+        f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+    }
 };
 
 __device__ __forceinline__ void bf2_to_float(uint32_t w, float& lo, float& hi) {
@@ -75,6 +79,13 @@ struct Vec<__nv_bfloat16> {
     }
     __device__ static void store1(void* base, long long i, float x) {
         static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+    }
+    // element 2k is the low half of word k
+    __device__ static void to_float2(const uint4& r, float2 (&f)[4]) {
+        f[0] = make_float2(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u));
+        f[1] = make_float2(__uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+        f[2] = make_float2(__uint_as_float(r.z << 16), __uint_as_float(r.z & 0xffff0000u));
+        f[3] = make_float2(__uint_as_float(r.w << 16), __uint_as_float(r.w & 0xffff0000u));
     }
 };
 
@@ -104,6 +115,12 @@ struct Vec<__half> {
     }
     __device__ static void store1(void* base, long long i, float x) {
         static_cast<__half*>(base)[i] = __float2half_rn(x);
+    }
+    __device__ static void to_float2(const uint4& r, float2 (&f)[4]) {
+        f[0] = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+        f[1] = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+        f[2] = __half22float2(*reinterpret_cast<const __half2*>(&r.z));
+        f[3] = __half22float2(*reinterpret_cast<const __half2*>(&r.w));
     }
 };
 
@@ -160,6 +177,142 @@ struct Lanes {
 };
 
 // ---------------------------------------------------------------------------
+// Per-lane state of one work item.
+// ---------------------------------------------------------------------------
+template <int NV, int VP>
+struct ItemState {
+    float2 q[NV][VP];    // query, pre-scaled (pairs of features)
+    float2 acc[NV][VP];  // sum of weight * value
+    float m[NV], l[NV];  // reference max (log2 units) and sum of weights
+    int cbase, idx_lo, idx_hi;  // window of 64 source indices held one per lane
+};
+
+// One step of S = G * U edges starting at CSR position `base`.  TAIL: the
+// step runs past the row's end; slots beyond it re-read the row's last edge
+// (a valid, cached address) and get weight 0, so no load is branched.
+template <bool TAIL, typename T, typename OutT, int NV, bool RTM, int VP>
+__device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
+                                          const int e1) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    const int rv = L.rv, g = L.g, lph = L.lph;
+    const int S = L.G * U;
+    if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
+        st.cbase += 64;
+        st.idx_lo = (st.cbase + L.lane < e1) ? __ldg(p.col_idx + st.cbase + L.lane) : 0;
+        st.idx_hi = (st.cbase + 32 + L.lane < e1) ? __ldg(p.col_idx + st.cbase + 32 + L.lane) : 0;
+    }
+    const int off = base - st.cbase;  // 0, S, 2S, ... < 64
+    const int last = e1 - 1 - st.cbase;
+    int src[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        int pos = off + g * U + u;
+        ok[u] = !TAIL || pos <= last;
+        if (TAIL) pos = ok[u] ? pos : last;
+        if (S <= 32) {
+            const int v = (off & 32) ? st.idx_hi : st.idx_lo;  // warp-uniform choice
+            src[u] = __shfl_sync(kFull, v, pos & 31);
+        } else {
+            const int a = __shfl_sync(kFull, st.idx_lo, pos & 31);
+            const int b = __shfl_sync(kFull, st.idx_hi, pos & 31);
+            src[u] = pos < 32 ? a : b;
+        }
+    }
+
+    const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
+    const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
+    uint4 kr[U][NV], vr[U][NV];
+    uint4 er[RTM ? U : 1][RTM ? NV : 1];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const long long o = (long long)src[u] * rv;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            kr[u][j] = ldg16(K4 + o + 32 * j);
+            vr[u][j] = ldg16(V4 + o + 32 * j);
+            if constexpr (RTM) {
+                const int e = ok[u] ? base + g * U + u : e1 - 1;
+                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)e * rv + 32 * j);
+            }
+        }
+    }
+
+    float lg[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float2 kf[VP];
+            VT::to_float2(kr[u][j], kf);
+            float s;
+            if constexpr (RTM) {
+                float2 ef[VP];
+                VT::to_float2(er[u][j], ef);
+                float uo[VE];
+                s = 0.f;
+#pragma unroll
+                for (int k = 0; k < VP; ++k) {
+                    float t0 = st.q[j][k].x * kf[k].x, t1 = st.q[j][k].y * kf[k].y;
+                    if (p.elementwise_clamp) {
+                        t0 = clamp5(t0);
+                        t1 = clamp5(t1);
+                    }
+                    uo[2 * k] = t0 * ef[k].x;
+                    uo[2 * k + 1] = t1 * ef[k].y;
+                    s += uo[2 * k];
+                    s += uo[2 * k + 1];
+                }
+                if (p.Eout != nullptr && ok[u])
+                    Store<OutT, VE>::run(p.Eout, ((long long)(base + g * U + u) * rv + L.sub + 32 * j) * VE, uo);
+            } else {
+                float2 s2 = make_float2(0.f, 0.f);  // packed fp32 FMA
+#pragma unroll
+                for (int k = 0; k < VP; ++k) s2 = __ffma2_rn(st.q[j][k], kf[k], s2);
+                s = s2.x + s2.y;
+            }
+            for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
+            lg[u][j] = s;
+        }
+    }
+
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        float w[U];
+        if constexpr (RTM) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = ok[u] ? ex2(clamp5(lg[u][j]) * kLog2e) : 0.f;
+        } else {
+            float mx = st.m[j];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (ok[u]) mx = fmaxf(mx, lg[u][j]);
+            if (mx > st.m[j] + kRescaleSlack) {  // move the reference max
+                const float corr = ex2(st.m[j] - mx);
+                const float2 c2 = make_float2(corr, corr);
+                st.l[j] *= corr;
+#pragma unroll
+                for (int k = 0; k < VP; ++k) st.acc[j][k] = __fmul2_rn(st.acc[j][k], c2);
+                st.m[j] = mx;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = ok[u] ? ex2(lg[u][j] - st.m[j]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float2 vf[VP];
+            VT::to_float2(vr[u][j], vf);
+            st.l[j] += w[u];
+            const float2 w2 = make_float2(w[u], w[u]);
+#pragma unroll
+            for (int k = 0; k < VP; ++k) st.acc[j][k] = __ffma2_rn(w2, vf[k], st.acc[j][k]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // One work item: destination `row`, CSR positions [e0, e1).  chunk >= 0 means
 // this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
 // otherwise normalise and write O.
@@ -168,180 +321,59 @@ template <typename T, typename OutT, int NV, bool RTM>
 __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
                                              const int e1, const long long chunk) {
     using VT = Vec<T>;
-    constexpr int VE = VT::N;                // elements per 16-byte vector
-    constexpr int U = NV >= 4 ? 1 : 4 / NV;  // edges per lane group per step
+    constexpr int VE = VT::N;  // elements per 16-byte vector
+    constexpr int VP = VE / 2;
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;
     const int rv = L.rv, g = L.g, sub = L.sub, lph = L.lph;
-    const int S = L.G * U;                   // edges per step (power of two, <= 64)
+    const int S = L.G * U;
 
+    ItemState<NV, VP> st;
+    st.cbase = e0;
+    st.idx_lo = (e0 + L.lane < e1) ? __ldg(p.col_idx + e0 + L.lane) : 0;
+    st.idx_hi = (e0 + 32 + L.lane < e1) ? __ldg(p.col_idx + e0 + 32 + L.lane) : 0;
     const uint4* Q4 = static_cast<const uint4*>(p.Q);
-    const uint4* K4 = static_cast<const uint4*>(p.K) + sub;
-    const uint4* V4 = static_cast<const uint4*>(p.V) + sub;
-    const uint4* E4 = static_cast<const uint4*>(p.E) + sub;
-
-    // source indices of the first 64 edges, one per lane in two registers
-    int cbase = e0;
-    int idx_lo = (e0 + L.lane < e1) ? __ldg(p.col_idx + e0 + L.lane) : 0;
-    int idx_hi = (e0 + 32 + L.lane < e1) ? __ldg(p.col_idx + e0 + 32 + L.lane) : 0;
-
-    float q[NV][VE];
+    const float2 qs = make_float2(p.qscale, p.qscale);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-        VT::to_float(ldg16(Q4 + (long long)row * rv + sub + 32 * j), q[j]);
+        VT::to_float2(ldg16(Q4 + (long long)row * rv + sub + 32 * j), st.q[j]);
 #pragma unroll
-        for (int k = 0; k < VE; ++k) q[j][k] *= p.qscale;
+        for (int k = 0; k < VP; ++k) {
+            st.q[j][k] = __fmul2_rn(st.q[j][k], qs);
+            st.acc[j][k] = make_float2(0.f, 0.f);
+        }
+        st.m[j] = kNegBig;
+        st.l[j] = 0.f;
     }
 
-    float m[NV], l[NV], acc[NV][VE];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        m[j] = kNegBig;
-        l[j] = 0.f;
-#pragma unroll
-        for (int k = 0; k < VE; ++k) acc[j][k] = 0.f;
-    }
-
-    for (int base = e0; base < e1; base += S) {
-        if (base - cbase >= 64) {  // warp-uniform: next 64 indices
-            cbase += 64;
-            idx_lo = (cbase + L.lane < e1) ? __ldg(p.col_idx + cbase + L.lane) : 0;
-            idx_hi = (cbase + 32 + L.lane < e1) ? __ldg(p.col_idx + cbase + 32 + L.lane) : 0;
-        }
-        const int off = base - cbase;   // 0, S, 2S, ... < 64
-        const int last = e1 - 1 - cbase;  // window position of the row's last edge
-        // Slots past the row's end re-read its last edge (a valid, cached
-        // address) and get weight 0, so the loads need no branch.
-        int src[U];
-        bool ok[U];
-        if (S <= 32) {
-            const int v = (off & 32) ? idx_hi : idx_lo;  // warp-uniform choice
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int pos = off + g * U + u;
-                ok[u] = pos <= last;
-                src[u] = __shfl_sync(kFull, v, (ok[u] ? pos : last) & 31);
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                int pos = off + g * U + u;
-                ok[u] = pos <= last;
-                pos = ok[u] ? pos : last;
-                const int a = __shfl_sync(kFull, idx_lo, pos & 31);
-                const int b = __shfl_sync(kFull, idx_hi, pos & 31);
-                src[u] = pos < 32 ? a : b;
-            }
-        }
-
-        uint4 kr[U][NV], vr[U][NV];
-        uint4 er[RTM ? U : 1][RTM ? NV : 1];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const long long o = (long long)src[u] * rv;
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                kr[u][j] = ldg16(K4 + o + 32 * j);
-                vr[u][j] = ldg16(V4 + o + 32 * j);
-                if constexpr (RTM) {
-                    const int e = ok[u] ? base + g * U + u : e1 - 1;
-                    er[u][j] = ldg16(E4 + (long long)e * rv + 32 * j);
-                }
-            }
-        }
-
-        float lg[U][NV];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                float kf[VE];
-                VT::to_float(kr[u][j], kf);
-                float s = 0.f;
-                if constexpr (RTM) {
-                    float ef[VE], uo[VE];
-                    VT::to_float(er[u][j], ef);
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) {
-                        float t = q[j][k] * kf[k];
-                        if (p.elementwise_clamp) t = clamp5(t);
-                        uo[k] = t * ef[k];
-                        s += uo[k];
-                    }
-                    if (p.Eout != nullptr && ok[u])
-                        Store<OutT, VE>::run(p.Eout, ((long long)(base + g * U + u) * rv + sub + 32 * j) * VE, uo);
-                } else {
-                    float2 s2 = make_float2(0.f, 0.f);  // packed fp32 FMA (two lanes of work per instruction)
-#pragma unroll
-                    for (int k = 0; k < VE; k += 2)
-                        s2 = __ffma2_rn(make_float2(q[j][k], q[j][k + 1]), make_float2(kf[k], kf[k + 1]), s2);
-                    s = s2.x + s2.y;
-                }
-                for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
-                lg[u][j] = s;
-            }
-        }
-
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if constexpr (RTM) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float sc = ok[u] ? ex2(clamp5(lg[u][j]) * kLog2e) : 0.f;
-                    float vf[VE];
-                    VT::to_float(vr[u][j], vf);
-                    l[j] += sc;
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) acc[j][k] = fmaf(sc, vf[k], acc[j][k]);
-                }
-            } else {
-                float mx = m[j];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (ok[u]) mx = fmaxf(mx, lg[u][j]);
-                if (mx > m[j] + kRescaleSlack) {  // move the reference max
-                    const float corr = ex2(m[j] - mx);
-                    l[j] *= corr;
-#pragma unroll
-                    for (int k = 0; k < VE; ++k) acc[j][k] *= corr;
-                    m[j] = mx;
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float pw = ok[u] ? ex2(lg[u][j] - m[j]) : 0.f;
-                    float vf[VE];
-                    VT::to_float(vr[u][j], vf);
-                    l[j] += pw;
-                    const float2 pw2 = make_float2(pw, pw);
-#pragma unroll
-                    for (int k = 0; k < VE; k += 2) {
-                        const float2 a2 = __ffma2_rn(pw2, make_float2(vf[k], vf[k + 1]), make_float2(acc[j][k], acc[j][k + 1]));
-                        acc[j][k] = a2.x;
-                        acc[j][k + 1] = a2.y;
-                    }
-                }
-            }
-        }
-    }
+    const int full_end = e0 + ((e1 - e0) & ~(S - 1));  // S is a power of two
+    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, RTM, VP>(p, L, st, base, e1);
+    if (full_end < e1) edge_step<true, T, OutT, NV, RTM, VP>(p, L, st, full_end, e1);
 
     // merge the lane groups (fixed butterfly order)
     for (int off = L.gsize; off < 32; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             if constexpr (RTM) {
-                l[j] += __shfl_xor_sync(kFull, l[j], off);
+                st.l[j] += __shfl_xor_sync(kFull, st.l[j], off);
 #pragma unroll
-                for (int k = 0; k < VE; ++k) acc[j][k] += __shfl_xor_sync(kFull, acc[j][k], off);
-            } else {
-                const float mo = __shfl_xor_sync(kFull, m[j], off);
-                const float lo = __shfl_xor_sync(kFull, l[j], off);
-                const float mx = fmaxf(m[j], mo);
-                const float ca = ex2(m[j] - mx), cb = ex2(mo - mx);
-                l[j] = l[j] * ca + lo * cb;
-#pragma unroll
-                for (int k = 0; k < VE; ++k) {
-                    const float ao = __shfl_xor_sync(kFull, acc[j][k], off);
-                    acc[j][k] = acc[j][k] * ca + ao * cb;
+                for (int k = 0; k < VP; ++k) {
+                    st.acc[j][k].x += __shfl_xor_sync(kFull, st.acc[j][k].x, off);
+                    st.acc[j][k].y += __shfl_xor_sync(kFull, st.acc[j][k].y, off);
                 }
-                m[j] = mx;
+            } else {
+                const float mo = __shfl_xor_sync(kFull, st.m[j], off);
+                const float lo = __shfl_xor_sync(kFull, st.l[j], off);
+                const float mx = fmaxf(st.m[j], mo);
+                const float ca = ex2(st.m[j] - mx), cb = ex2(mo - mx);
+                st.l[j] = st.l[j] * ca + lo * cb;
+#pragma unroll
+                for (int k = 0; k < VP; ++k) {
+                    const float ax = __shfl_xor_sync(kFull, st.acc[j][k].x, off);
+                    const float ay = __shfl_xor_sync(kFull, st.acc[j][k].y, off);
+                    st.acc[j][k].x = st.acc[j][k].x * ca + ax * cb;
+                    st.acc[j][k].y = st.acc[j][k].y * ca + ay * cb;
+                }
+                st.m[j] = mx;
             }
         }
     }
@@ -355,11 +387,12 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
             const int v = sub + 32 * j;
             float4* dst = reinterpret_cast<float4*>(pa + (long long)v * VE);
 #pragma unroll
-            for (int k = 0; k < VE; k += 4) dst[k / 4] = make_float4(acc[j][k], acc[j][k + 1], acc[j][k + 2], acc[j][k + 3]);
+            for (int k = 0; k < VP; k += 2)
+                dst[k / 2] = make_float4(st.acc[j][k].x, st.acc[j][k].y, st.acc[j][k + 1].x, st.acc[j][k + 1].y);
             if (v % lph == 0) {
                 float* ml = p.part_ml + (chunk * p.H + v / lph) * 2;
-                ml[0] = m[j];
-                ml[1] = l[j];
+                ml[0] = st.m[j];
+                ml[1] = st.l[j];
             }
         }
     } else {
@@ -367,12 +400,15 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
         for (int j = 0; j < NV; ++j) {
             float inv;
             if constexpr (RTM)
-                inv = 1.0f / (l[j] + p.eps);
+                inv = 1.0f / (st.l[j] + p.eps);
             else
-                inv = l[j] > 0.f ? 1.0f / l[j] : 0.f;
+                inv = st.l[j] > 0.f ? 1.0f / st.l[j] : 0.f;
             float o[VE];
 #pragma unroll
-            for (int k = 0; k < VE; ++k) o[k] = acc[j][k] * inv;
+            for (int k = 0; k < VP; ++k) {
+                o[2 * k] = st.acc[j][k].x * inv;
+                o[2 * k + 1] = st.acc[j][k].y * inv;
+            }
             Store<OutT, VE>::run(p.O, ((long long)row * rv + sub + 32 * j) * VE, o);
         }
     }
@@ -390,7 +426,7 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 // on its own data, so the dynamic order does not change any output.
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT, int NV, bool RTM>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? 4 : 1) core_kernel(const CoreParams p) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (RTM ? 3 : 4) : 1) core_kernel(const CoreParams p) {
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
     const unsigned long long total = n_chunks + (unsigned long long)p.N;

@@ -1,0 +1,53 @@
+"""bench.py's multi-rank host logic on CPU: two gloo ranks agree on the
+slowest rank's time, and the whole-job rate counts every replica."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(10.0 + 5.0 * rank, dist, "cpu")
+        with open(os.path.join(out_dir, "rank%d" % rank), "w") as f:
+            f.write(repr(t))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks(tmp_path):
+    port = _free_port()
+    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    got = [float(open(tmp_path / ("rank%d" % r)).read()) for r in range(2)]
+    assert got == [15.0, 15.0]
+
+
+def test_single_process_paths():
+    assert bench.max_over_ranks(3.5) == 3.5
+    # 100 edges x 10 steps x 4 replicas in 2 ms
+    assert bench.whole_job_rate(100, 10, 4, 2.0) == pytest.approx(2.0e6)
+
+
+def test_byte_model():
+    import graphgen
+
+    g = graphgen.tiny_poisson()
+    w = graphgen.WORKLOADS["tiny_poisson"]
+    gathered, compulsory = bench.byte_counts(g, w, "f32")
+    hd = w.heads * w.head_dim
+    assert gathered == 4 * (g.num_nodes + 1) + 4 * g.num_edges + 2 * g.num_nodes * hd * 4 + 2 * g.num_edges * hd * 4
+    assert compulsory == 4 * (g.num_nodes + 1) + 4 * g.num_edges + 4 * g.num_nodes * hd * 4

@@ -28,9 +28,18 @@ def _run(g, H, dtype, plan_kw, seed=7):
 
 def test_tile_small_batched_dense():
     g = graphgen.batched_dense(num_graphs=24, seed=3)
-    plan, _, _ = _run(g, 8, "bf16", dict(tile_path=1))
+    plan, _, _ = _run(g, 8, "bf16", dict(tile_path=1, tile_density_milli=150))
     st = plan.stats()
     assert st["tile_path"] == 1 and st["tile_windows"] > 0
+
+
+def test_full_batched_dense_on_tile_path():
+    """The batched dense-ish workload at full size with its windows on the tile path."""
+    g, vals, w = graphgen.make_workload("batched_dense", "full")
+    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant,
+                          plan_kw=dict(tile_path=1, tile_density_milli=150))
+    plan.check()
+    assert plan.stats()["tile_windows"] > 0.8 * plan.stats()["windows"]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -97,7 +106,7 @@ def test_tile_multigraph_windows_stay_on_core():
 
 def test_tile_sixteen_bit_output():
     g = graphgen.batched_dense(num_graphs=16, seed=19)
-    plan, O, _ = _run(g, 8, "bf16", dict(tile_path=1, out_dtype="bf16"))
+    plan, O, _ = _run(g, 8, "bf16", dict(tile_path=1, out_dtype="bf16", tile_density_milli=150))
     assert O.dtype == torch.bfloat16 and plan.stats()["tile_windows"] > 0
 
 
