@@ -14,7 +14,10 @@
 // the MMA; the group's tiles are concatenated (window by window) and walked
 // 64 columns (8 tiles) at a time:
 //   1. cp.async gathers the K and V rows of the 64 columns (head h, d = 64)
-//      into 128-byte-swizzled shared memory (Q rows once per CTA);
+//      into 128-byte-swizzled shared memory (Q rows once per CTA); the
+//      gathers of the next chunk (two buffers) and the column ids and bitmaps
+//      of the chunk after it (three buffers) are in flight while this chunk
+//      is computed;
 //   2. S = Q K^T (M=128, N=64, K=64) into TMEM columns [0, 64);
 //   3. thread i reads row i of S, masks entries outside its own window's
 //      tiles or absent from the bitmap, updates its running max / sum and
@@ -45,14 +48,14 @@ constexpr float kRescaleSlack = 8.0f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 struct TileSmem {
-    uint8_t q[128 * 128];  // Q rows, 128B-swizzled, K-major A operand
-    uint8_t k[kNC * 128];  // K rows of the chunk (K-major B operand of S)
-    uint8_t v[kNC * 128];  // V rows of the chunk (MN-major B operand of O)
-    uint8_t p[128 * 128];  // P rows (K-major A operand of O)
-    int cols[kNC];
-    uint32_t bits[8][4];
-    int tile_g[kMaxGroupTiles];      // global tile index of each group tile
-    int8_t tile_j[kMaxGroupTiles];   // window slot of each group tile
+    uint8_t q[128 * 128];     // Q rows, 128B-swizzled, K-major A operand
+    uint8_t k[2][kNC * 128];  // K rows of a chunk (K-major B operand of S), two stages
+    uint8_t v[2][kNC * 128];  // V rows of a chunk (MN-major B operand of O), two stages
+    uint8_t p[128 * 128];     // P rows (K-major A operand of O)
+    int cols[3][kNC];         // column ids of a chunk, three stages
+    uint32_t bits[3][8][4];   // bitmaps of a chunk's 8 tiles, three stages
+    int tile_g[kMaxGroupTiles];     // global tile index of each group tile
+    int8_t tile_j[kMaxGroupTiles];  // window slot of each group tile
     int win[kGroupWindows];
     unsigned long long mbar;
     uint32_t tmem_base;
@@ -247,24 +250,38 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     // ---- set-up: TMEM, mbarrier, the group's windows and tiles ---------------
     if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid == 0) mbar_init(&sm.mbar, 1);
-    if (tid < kGroupWindows) {
-        const long long idx = (long long)group * kGroupWindows + tid;
-        sm.win[tid] = idx < p.n_tile_windows ? p.tile_windows[idx] : -1;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int nw = 0, tt = 0;
-        for (int j = 0; j < kGroupWindows && sm.win[j] >= 0; ++j) {
-            const int w = sm.win[j];
-            for (int t = p.win_tile_ptr[w]; t < p.win_tile_ptr[w + 1] && tt < kMaxGroupTiles; ++t) {
-                sm.tile_g[tt] = t;
-                sm.tile_j[tt] = (int8_t)j;
-                ++tt;
+    // windows of the group and their tile ranges, read in parallel by the first warp
+    if (warp == 0) {
+        const int lane = tid;
+        int w = -1, t0 = 0, cnt = 0;
+        if (lane < kGroupWindows) {
+            const long long idx = (long long)group * kGroupWindows + lane;
+            if (idx < p.n_tile_windows) {
+                w = p.tile_windows[idx];
+                t0 = p.win_tile_ptr[w];
+                cnt = min(p.win_tile_ptr[w + 1] - t0, kTileMaxTilesPerWindow);
             }
-            ++nw;
+            sm.win[lane] = w;
         }
-        sm.nw = nw;
-        sm.tt = tt;
+        int start = cnt;  // exclusive prefix of the tile counts over the 8 windows
+#pragma unroll
+        for (int o = 1; o < kGroupWindows; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, start, o);
+            if (lane >= o) start += y;
+        }
+        start -= cnt;
+        if (lane < kGroupWindows) {
+            for (int k = 0; k < cnt; ++k) {
+                sm.tile_g[start + k] = t0 + k;
+                sm.tile_j[start + k] = (int8_t)lane;
+            }
+        }
+        const int nw = __popc(__ballot_sync(0xffffffffu, w >= 0));
+        const int tt = __shfl_sync(0xffffffffu, start + cnt, kGroupWindows - 1);
+        if (lane == 0) {
+            sm.nw = nw;
+            sm.tt = tt;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -272,6 +289,35 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     const uint32_t tmem = sm.tmem_base;
     const uint32_t tmem_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
     const int tt = sm.tt;
+    const int nchunks = (tt + 7) / 8;
+
+    // chunk `ch`'s column ids and bitmaps into meta stage `ms` (24 copies of 16 B)
+    auto issue_meta = [&](int ch, int ms) {
+        if (tid < 24) {
+            const int slot = tid / 3, part = tid - 3 * slot;
+            const int t = ch * 8 + slot;
+            const bool valid = t < tt;
+            const long long g = valid ? sm.tile_g[t] : 0;
+            if (part < 2)
+                cp_async16(smem_u32(&sm.cols[ms][slot * 8 + part * 4]), p.tile_cols + g * kTileCols + part * 4,
+                           valid ? 16u : 0u);
+            else
+                cp_async16(smem_u32(&sm.bits[ms][slot][0]), p.tile_bits + g * 4, valid ? 16u : 0u);
+        }
+    };
+    // chunk `ch`'s K and V rows (64 rows x 8 pieces of 16 B) into stage `ks`
+    auto issue_gather = [&](int ch, int ks, int ms) {
+#pragma unroll
+        for (int it = 0; it < (kNC * 8) / kThreads; ++it) {
+            const int piece = tid + kThreads * it;
+            const int c = piece >> 3, x = piece & 7;
+            const int col = (ch * 8 + (c >> 3)) < tt ? sm.cols[ms][c] : -1;
+            const long long off = col >= 0 ? ((long long)col * p.H + h) * kD + x * 8 : 0;
+            const uint32_t d = (uint32_t)(c * 128 + ((x ^ (c & 7)) << 4));
+            cp_async16(smem_u32(sm.k[ks]) + d, K + off, col >= 0 ? 16u : 0u);
+            cp_async16(smem_u32(sm.v[ks]) + d, V + off, col >= 0 ? 16u : 0u);
+        }
+    };
 
     // ---- this thread's row ------------------------------------------------------
     const int j = tid >> 4, r = tid & 15;
@@ -280,12 +326,21 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         const long long n = (long long)sm.win[j] * kWinRows + r;
         if (n < p.N) node = n;
     }
+
+    // ---- prologue: Q, chunk 0's metadata, then chunk 0's rows + chunk 1's metadata
     {
         const T* qrow = node >= 0 ? Q + (node * p.H + h) * kD : Q;
         const uint32_t qdst = smem_u32(sm.q) + tid * 128;
 #pragma unroll
         for (int x = 0; x < 8; ++x) cp_async16(qdst + ((x ^ (tid & 7)) << 4), qrow + x * 8, node >= 0 ? 16u : 0u);
     }
+    issue_meta(0, 0);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    if (nchunks > 0) issue_gather(0, 0, 0);
+    if (nchunks > 1) issue_meta(1, 1);
+    cp_async_commit();
 
     float o[kD];
 #pragma unroll
@@ -294,32 +349,10 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     uint32_t phase = 0;
     bool failed = false;
     const float scale = p.scale_log2;
-    const int nchunks = (tt + 7) / 8;
 
     for (int ch = 0; ch < nchunks; ++ch) {
-        // chunk metadata
-        if (tid < kNC) {
-            const int t = ch * 8 + (tid >> 3);
-            sm.cols[tid] = t < tt ? p.tile_cols[(long long)sm.tile_g[t] * kTileCols + (tid & 7)] : -1;
-        } else if (tid < kNC + 32) {
-            const int s = (tid - kNC) >> 2, wd = (tid - kNC) & 3;
-            const int t = ch * 8 + s;
-            sm.bits[s][wd] = t < tt ? p.tile_bits[(long long)sm.tile_g[t] * 4 + wd] : 0u;
-        }
-        __syncthreads();
-        // gather the chunk's K and V rows (64 rows x 8 pieces of 16 B each)
-#pragma unroll
-        for (int it = 0; it < (kNC * 8) / kThreads; ++it) {
-            const int piece = tid + kThreads * it;
-            const int c = piece >> 3, x = piece & 7;
-            const int col = sm.cols[c];
-            const long long off = col >= 0 ? ((long long)col * p.H + h) * kD + x * 8 : 0;
-            const uint32_t d = (uint32_t)(c * 128 + ((x ^ (c & 7)) << 4));
-            cp_async16(smem_u32(sm.k) + d, K + off, col >= 0 ? 16u : 0u);
-            cp_async16(smem_u32(sm.v) + d, V + off, col >= 0 ? 16u : 0u);
-        }
-        cp_async_commit();
-        cp_async_wait_all();
+        const int ks = ch & 1, ms = ch % 3;
+        cp_async_wait_all();  // chunk ch's rows and chunk ch+1's metadata
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -328,11 +361,17 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         // S = Q K^T
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)
-                mma_f16(tmem, sdesc_sw128(smem_u32(sm.q) + ks * 32, 16, 1024), sdesc_sw128(smem_u32(sm.k) + ks * 32, 16, 1024),
-                        kIdescS, ks > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kD / 16; ++kk)
+                mma_f16(tmem, sdesc_sw128(smem_u32(sm.q) + kk * 32, 16, 1024),
+                        sdesc_sw128(smem_u32(sm.k[ks]) + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
             mma_commit(&sm.mbar);
         }
+        // next chunk's rows (into the other stage, free since the last chunk's MMAs
+        // completed) and the metadata two chunks ahead, in flight during this chunk
+        if (ch + 1 < nchunks) issue_gather(ch + 1, ks ^ 1, (ch + 1) % 3);
+        if (ch + 2 < nchunks) issue_meta(ch + 2, (ch + 2) % 3);
+        cp_async_commit();
+
         bool ok = mbar_wait_bounded(&sm.mbar, phase);
         phase ^= 1u;
         if (__syncthreads_or(!ok)) {
@@ -355,7 +394,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         for (int slot = 0; slot < 8; ++slot) {
             const int t = ch * 8 + slot;
             uint32_t mask8 = 0;
-            if (node >= 0 && t < tt && sm.tile_j[t] == j) mask8 = (sm.bits[slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
+            if (node >= 0 && t < tt && sm.tile_j[t] == j) mask8 = (sm.bits[ms][slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float x = ((mask8 >> c) & 1u) ? s[slot * 8 + c] * scale : -INFINITY;
@@ -394,9 +433,9 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         // O_chunk = P V
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < kNC / 16; ++ks)
-                mma_f16(tmem + kNC, sdesc_sw128(smem_u32(sm.p) + ks * 32, 16, 1024),
-                        sdesc_sw128(smem_u32(sm.v) + ks * 16 * 128, kNC * 128, 1024), kIdescO, ks > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kNC / 16; ++kk)
+                mma_f16(tmem + kNC, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
+                        sdesc_sw128(smem_u32(sm.v[ks]) + kk * 16 * 128, kNC * 128, 1024), kIdescO, kk > 0 ? 1u : 0u);
             mma_commit(&sm.mbar);
         }
         ok = mbar_wait_bounded(&sm.mbar, phase);
@@ -414,7 +453,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
             for (int i = 0; i < 16; ++i) o[q4 * 16 + i] += v16[i];
         }
         tc_fence_before();
-        __syncthreads();  // TMEM and shared buffers are reused by the next chunk
+        __syncthreads();  // TMEM, P and this chunk's stages are reused next
     }
     cp_async_wait_all();
 
