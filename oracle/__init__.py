@@ -6,6 +6,7 @@ product library never loads it, and it never loads the product library.
 
 * ``forward``   -- the attention definitions, in C (``g3s_oracle.c``), fp64,
                    OpenMP over rows.
+* ``aggregate`` -- the weighted (optionally normalised) aggregation, same file.
 * ``decode``    -- the exact widening of stored fp32 / fp16 / bf16 values.
 * ``planner``   -- numpy reference of the degree buckets, heavy-row chunks and
                    BSB tiles (``planner.py``).
@@ -57,6 +58,9 @@ def _bind(path):
     lib.g3s_oracle_decode.argtypes = [ctypes.c_int, P, ctypes.c_int64, P]
     lib.g3s_oracle_decode.restype = ctypes.c_int
     lib.g3s_oracle_threads.restype = ctypes.c_int
+    lib.g3s_oracle_aggregate.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
+                                         ctypes.c_int64, P, ctypes.c_int, ctypes.c_double]
+    lib.g3s_oracle_aggregate.restype = ctypes.c_int
     return lib
 
 
@@ -154,3 +158,27 @@ def forward(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant, Q, K, 
     if rc:
         raise ValueError("bad oracle arguments")
     return (O, Eout) if want_eout else O
+
+
+def aggregate(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, W, X, rows=None, normalize=False, eps=1e-6,
+              lib=None):
+    """fp64 weighted aggregation for ``rows`` (default all): O of shape (len(rows), H, d)."""
+    lib = lib if lib is not None else _load()
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    n = int(num_nodes)
+    rows = np.arange(n, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    w, x = _raw(W, dtype), _raw(X, dtype)
+    if w.size != col_idx.size * heads:
+        raise ValueError("W must have E*H elements")
+    if x.size != n * heads * head_dim:
+        raise ValueError("X must have N*H*d elements")
+    O = np.zeros((rows.size, heads, head_dim), np.float64)
+    rc = lib.g3s_oracle_aggregate(row_ptr.ctypes.data, col_idx.ctypes.data, n, heads, head_dim, DTYPES[dtype],
+                                  w.ctypes.data, x.ctypes.data, rows.ctypes.data, rows.size, O.ctypes.data,
+                                  1 if normalize else 0, float(eps))
+    if rc == 2:
+        raise ValueError("graph index out of range")
+    if rc:
+        raise ValueError("bad oracle arguments")
+    return O

@@ -30,8 +30,16 @@
  *       s     = exp(clamp(l, -5, 5))
  *       O_i^h = sum_j s_j v_j[h,:] / (sum_j s_j + eps)
  *
- * Layouts: Q, K, V, O are (N, H, d) row-major; E and Eout are (E, H, d)
- * row-major indexed by CSR position.  row_ptr (N+1) and col_idx (E) int32.
+ *   Weighted aggregation (the article's normalised scatter-add, section
+ *   "Optimizing the scatter add in Triton" and "Using the CSC index for fast
+ *   edge lookup"; the POPCORNBENCH CSR aggregation task's reference loop):
+ *       O_i^h = sum_j w_ij^h x_j[h,:]                          (normalize = 0)
+ *       O_i^h = sum_j w_ij^h x_j[h,:] / (sum_j w_ij^h + eps)    (normalize = 1)
+ *   with the weights w given per CSR entry and head, W of shape (E, H).
+ *
+ * Layouts: Q, K, V, X, O are (N, H, d) row-major; E and Eout are (E, H, d)
+ * row-major indexed by CSR position; W is (E, H).  row_ptr (N+1) and col_idx
+ * (E) int32.
  *
  * Parallelism: OpenMP over the listed rows only; the per-row arithmetic order
  * is fixed (edges in CSR order, features in index order), so results do not
@@ -181,6 +189,41 @@ int g3s_oracle_forward(const int32_t *row_ptr, const int32_t *col_idx, int64_t N
                 }
                 for (int f = 0; f < d; ++f) o[(int64_t)h * d + f] /= (ssum + eps);
             }
+        }
+    }
+    return bad ? 2 : 0;
+}
+
+/*
+ * Weighted aggregation for the rows listed in rows[0..n_rows); O_out is
+ * (n_rows, H, d).  Returns 0 on success, 1 on bad arguments, 2 on an index
+ * outside [0, N).
+ */
+int g3s_oracle_aggregate(const int32_t *row_ptr, const int32_t *col_idx, int64_t N, int H, int d, int dtype,
+                         const void *W, const void *X, const int64_t *rows, int64_t n_rows, double *O_out,
+                         int normalize, double eps)
+{
+    if (H <= 0 || d <= 0 || dtype < 0 || dtype > 2 || W == NULL || X == NULL) return 1;
+    const int64_t HD = (int64_t)H * d;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (int64_t k = 0; k < n_rows; ++k) {
+        const int64_t i = rows[k];
+        double *o = O_out + k * HD;
+        for (int64_t x = 0; x < HD; ++x) o[x] = 0.0;
+        if (i < 0 || i >= N) { bad = 1; continue; }
+        for (int h = 0; h < H; ++h) {
+            double wsum = 0.0;
+            for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+                const int64_t j = col_idx[e];
+                if (j < 0 || j >= N) { bad = 1; continue; }
+                const double w = load_elem(W, dtype, e * H + h);
+                wsum += w;
+                for (int f = 0; f < d; ++f)
+                    o[(int64_t)h * d + f] += w * load_elem(X, dtype, j * HD + (int64_t)h * d + f);
+            }
+            if (normalize)
+                for (int f = 0; f < d; ++f) o[(int64_t)h * d + f] /= (wsum + eps);
         }
     }
     return bad ? 2 : 0;

@@ -295,6 +295,66 @@ def pin_sixteen_bit_inputs(fwd):
             assert np.array_equal(got, want)
 
 
+# ---------------------------------------------------------------------------
+# 4. Weighted aggregation
+# ---------------------------------------------------------------------------
+def pin_aggregate_reference_loop(agg):
+    """The CSR aggregation task's reference loop: out[dst] = (x[src] * w[start:end, :, None]).sum(0)."""
+    for seed, (n, H, d, multi) in enumerate([(40, 8, 32, False), (33, 2, 16, True), (17, 1, 64, False)]):
+        rng = np.random.default_rng(500 + seed)
+        rp, col = _rand_graph(600 + seed, n, 20, multi)
+        x = rng.standard_normal((n, H, d)).astype(np.float32)
+        w = rng.standard_normal((col.size, H)).astype(np.float32)
+        want = np.zeros((n, H, d))
+        for dst in range(n):
+            a, b = rp[dst], rp[dst + 1]
+            if b > a:
+                want[dst] = (x[col[a:b]].astype(np.float64) * w[a:b, :, None].astype(np.float64)).sum(0)
+        got = agg(rp, col, n, H, d, "f32", w, x)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12), np.abs(got - want).max()
+
+
+def pin_aggregate_index_add(agg):
+    """The article's normalised scatter-add: two index_add_ scatters (sum of scaled
+    values, sum of scores) and numerator / (denominator + eps), in torch fp64."""
+    import torch
+
+    n, H, d = 37, 4, 16
+    rng = np.random.default_rng(71)
+    rp, col = _rand_graph(72, n, 15, True)
+    x = rng.standard_normal((n, H, d)).astype(np.float32)
+    w = rng.random((col.size, H)).astype(np.float32) + 0.1
+    dst = torch.from_numpy(np.repeat(np.arange(n), np.diff(rp)))
+    v_scaled = torch.from_numpy(x).double()[torch.from_numpy(col.astype(np.int64))] * torch.from_numpy(w).double()[:, :, None]
+    num = torch.zeros(n, H, d, dtype=torch.float64).index_add_(0, dst, v_scaled)
+    den = torch.zeros(n, H, 1, dtype=torch.float64).index_add_(0, dst, torch.from_numpy(w).double()[:, :, None])
+    want = (num / (den + EPS)).numpy()
+    got = agg(rp, col, n, H, d, "f32", w, x, normalize=True, eps=EPS)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-13)
+    got0 = agg(rp, col, n, H, d, "f32", w, x)
+    assert np.allclose(got0, num.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_aggregate_closed_forms(agg):
+    rp, col, q, k, v, _ = _graph_and_values(91)
+    n, H, d = v.shape
+    deg = np.diff(rp)
+    ones = np.ones((col.size, H), np.float32)
+    sums = np.zeros((n, H, d))
+    for i in range(n):
+        if deg[i]:
+            sums[i] = v[col[rp[i]:rp[i + 1]]].astype(np.float64).sum(0)
+    assert np.allclose(agg(rp, col, n, H, d, "f32", ones, v), sums, rtol=1e-13, atol=1e-14)
+    want = sums / (deg[:, None, None] + 0.5)
+    assert np.allclose(agg(rp, col, n, H, d, "f32", ones, v, normalize=True, eps=0.5), want, rtol=1e-13, atol=1e-14)
+    zero = np.zeros_like(ones)
+    out = agg(rp, col, n, H, d, "f32", zero, v, normalize=True, eps=1e-6)
+    assert np.all(out == 0.0)
+
+
+AGG_PINS = [pin_aggregate_reference_loop, pin_aggregate_index_add, pin_aggregate_closed_forms]
+
+
 ALL_PINS = [
     pin_four_node_standard,
     pin_four_node_rtmscore,

@@ -28,6 +28,9 @@ MUTANTS = [
     ("variant_value_weight_unexp", "o[(int64_t)h * d + f] += s * load_elem", "o[(int64_t)h * d + f] += l * load_elem", 1),
     ("f16_exponent_bias", "expo - 25", "expo - 24", 1),
     ("bf16_shift", "(uint32_t)b << 16", "(uint32_t)b << 15", 1),
+    ("aggregate_weight_of_wrong_head", "load_elem(W, dtype, e * H + h)", "load_elem(W, dtype, e * H)", 1),
+    ("aggregate_feature_of_destination", "w * load_elem(X, dtype, j * HD", "w * load_elem(X, dtype, i * HD", 1),
+    ("aggregate_no_epsilon", "/= (wsum + eps);", "/= (wsum);", 1),
     ("variant_scale_applied_twice", "load_elem(K, dtype, j * HD + (int64_t)h * d + f) * scale;",
      "load_elem(K, dtype, j * HD + (int64_t)h * d + f) * scale * scale;", 1),
 ]
@@ -36,9 +39,10 @@ MUTANTS = [
 def _pins_fail(lib):
     fwd = functools.partial(oracle.forward, lib=lib)
     caught = []
-    for pin in pins.ALL_PINS:
+    agg = functools.partial(oracle.aggregate, lib=lib)
+    for pin in pins.ALL_PINS + pins.AGG_PINS:
         try:
-            pin(fwd)
+            pin(agg if pin in pins.AGG_PINS else fwd)
         except (AssertionError, ValueError, FloatingPointError):
             caught.append(pin.__name__)
     return caught

@@ -12,6 +12,24 @@ def test_pin(pin):
     pin(oracle.forward)
 
 
+@pytest.mark.parametrize("pin", pins.AGG_PINS, ids=lambda p: p.__name__)
+def test_aggregate_pin(pin):
+    pin(oracle.aggregate)
+
+
+def test_aggregate_sixteen_bit_inputs_read_exactly():
+    import torch
+
+    rp, col, q, k, v, _ = pins._graph_and_values(93)
+    n, H, d = v.shape
+    w = np.random.default_rng(1).standard_normal((col.size, H)).astype(np.float32)
+    for tdt, name in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        wt, xt = torch.from_numpy(w).to(tdt), torch.from_numpy(v).to(tdt)
+        got = oracle.aggregate(rp, col, n, H, d, name, wt, xt, normalize=True)
+        want = oracle.aggregate(rp, col, n, H, d, "f32", wt.float().numpy(), xt.float().numpy(), normalize=True)
+        assert np.array_equal(got, want)
+
+
 def test_decode_f16_all_bit_patterns():
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     got = oracle.decode("f16", bits)
