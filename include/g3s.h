@@ -213,6 +213,25 @@ g3s_status g3s_forward(const g3s_plan *plan, const void *Q, const void *K, const
                        const void *Eproj, void *O, void *Eout, g3s_stream_t stream);
 
 /*
+ * Weighted aggregation over the plan's graph, enqueued on `stream`:
+ *   O_i^h = sum_e W[e][h] * X[col_idx[e]][h][:]                 normalize = 0
+ *   O_i^h = sum_e W[e][h] * X[...][h][:] / (sum_e W[e][h] + eps) normalize = 1
+ * over the CSR entries e of row i: the normalised scatter-add of the Triton
+ * article (stondelli.it/articles/gattn-triton, "Optimizing the scatter add in
+ * Triton" and "Using the CSC index for fast edge lookup") and the CSR weighted
+ * aggregation of the POPCORNBENCH task (normalize = 0).  Rows without edges
+ * give 0.
+ *   W  device [E][H] weights in the plan's dtype, indexed by CSR position
+ *   X  device [N][H][d] features in the plan's dtype
+ *   O  device [N][H][d] output in the plan's out_dtype (fully overwritten)
+ * Works with a plan of either variant (it needs only the graph, H, d and
+ * dtype) and uses its workspace, so it must not overlap another call on the
+ * same plan.  INVALID_ARG for NULL or misaligned pointers or eps < 0.
+ */
+g3s_status g3s_aggregate(const g3s_plan *plan, const void *W, const void *X, void *O, int normalize, float eps,
+                         g3s_stream_t stream);
+
+/*
  * Bytes of device staging g3s_forward_host needs for this plan: room for
  * Q, K, V, O (and Eproj, Eout for RTMScore), each 256-byte aligned.
  */

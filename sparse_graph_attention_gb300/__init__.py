@@ -87,7 +87,7 @@ _lib = None
 EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_options_init",
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
             "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
-            "g3s_forward_noalloc", "g3s_forward_check"]
+            "g3s_forward_noalloc", "g3s_forward_check", "g3s_aggregate"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -123,6 +123,8 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_forward_noalloc.restype = I
         lib.g3s_forward_check.argtypes = [P, P]
         lib.g3s_forward_check.restype = I
+        lib.g3s_aggregate.argtypes = [P, P, P, P, I, ctypes.c_float, P]
+        lib.g3s_aggregate.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -320,6 +322,22 @@ class Plan:
         with torch.cuda.device(self.device):
             _check(self._lib.g3s_forward(self.handle, q, k, v, e, o, eo, _stream_handle(stream)))
         return (O, Eout) if want_eout else O
+
+    def aggregate(self, W, X, O=None, normalize: bool = False, eps: float = 1e-6, stream=None):
+        """``g3s_aggregate``: O_i = sum_e W[e] X[src(e)] (optionally / (sum_e W[e] + eps))."""
+        torch = _torch()
+        tdt = torch_dtype(self.dtype)
+        odt = torch_dtype(self.out_dtype)
+        nn = self._node_numel()
+        w = _dev_ptr(W, "W", tdt, self.num_edges * self.heads, self.device) if self.num_edges else None
+        x = _dev_ptr(X, "X", tdt, nn, self.device)
+        if O is None:
+            O = torch.empty((self.num_nodes, self.heads, self.head_dim), dtype=odt, device=self.device)
+        o = _dev_ptr(O, "O", odt, nn, self.device)
+        with torch.cuda.device(self.device):
+            _check(self._lib.g3s_aggregate(self.handle, w, x, o, 1 if normalize else 0, float(eps),
+                                           _stream_handle(stream)))
+        return O
 
     def check(self, stream=None):
         """``g3s_forward_check``: synchronise and raise G3SError(G3S_ERR_TIMEOUT)

@@ -369,6 +369,8 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
 
     const int esz = dtype_size(p->dtype);
     CoreParams cp;
+    cp.W = nullptr;
+    cp.normalize = 0;
     cp.row_ptr = p->row_ptr;
     cp.col_idx = p->col_idx;
     cp.Q = Q;
@@ -422,7 +424,67 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         mp.H = s.H;
         mp.D = s.D;
         mp.eps = p->opts.rtm_epsilon;
+        mp.normalize = 1;
         CUDA_OR_FAIL(merge_launch(p->opts.out_dtype, rtm, mp, stream), "merge kernel launch");
+    }
+    return G3S_OK;
+}
+
+g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* O, int normalize, float eps,
+                         g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    const PlanShape& s = p->shape;
+    const int esz = dtype_size(p->dtype);
+    if (s.N > 0 && (!X || !O)) return fail(G3S_ERR_INVALID_ARG, "X and O must be non-NULL");
+    if (s.E > 0 && !W) return fail(G3S_ERR_INVALID_ARG, "W must be non-NULL when the graph has edges");
+    if (!aligned16(X) || !aligned16(O) || (reinterpret_cast<uintptr_t>(W) % esz))
+        return fail(G3S_ERR_INVALID_ARG, "X and O must be 16-byte aligned, W aligned to its element size");
+    if (!(eps >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "eps must be >= 0");
+    int dev = -1;
+    CUDA_OR_FAIL(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != p->device) return fail(G3S_ERR_INVALID_ARG, "plan was built on device %d, current is %d", p->device, dev);
+    if (s.N == 0) return G3S_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    CoreParams cp;
+    cp.row_ptr = p->row_ptr;
+    cp.col_idx = p->col_idx;
+    cp.Q = nullptr;
+    cp.K = nullptr;
+    cp.V = X;
+    cp.E = nullptr;
+    cp.W = W;
+    cp.O = O;
+    cp.Eout = nullptr;
+    cp.chunks = p->arr.chunks;
+    cp.part_acc = p->arr.part_acc;
+    cp.part_ml = p->arr.part_ml;
+    cp.win_flags = nullptr;  // every row, including tile-path windows
+    cp.work_counter = p->arr.work_counter;
+    cp.N = s.N;
+    cp.n_chunks = p->counts.n_chunks;
+    cp.H = s.H;
+    cp.D = s.D;
+    cp.heavy_threshold = s.heavy_threshold;
+    cp.row_vecs = s.H * s.D * esz / 16;
+    cp.lph = s.D * esz / 16;
+    cp.qscale = 0.f;
+    cp.eps = eps;
+    cp.elementwise_clamp = 0;
+    cp.normalize = normalize ? 1 : 0;
+    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, cp, stream), "aggregation kernel launch");
+    if (p->counts.n_chunks > 0) {
+        MergeParams mp;
+        mp.heavy_rows = p->arr.heavy_rows;
+        mp.heavy_chunk_ptr = p->arr.heavy_chunk_ptr;
+        mp.part_acc = p->arr.part_acc;
+        mp.part_ml = p->arr.part_ml;
+        mp.O = O;
+        mp.n_heavy = p->counts.n_heavy;
+        mp.H = s.H;
+        mp.D = s.D;
+        mp.eps = eps;
+        mp.normalize = normalize ? 1 : 0;
+        CUDA_OR_FAIL(merge_launch(p->opts.out_dtype, true, mp, stream), "merge kernel launch");
     }
     return G3S_OK;
 }

@@ -10,22 +10,22 @@ bool core_supported(int dtype, int row_vecs) {
     return true;
 }
 
-cudaError_t core_launch(int dtype, int out_dtype, bool rtm, const CoreParams& p, cudaStream_t st) {
+cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st) {
     const bool out_f32 = out_dtype == 0;
     if (!out_f32 && out_dtype != dtype) return cudaErrorInvalidValue;
     switch (dtype) {
-        case 0: return core_launch_f32(true, rtm, p, st);
-        case 1: return core_launch_f16(out_f32, rtm, p, st);
-        case 2: return core_launch_bf16(out_f32, rtm, p, st);
+        case 0: return core_launch_f32(true, mode, p, st);
+        case 1: return core_launch_f16(out_f32, mode, p, st);
+        case 2: return core_launch_bf16(out_f32, mode, p, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t merge_launch(int out_dtype, bool rtm, const MergeParams& p, cudaStream_t st) {
+cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st) {
     switch (out_dtype) {
-        case 0: return merge_launch_f32(rtm, p, st);
-        case 1: return merge_launch_f16(rtm, p, st);
-        case 2: return merge_launch_bf16(rtm, p, st);
+        case 0: return merge_launch_f32(plain, p, st);
+        case 1: return merge_launch_f16(plain, p, st);
+        case 2: return merge_launch_bf16(plain, p, st);
         default: return cudaErrorInvalidValue;
     }
 }

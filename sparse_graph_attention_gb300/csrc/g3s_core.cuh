@@ -29,6 +29,9 @@ namespace g3s {
 namespace core_detail {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kModeStd = 0;  // softmax(<q,k>/sqrt d)
+constexpr int kModeRtm = 1;  // RTMScore edge-modulated form
+constexpr int kModeAgg = 2;  // weighted aggregation with given weights
 constexpr float kNegBig = -1e30f;  // finite start of the running max
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -49,6 +52,7 @@ struct Vec<float> {
                           __float_as_uint(f[3]));
     }
     __device__ static void store1(void* base, long long i, float x) { static_cast<float*>(base)[i] = x; }
+    __device__ static float load1(const void* base, long long i) { return __ldg(static_cast<const float*>(base) + i); }
     __device__ static void to_float2(const uint4& r, float2 (&f)[2]) {
         f[0] = make_float2(__uint_as_float(r.x), __uint_as_float(r.y));
         f[1] = make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
@@ -79,6 +83,10 @@ struct Vec<__nv_bfloat16> {
     }
     __device__ static void store1(void* base, long long i, float x) {
         static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+    }
+    __device__ static float load1(const void* base, long long i) {
+        const unsigned short b = __ldg(static_cast<const unsigned short*>(base) + i);
+        return __uint_as_float((uint32_t)b << 16);
     }
     // element 2k is the low half of word k
     __device__ static void to_float2(const uint4& r, float2 (&f)[4]) {
@@ -115,6 +123,9 @@ struct Vec<__half> {
     }
     __device__ static void store1(void* base, long long i, float x) {
         static_cast<__half*>(base)[i] = __float2half_rn(x);
+    }
+    __device__ static float load1(const void* base, long long i) {
+        return __half2float(__ldg(static_cast<const __half*>(base) + i));
     }
     __device__ static void to_float2(const uint4& r, float2 (&f)[4]) {
         f[0] = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
@@ -190,12 +201,14 @@ struct ItemState {
 // One step of S = G * U edges starting at CSR position `base`.  TAIL: the
 // step runs past the row's end; slots beyond it re-read the row's last edge
 // (a valid, cached address) and get weight 0, so no load is branched.
-template <bool TAIL, typename T, typename OutT, int NV, bool RTM, int VP>
+template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP>
 __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
                                           const int e1) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    constexpr bool RTM = MODE == kModeRtm;
+    constexpr bool AGG = MODE == kModeAgg;
     const int rv = L.rv, g = L.g, lph = L.lph;
     const int S = L.G * U;
     if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
@@ -224,15 +237,20 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
 
     const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
     const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
-    uint4 kr[U][NV], vr[U][NV];
+    uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
     uint4 er[RTM ? U : 1][RTM ? NV : 1];
+    float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const long long o = (long long)src[u] * rv;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            kr[u][j] = ldg16(K4 + o + 32 * j);
+            if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
             vr[u][j] = ldg16(V4 + o + 32 * j);
+            if constexpr (AGG) {
+                const int e = ok[u] ? base + g * U + u : e1 - 1;
+                wg[u][j] = Vec<T>::load1(p.W, (long long)e * p.H + (L.sub + 32 * j) / lph);
+            }
             if constexpr (RTM) {
                 const int e = ok[u] ? base + g * U + u : e1 - 1;
                 er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)e * rv + 32 * j);
@@ -245,6 +263,10 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
     for (int u = 0; u < U; ++u) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
+            if constexpr (AGG) {
+                lg[u][j] = 0.f;
+                continue;
+            }
             float2 kf[VP];
             VT::to_float2(kr[u][j], kf);
             float s;
@@ -281,7 +303,10 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
         float w[U];
-        if constexpr (RTM) {
+        if constexpr (AGG) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = ok[u] ? wg[u][j] : 0.f;
+        } else if constexpr (RTM) {
 #pragma unroll
             for (int u = 0; u < U; ++u) w[u] = ok[u] ? ex2(clamp5(lg[u][j]) * kLog2e) : 0.f;
         } else {
@@ -317,13 +342,14 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
 // this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
 // otherwise normalise and write O.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, bool RTM>
+template <typename T, typename OutT, int NV, int MODE>
 __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
                                              const int e1, const long long chunk) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;  // elements per 16-byte vector
     constexpr int VP = VE / 2;
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    constexpr bool PLAIN = MODE != kModeStd;  // weights need no running max
     const int rv = L.rv, g = L.g, sub = L.sub, lph = L.lph;
     const int S = L.G * U;
 
@@ -335,10 +361,10 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
     const float2 qs = make_float2(p.qscale, p.qscale);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-        VT::to_float2(ldg16(Q4 + (long long)row * rv + sub + 32 * j), st.q[j]);
+        if constexpr (MODE != kModeAgg) VT::to_float2(ldg16(Q4 + (long long)row * rv + sub + 32 * j), st.q[j]);
 #pragma unroll
         for (int k = 0; k < VP; ++k) {
-            st.q[j][k] = __fmul2_rn(st.q[j][k], qs);
+            if constexpr (MODE != kModeAgg) st.q[j][k] = __fmul2_rn(st.q[j][k], qs);
             st.acc[j][k] = make_float2(0.f, 0.f);
         }
         st.m[j] = kNegBig;
@@ -346,14 +372,14 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
     }
 
     const int full_end = e0 + ((e1 - e0) & ~(S - 1));  // S is a power of two
-    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, RTM, VP>(p, L, st, base, e1);
-    if (full_end < e1) edge_step<true, T, OutT, NV, RTM, VP>(p, L, st, full_end, e1);
+    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, MODE, VP>(p, L, st, base, e1);
+    if (full_end < e1) edge_step<true, T, OutT, NV, MODE, VP>(p, L, st, full_end, e1);
 
     // merge the lane groups (fixed butterfly order)
     for (int off = L.gsize; off < 32; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            if constexpr (RTM) {
+            if constexpr (PLAIN) {
                 st.l[j] += __shfl_xor_sync(kFull, st.l[j], off);
 #pragma unroll
                 for (int k = 0; k < VP; ++k) {
@@ -399,8 +425,10 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             float inv;
-            if constexpr (RTM)
+            if constexpr (MODE == kModeRtm)
                 inv = 1.0f / (st.l[j] + p.eps);
+            else if constexpr (MODE == kModeAgg)
+                inv = p.normalize ? 1.0f / (st.l[j] + p.eps) : 1.0f;
             else
                 inv = st.l[j] > 0.f ? 1.0f / st.l[j] : 0.f;
             float o[VE];
@@ -425,8 +453,9 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 // L2 keeps serving the sources near them).  Each item's result depends only
 // on its own data, so the dynamic order does not change any output.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, bool RTM>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (RTM ? 3 : 4) : 1) core_kernel(const CoreParams p) {
+template <typename T, typename OutT, int NV, int MODE>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : 1)
+    core_kernel(const CoreParams p) {
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
     const unsigned long long total = n_chunks + (unsigned long long)p.N;
@@ -439,13 +468,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (RTM ? 3 : 4) : 1
         for (unsigned long long it = first; it < last; ++it) {
             if (it < n_chunks) {
                 const int32_t* c = p.chunks + 3 * it;
-                process_item<T, OutT, NV, RTM>(p, L, c[0], c[1], c[2], (long long)it);
+                process_item<T, OutT, NV, MODE>(p, L, c[0], c[1], c[2], (long long)it);
             } else {
                 const int row = (int)(it - n_chunks);
                 const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
                 if (e1 - e0 > p.heavy_threshold) continue;  // done by chunks + merge
                 if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) continue;  // tile path
-                process_item<T, OutT, NV, RTM>(p, L, row, e0, e1, -1);
+                process_item<T, OutT, NV, MODE>(p, L, row, e0, e1, -1);
             }
         }
     }
@@ -456,7 +485,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (RTM ? 3 : 4) : 1
 // ascending order (m = max m_c, l = sum l_c 2^(m_c - m), O = sum acc_c 2^(m_c - m) / l;
 // RTMScore: plain sums, epsilon added once).
 // ---------------------------------------------------------------------------
-template <typename OutT, bool RTM>
+template <typename OutT, bool PLAIN>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergeParams p) {
     const int lane = threadIdx.x & 31;
     const long long k = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
@@ -467,13 +496,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
     for (int x = lane; x < HD; x += 32) {
         const int h = x / p.D;
         float o;
-        if constexpr (RTM) {
+        if constexpr (PLAIN) {
             float a = 0.f, s = 0.f;
             for (int c = c0; c < c1; ++c) {
                 a += p.part_acc[(long long)c * HD + x];
                 s += p.part_ml[((long long)c * p.H + h) * 2 + 1];
             }
-            o = a / (s + p.eps);
+            o = p.normalize ? a / (s + p.eps) : a;
         } else {
             float mx = kNegBig;
             for (int c = c0; c < c1; ++c) mx = fmaxf(mx, p.part_ml[((long long)c * p.H + h) * 2]);
@@ -491,7 +520,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
-template <typename T, typename OutT, int NV, bool RTM>
+template <typename T, typename OutT, int NV, int MODE>
 cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
     const long long items = p.n_chunks + p.N;
     if (items <= 0) return cudaSuccess;
@@ -504,7 +533,7 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, RTM>, kWarpsPerCta * 32, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE>, kWarpsPerCta * 32, 0);
         if (e != cudaSuccess) return e;
         cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
         cached_dev = dev;
@@ -513,27 +542,37 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
     const int ctas = (int)(need < cached_ctas ? need : cached_ctas);
     e = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned long long), st);
     if (e != cudaSuccess) return e;
-    core_kernel<T, OutT, NV, RTM><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
+    core_kernel<T, OutT, NV, MODE><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 
-template <typename T, typename OutT, bool RTM>
+template <typename T, typename OutT, int MODE>
 cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
     const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
     switch (nv) {
-        case 1: return launch_core_nv<T, OutT, 1, RTM>(p, st);
-        case 2: return launch_core_nv<T, OutT, 2, RTM>(p, st);
-        case 4: return launch_core_nv<T, OutT, 4, RTM>(p, st);
-        case 8: return launch_core_nv<T, OutT, 8, RTM>(p, st);
+        case 1: return launch_core_nv<T, OutT, 1, MODE>(p, st);
+        case 2: return launch_core_nv<T, OutT, 2, MODE>(p, st);
+        case 4: return launch_core_nv<T, OutT, 4, MODE>(p, st);
+        case 8: return launch_core_nv<T, OutT, 8, MODE>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, typename OutT>
+cudaError_t launch_core_mode(int mode, const CoreParams& p, cudaStream_t st) {
+    switch (mode) {
+        case kModeStd: return launch_core<T, OutT, kModeStd>(p, st);
+        case kModeRtm: return launch_core<T, OutT, kModeRtm>(p, st);
+        case kModeAgg: return launch_core<T, OutT, kModeAgg>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename OutT>
-cudaError_t launch_merge(bool rtm, const MergeParams& p, cudaStream_t st) {
+cudaError_t launch_merge(bool plain, const MergeParams& p, cudaStream_t st) {
     if (p.n_heavy <= 0) return cudaSuccess;
     dim3 grid((unsigned)((p.n_heavy + kWarpsPerCta - 1) / kWarpsPerCta)), block(kWarpsPerCta * 32);
-    if (rtm)
+    if (plain)
         merge_kernel<OutT, true><<<grid, block, 0, st>>>(p);
     else
         merge_kernel<OutT, false><<<grid, block, 0, st>>>(p);

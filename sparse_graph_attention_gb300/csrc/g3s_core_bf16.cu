@@ -4,14 +4,14 @@
 
 namespace g3s {
 
-cudaError_t core_launch_bf16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st) {
+cudaError_t core_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st) {
     using namespace core_detail;
-    if (out_f32) return rtm ? launch_core<__nv_bfloat16, float, true>(p, st) : launch_core<__nv_bfloat16, float, false>(p, st);
-    return rtm ? launch_core<__nv_bfloat16, __nv_bfloat16, true>(p, st) : launch_core<__nv_bfloat16, __nv_bfloat16, false>(p, st);
+    if (out_f32) return launch_core_mode<__nv_bfloat16, float>(mode, p, st);
+    return launch_core_mode<__nv_bfloat16, __nv_bfloat16>(mode, p, st);
 }
 
-cudaError_t merge_launch_bf16(bool rtm, const MergeParams& p, cudaStream_t st) {
-    return core_detail::launch_merge<__nv_bfloat16>(rtm, p, st);
+cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st) {
+    return core_detail::launch_merge<__nv_bfloat16>(plain, p, st);
 }
 
 }  // namespace g3s

@@ -4,14 +4,14 @@
 
 namespace g3s {
 
-cudaError_t core_launch_f16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st) {
+cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st) {
     using namespace core_detail;
-    if (out_f32) return rtm ? launch_core<__half, float, true>(p, st) : launch_core<__half, float, false>(p, st);
-    return rtm ? launch_core<__half, __half, true>(p, st) : launch_core<__half, __half, false>(p, st);
+    if (out_f32) return launch_core_mode<__half, float>(mode, p, st);
+    return launch_core_mode<__half, __half>(mode, p, st);
 }
 
-cudaError_t merge_launch_f16(bool rtm, const MergeParams& p, cudaStream_t st) {
-    return core_detail::launch_merge<__half>(rtm, p, st);
+cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st) {
+    return core_detail::launch_merge<__half>(plain, p, st);
 }
 
 }  // namespace g3s

@@ -4,14 +4,14 @@
 
 namespace g3s {
 
-cudaError_t core_launch_f32(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st) {
+cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st) {
     using namespace core_detail;
     (void)out_f32;
-    return rtm ? launch_core<float, float, true>(p, st) : launch_core<float, float, false>(p, st);
+    return launch_core_mode<float, float>(mode, p, st);
 }
 
-cudaError_t merge_launch_f32(bool rtm, const MergeParams& p, cudaStream_t st) {
-    return core_detail::launch_merge<float>(rtm, p, st);
+cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st) {
+    return core_detail::launch_merge<float>(plain, p, st);
 }
 
 }  // namespace g3s

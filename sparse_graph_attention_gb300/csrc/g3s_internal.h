@@ -95,6 +95,7 @@ struct CoreParams {
     const void* K;
     const void* V;
     const void* E;
+    const void* W;  // aggregation weights [E][H] (input type), mode 2 only
     void* O;
     void* Eout;
     const int32_t* chunks;
@@ -111,6 +112,7 @@ struct CoreParams {
     float qscale;  // standard: log2(e)/sqrt(d); RTMScore: 1/sqrt(d)
     float eps;
     int elementwise_clamp;
+    int normalize;  // aggregation: divide by (sum of weights + eps)
 };
 
 struct MergeParams {
@@ -122,19 +124,21 @@ struct MergeParams {
     int n_heavy;
     int H, D;
     float eps;
+    int normalize;  // plain (RTMScore / aggregation) merges: divide by (sum + eps)
 };
 
 // dtype / out_dtype: 0 f32, 1 f16, 2 bf16; out_dtype is f32 or the input dtype.
+// mode: 0 standard softmax, 1 RTMScore, 2 weighted aggregation.
 // Launchers return cudaErrorInvalidValue for shapes without a kernel.
 bool core_supported(int dtype, int row_vecs);
-cudaError_t core_launch(int dtype, int out_dtype, bool rtm, const CoreParams& p, cudaStream_t st);
-cudaError_t merge_launch(int out_dtype, bool rtm, const MergeParams& p, cudaStream_t st);
-cudaError_t core_launch_f32(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
-cudaError_t core_launch_f16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
-cudaError_t core_launch_bf16(bool out_f32, bool rtm, const CoreParams& p, cudaStream_t st);
-cudaError_t merge_launch_f32(bool rtm, const MergeParams& p, cudaStream_t st);
-cudaError_t merge_launch_f16(bool rtm, const MergeParams& p, cudaStream_t st);
-cudaError_t merge_launch_bf16(bool rtm, const MergeParams& p, cudaStream_t st);
+cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st);
+cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st);
+cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st);
+cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st);
 
 // ---- tensor-core tile kernel (g3s_tile.cu) -------------------------------
 struct TileParams {

@@ -117,6 +117,8 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     // the fused forward, heavy-row partials in the static scratch
     const int esz = dtype_size(dtype);
     CoreParams cp;
+    cp.W = nullptr;
+    cp.normalize = 0;
     cp.row_ptr = row_ptr_d;
     cp.col_idx = col_idx_d;
     cp.Q = Q;
@@ -153,6 +155,7 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
         mp.H = s.H;
         mp.D = s.D;
         mp.eps = o.rtm_epsilon;
+        mp.normalize = 1;
         NOALLOC_CUDA(merge_launch(o.out_dtype, rtm, mp, stream), "merge kernel launch");
     }
     return G3S_OK;
