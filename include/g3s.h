@@ -185,6 +185,22 @@ g3s_status g3s_plan_create(const int32_t *row_ptr_d, const int32_t *col_idx_d, i
                            g3s_variant variant, const g3s_plan_options *opts, void *workspace_d,
                            size_t workspace_bytes, g3s_stream_t stream, g3s_plan **out);
 
+/*
+ * Attach a physical edge numbering to the plan, as the Triton article's CSC
+ * index does with its position-to-edge-id vector (stondelli.it/articles/
+ * gattn-triton, "Using the CSC index for fast edge lookup"): edge features
+ * live in their own storage order and several sparse indices can share them.
+ *   edge_id_d       device int32 [E]: CSR position e -> slot in [0, num_edge_slots);
+ *                   must outlive the plan.  NULL restores CSR-position indexing.
+ *   num_edge_slots  rows of the edge arrays (Eproj, Eout and the aggregation W)
+ * From then on g3s_forward reads Eproj[edge_id[e]] and writes
+ * Eout[edge_id[e]] (RTMScore), g3s_aggregate reads W[edge_id[e]], and the
+ * host staging holds num_edge_slots edge rows.  Validates every id on the
+ * device (synchronises `stream`): BAD_GRAPH when one is out of range.
+ */
+g3s_status g3s_plan_set_edge_ids(g3s_plan *plan, const int32_t *edge_id_d, int64_t num_edge_slots,
+                                 g3s_stream_t stream);
+
 /* Sizes and counts of a plan. */
 g3s_status g3s_plan_get_stats(const g3s_plan *plan, g3s_plan_stats *stats);
 
@@ -201,6 +217,7 @@ g3s_status g3s_plan_export(const g3s_plan *plan, g3s_plan_array which, void *hos
  * One fused forward pass over the whole graph, enqueued on `stream`.
  *   Q, K, V  device [N][H][d] inputs
  *   Eproj    device [E][H][d] edge projections; RTMScore only, else NULL
+ *            ([slots][H][d] in physical edge order after g3s_plan_set_edge_ids)
  *   O        device [N][H][d] output in out_dtype (fully overwritten)
  *   Eout     device [E][H][d] updated edge features in out_dtype (RTMScore;
  *            NULL skips the store)
@@ -256,6 +273,15 @@ g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K
  * outputs of that forward are incomplete.  G3S_OK otherwise.
  */
 g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
+
+/*
+ * Self-test of the device-side timeout path: launches one CTA that waits, with
+ * the same bounded wait the tile kernel uses, on an mbarrier that nothing ever
+ * completes; after limit_ns (at most 2 s) it gives up and sets the plan's
+ * status word.  Then behaves as g3s_forward_check: synchronises `stream` and
+ * returns G3S_ERR_TIMEOUT, clearing the flag.  The context stays usable.
+ */
+g3s_status g3s_selftest_wait_timeout(const g3s_plan *plan, uint64_t limit_ns, g3s_stream_t stream);
 
 /* Release the plan's host struct (the caller still owns the workspace). NULL is a no-op. */
 void g3s_plan_destroy(g3s_plan *plan);

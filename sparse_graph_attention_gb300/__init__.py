@@ -87,7 +87,8 @@ _lib = None
 EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_options_init",
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
             "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
-            "g3s_forward_noalloc", "g3s_forward_check", "g3s_aggregate"]
+            "g3s_forward_noalloc", "g3s_forward_check", "g3s_aggregate", "g3s_selftest_wait_timeout",
+            "g3s_plan_set_edge_ids"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -125,6 +126,10 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_forward_check.restype = I
         lib.g3s_aggregate.argtypes = [P, P, P, P, I, ctypes.c_float, P]
         lib.g3s_aggregate.restype = I
+        lib.g3s_selftest_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
+        lib.g3s_selftest_wait_timeout.restype = I
+        lib.g3s_plan_set_edge_ids.argtypes = [P, P, I64, P]
+        lib.g3s_plan_set_edge_ids.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -257,6 +262,18 @@ class Plan:
                                        ctypes.byref(h)))
         self._handle = h
         self.row_ptr, self.col_idx = row_ptr, col_idx
+        self.edge_slots = self.num_edges
+        self.edge_id = None
+
+    def set_edge_ids(self, edge_id, num_edge_slots: int, stream=None):
+        """``g3s_plan_set_edge_ids``: CSR position -> physical edge slot (None to clear)."""
+        torch = _torch()
+        ptr = _dev_ptr(edge_id, "edge_id", torch.int32, self.num_edges, self.device) if edge_id is not None else None
+        with torch.cuda.device(self.device):
+            _check(self._lib.g3s_plan_set_edge_ids(self.handle, ptr, int(num_edge_slots) if edge_id is not None else 0,
+                                                   _stream_handle(stream)))
+        self.edge_id = edge_id
+        self.edge_slots = int(num_edge_slots) if edge_id is not None else self.num_edges
 
     # -- lifetime -----------------------------------------------------------
     def close(self):
@@ -303,7 +320,7 @@ class Plan:
         tdt = torch_dtype(self.dtype)
         odt = torch_dtype(self.out_dtype)
         nn = self._node_numel()
-        ne = self.num_edges * self.heads * self.head_dim
+        ne = self.edge_slots * self.heads * self.head_dim
         q = _dev_ptr(Q, "Q", tdt, nn, self.device)
         k = _dev_ptr(K, "K", tdt, nn, self.device)
         v = _dev_ptr(V, "V", tdt, nn, self.device)
@@ -314,7 +331,7 @@ class Plan:
         if self.variant == "rtmscore":
             e = _dev_ptr(E, "E", tdt, ne, self.device) if self.num_edges else None
             if want_eout and Eout is None:
-                Eout = torch.empty((self.num_edges, self.heads, self.head_dim), dtype=odt, device=self.device)
+                Eout = torch.empty((self.edge_slots, self.heads, self.head_dim), dtype=odt, device=self.device)
             if Eout is not None:
                 eo = _dev_ptr(Eout, "Eout", odt, ne, self.device)
         elif E is not None or Eout is not None:
@@ -329,7 +346,7 @@ class Plan:
         tdt = torch_dtype(self.dtype)
         odt = torch_dtype(self.out_dtype)
         nn = self._node_numel()
-        w = _dev_ptr(W, "W", tdt, self.num_edges * self.heads, self.device) if self.num_edges else None
+        w = _dev_ptr(W, "W", tdt, self.edge_slots * self.heads, self.device) if self.num_edges else None
         x = _dev_ptr(X, "X", tdt, nn, self.device)
         if O is None:
             O = torch.empty((self.num_nodes, self.heads, self.head_dim), dtype=odt, device=self.device)
@@ -358,7 +375,7 @@ class Plan:
         tdt = torch_dtype(self.dtype)
         odt = torch_dtype(self.out_dtype)
         nn = self._node_numel()
-        ne = self.num_edges * self.heads * self.head_dim
+        ne = self.edge_slots * self.heads * self.head_dim
         if staging is None:
             staging = torch.empty(self.staging_size(), dtype=torch.uint8, device=self.device)
         ptrs = [_host_ptr(Qh, "Q", tdt, nn), _host_ptr(Kh, "K", tdt, nn), _host_ptr(Vh, "V", tdt, nn)]

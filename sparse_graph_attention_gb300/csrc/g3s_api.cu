@@ -183,6 +183,8 @@ struct g3s_plan {
     const int32_t* row_ptr;
     const int32_t* col_idx;
     size_t ws_used;
+    const int32_t* edge_id;  // optional CSR position -> physical edge slot
+    long long edge_slots;    // rows of E / Eout / W (E without edge ids)
 };
 
 extern "C" {
@@ -288,6 +290,8 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
     p->row_ptr = row_ptr_d;
     p->col_idx = col_idx_d;
     p->ws_used = need;
+    p->edge_id = nullptr;
+    p->edge_slots = num_edges;
     *out = p;
     return G3S_OK;
 }
@@ -371,6 +375,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     CoreParams cp;
     cp.W = nullptr;
     cp.normalize = 0;
+    cp.edge_id = p->edge_id;
     cp.row_ptr = p->row_ptr;
     cp.col_idx = p->col_idx;
     cp.Q = Q;
@@ -436,7 +441,7 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     const PlanShape& s = p->shape;
     const int esz = dtype_size(p->dtype);
     if (s.N > 0 && (!X || !O)) return fail(G3S_ERR_INVALID_ARG, "X and O must be non-NULL");
-    if (s.E > 0 && !W) return fail(G3S_ERR_INVALID_ARG, "W must be non-NULL when the graph has edges");
+    if (p->edge_slots > 0 && s.E > 0 && !W) return fail(G3S_ERR_INVALID_ARG, "W must be non-NULL when the graph has edges");
     if (!aligned16(X) || !aligned16(O) || (reinterpret_cast<uintptr_t>(W) % esz))
         return fail(G3S_ERR_INVALID_ARG, "X and O must be 16-byte aligned, W aligned to its element size");
     if (!(eps >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "eps must be >= 0");
@@ -453,6 +458,7 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     cp.V = X;
     cp.E = nullptr;
     cp.W = W;
+    cp.edge_id = p->edge_id;
     cp.O = O;
     cp.Eout = nullptr;
     cp.chunks = p->arr.chunks;
@@ -494,8 +500,8 @@ g3s_status g3s_host_staging_size(const g3s_plan* p, size_t* bytes) {
     const size_t hd = (size_t)p->shape.H * p->shape.D;
     const size_t node = (size_t)p->shape.N * hd * dtype_size(p->dtype);
     const size_t node_out = (size_t)p->shape.N * hd * dtype_size(p->opts.out_dtype);
-    const size_t edge = (size_t)p->shape.E * hd * dtype_size(p->dtype);
-    const size_t edge_out = (size_t)p->shape.E * hd * dtype_size(p->opts.out_dtype);
+    const size_t edge = (size_t)p->edge_slots * hd * dtype_size(p->dtype);
+    const size_t edge_out = (size_t)p->edge_slots * hd * dtype_size(p->opts.out_dtype);
     auto up = [](size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); };
     size_t n = 3 * up(node) + up(node_out);
     if (p->variant == G3S_RTMSCORE) n += up(edge) + up(edge_out);
@@ -514,8 +520,8 @@ g3s_status g3s_forward_host(const g3s_plan* p, const void* Qh, const void* Kh, c
     const size_t hd = (size_t)p->shape.H * p->shape.D;
     const size_t node = (size_t)p->shape.N * hd * dtype_size(p->dtype);
     const size_t node_out = (size_t)p->shape.N * hd * dtype_size(p->opts.out_dtype);
-    const size_t edge = (size_t)p->shape.E * hd * dtype_size(p->dtype);
-    const size_t edge_out = (size_t)p->shape.E * hd * dtype_size(p->opts.out_dtype);
+    const size_t edge = (size_t)p->edge_slots * hd * dtype_size(p->dtype);
+    const size_t edge_out = (size_t)p->edge_slots * hd * dtype_size(p->opts.out_dtype);
     if (p->shape.N > 0 && (!Qh || !Kh || !Vh || !Oh)) return fail(G3S_ERR_INVALID_ARG, "host Q, K, V, O must be non-NULL");
     if (rtm && p->shape.E > 0 && !Eh) return fail(G3S_ERR_INVALID_ARG, "RTMScore plan needs host Eproj");
     if (!rtm && (Eh || Eouth)) return fail(G3S_ERR_INVALID_ARG, "Eproj / Eout are only valid for an RTMScore plan");
@@ -542,6 +548,29 @@ g3s_status g3s_forward_host(const g3s_plan* p, const void* Qh, const void* Kh, c
     return G3S_OK;
 }
 
+g3s_status g3s_plan_set_edge_ids(g3s_plan* p, const int32_t* edge_id_d, int64_t num_edge_slots,
+                                 g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    if (!edge_id_d) {
+        p->edge_id = nullptr;
+        p->edge_slots = p->shape.E;
+        return G3S_OK;
+    }
+    if (reinterpret_cast<uintptr_t>(edge_id_d) & 3u) return fail(G3S_ERR_INVALID_ARG, "edge ids must be 4-byte aligned");
+    if (num_edge_slots < 1 || num_edge_slots > 0x7fffffffLL)
+        return fail(G3S_ERR_INVALID_ARG, "num_edge_slots must be in [1, 2^31)");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    PlanCounts hc;
+    CUDA_OR_FAIL(cudaMemsetAsync(&p->arr.counts->status, 0, sizeof(int32_t), stream), "cudaMemsetAsync(status)");
+    CUDA_OR_FAIL(validate_edge_ids(edge_id_d, p->shape.E, num_edge_slots, p->arr.counts, stream), "edge id validation");
+    CUDA_OR_FAIL(cudaMemcpyAsync(&hc, p->arr.counts, sizeof hc, cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync(counts)");
+    CUDA_OR_FAIL(cudaStreamSynchronize(stream), "cudaStreamSynchronize(edge ids)");
+    if (hc.status & kErrEdgeId) return fail(G3S_ERR_BAD_GRAPH, "an edge id is outside [0, %lld)", (long long)num_edge_slots);
+    p->edge_id = edge_id_d;
+    p->edge_slots = num_edge_slots;
+    return G3S_OK;
+}
+
 g3s_status g3s_forward_check(const g3s_plan* p, g3s_stream_t stream_) {
     if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -554,6 +583,14 @@ g3s_status g3s_forward_check(const g3s_plan* p, g3s_stream_t stream_) {
         return fail(G3S_ERR_TIMEOUT, "a forward kernel's bounded device wait gave up; its outputs are incomplete");
     }
     return G3S_OK;
+}
+
+g3s_status g3s_selftest_wait_timeout(const g3s_plan* p, uint64_t limit_ns, g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return fail(G3S_ERR_INVALID_ARG, "limit_ns must be in (0, 2e9]");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    CUDA_OR_FAIL(wait_selftest_launch(limit_ns, p->arr.fwd_status, stream), "self-test launch");
+    return g3s_forward_check(p, stream_);
 }
 
 void g3s_plan_destroy(g3s_plan* p) { delete p; }

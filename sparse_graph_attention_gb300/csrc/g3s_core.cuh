@@ -237,6 +237,15 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
 
     const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
     const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
+    // physical slot of each edge's features (RTMScore) or weights (aggregation)
+    int eid[(RTM || AGG) ? U : 1];
+    if constexpr (RTM || AGG) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = ok[u] ? base + g * U + u : e1 - 1;
+            eid[u] = p.edge_id != nullptr ? __ldg(p.edge_id + e) : e;
+        }
+    }
     uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
     uint4 er[RTM ? U : 1][RTM ? NV : 1];
     float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
@@ -247,13 +256,9 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
         for (int j = 0; j < NV; ++j) {
             if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
             vr[u][j] = ldg16(V4 + o + 32 * j);
-            if constexpr (AGG) {
-                const int e = ok[u] ? base + g * U + u : e1 - 1;
-                wg[u][j] = Vec<T>::load1(p.W, (long long)e * p.H + (L.sub + 32 * j) / lph);
-            }
+            if constexpr (AGG) wg[u][j] = Vec<T>::load1(p.W, (long long)eid[u] * p.H + (L.sub + 32 * j) / lph);
             if constexpr (RTM) {
-                const int e = ok[u] ? base + g * U + u : e1 - 1;
-                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)e * rv + 32 * j);
+                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)eid[u] * rv + 32 * j);
             }
         }
     }
@@ -288,7 +293,7 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
                     s += uo[2 * k + 1];
                 }
                 if (p.Eout != nullptr && ok[u])
-                    Store<OutT, VE>::run(p.Eout, ((long long)(base + g * U + u) * rv + L.sub + 32 * j) * VE, uo);
+                    Store<OutT, VE>::run(p.Eout, ((long long)eid[u] * rv + L.sub + 32 * j) * VE, uo);
             } else {
                 float2 s2 = make_float2(0.f, 0.f);  // packed fp32 FMA
 #pragma unroll

@@ -21,6 +21,7 @@ enum : int32_t {
     kErrRowPtrEnd = 4,    // row_ptr[N] != E
     kErrColRange = 8,     // a source outside [0, N)
     kErrTimeout = 16,     // a bounded device-side wait gave up (forward status word)
+    kErrEdgeId = 32,      // an edge id outside [0, edge slots)
 };
 
 constexpr int kTileMaxTilesPerWindow = 32;  // tile-path windows have at most this many 16x8 tiles
@@ -86,6 +87,7 @@ cudaError_t plan_validate(const int32_t* row_ptr, const int32_t* col_idx, const 
                           const PlanArrays& a, cudaStream_t st);
 cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s,
                        const PlanArrays& a, cudaStream_t st);
+cudaError_t validate_edge_ids(const int32_t* edge_id, long long E, long long slots, PlanCounts* c, cudaStream_t st);
 
 // ---- CUDA-core fused kernel (g3s_core.cu) ---------------------------------
 struct CoreParams {
@@ -95,7 +97,8 @@ struct CoreParams {
     const void* K;
     const void* V;
     const void* E;
-    const void* W;  // aggregation weights [E][H] (input type), mode 2 only
+    const void* W;  // aggregation weights [slots][H] (input type), mode 2 only
+    const int32_t* edge_id;  // CSR position -> physical edge slot of E/Eout/W, or nullptr
     void* O;
     void* Eout;
     const int32_t* chunks;
@@ -157,6 +160,7 @@ struct TileParams {
     int32_t* status;   // kErrTimeout is OR-ed in when a wait gives up
 };
 bool tile_supported(int dtype, int variant, int head_dim);
+cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st);
 cudaError_t tile_launch(int dtype, int out_dtype, const TileParams& p, cudaStream_t st);
 
 // ---- host helpers shared by the ABI translation units (g3s_api.cu) ---------

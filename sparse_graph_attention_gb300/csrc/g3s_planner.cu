@@ -575,6 +575,21 @@ struct TileFlag {
 
 }  // namespace
 
+__global__ void k_validate_edge_ids(const int32_t* ids, long long E, long long slots, PlanCounts* c) {
+    int err = 0;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < E; e += (long long)gridDim.x * blockDim.x) {
+        const int v = ids[e];
+        if (v < 0 || (long long)v >= slots) err = kErrEdgeId;
+    }
+    if (err) atomicOr(&c->status, err);
+}
+
+cudaError_t validate_edge_ids(const int32_t* edge_id, long long E, long long slots, PlanCounts* c, cudaStream_t st) {
+    if (E <= 0) return cudaSuccess;
+    k_validate_edge_ids<<<grid_for(E, 256), 256, 0, st>>>(edge_id, E, slots, c);
+    return cudaGetLastError();
+}
+
 cudaError_t plan_validate(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s, const PlanArrays& a,
                           cudaStream_t st) {
     k_validate_rows<<<grid_for(s.N + 1, 256), 256, 0, st>>>(row_ptr, s.N, s.E, a.counts);

@@ -97,13 +97,14 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
     return t;
 }
-// bounded wait: false when the phase did not complete within kWaitLimitNs
-__device__ bool mbar_wait_bounded(unsigned long long* m, uint32_t parity) {
+// bounded wait: false when the phase did not complete within limit_ns
+__device__ bool mbar_wait_bounded(unsigned long long* m, uint32_t parity,
+                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(m, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait(m, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -464,6 +465,17 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Self-test of the bounded wait: one CTA waits on an mbarrier that nothing
+// arrives at, gives up after limit_ns, and reports it through *status the way
+// the tile kernel does.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int32_t* status) {
+    __shared__ unsigned long long mbar;
+    if (threadIdx.x == 0) mbar_init(&mbar, 1);
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(&mbar, 0, limit_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(status, kErrTimeout);
+}
+
 template <typename T, typename OutT>
 cudaError_t launch(const TileParams& p, cudaStream_t st) {
     if (p.n_tile_windows <= 0) return cudaSuccess;
@@ -477,6 +489,11 @@ cudaError_t launch(const TileParams& p, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
+}
 
 bool tile_supported(int dtype, int variant, int head_dim) {
     return (dtype == G3S_F16 || dtype == G3S_BF16) && variant == G3S_STANDARD && head_dim == kD;
