@@ -201,7 +201,7 @@ struct ItemState {
 // One step of S = G * U edges starting at CSR position `base`.  TAIL: the
 // step runs past the row's end; slots beyond it re-read the row's last edge
 // (a valid, cached address) and get weight 0, so no load is branched.
-template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP>
+template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
 __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
                                           const int e1) {
     using VT = Vec<T>;
@@ -209,7 +209,7 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
     constexpr bool RTM = MODE == kModeRtm;
     constexpr bool AGG = MODE == kModeAgg;
-    const int rv = L.rv, g = L.g, lph = L.lph;
+    const int rv = L.rv, g = L.g, lph = LPH > 0 ? LPH : L.lph;
     const int S = L.G * U;
     if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
         st.cbase += 64;
@@ -300,7 +300,12 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
                 for (int k = 0; k < VP; ++k) s2 = __ffma2_rn(st.q[j][k], kf[k], s2);
                 s = s2.x + s2.y;
             }
-            for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
+            if constexpr (LPH > 0) {  // lanes per head known at compile time
+#pragma unroll
+                for (int o2 = 1; o2 < LPH; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
+            } else {
+                for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
+            }
             lg[u][j] = s;
         }
     }
@@ -347,7 +352,7 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
 // this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
 // otherwise normalise and write O.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, int MODE>
+template <typename T, typename OutT, int NV, int MODE, int LPH>
 __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
                                              const int e1, const long long chunk) {
     using VT = Vec<T>;
@@ -355,7 +360,7 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
     constexpr int VP = VE / 2;
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
     constexpr bool PLAIN = MODE != kModeStd;  // weights need no running max
-    const int rv = L.rv, g = L.g, sub = L.sub, lph = L.lph;
+    const int rv = L.rv, g = L.g, sub = L.sub, lph = LPH > 0 ? LPH : L.lph;
     const int S = L.G * U;
 
     ItemState<NV, VP> st;
@@ -377,8 +382,8 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
     }
 
     const int full_end = e0 + ((e1 - e0) & ~(S - 1));  // S is a power of two
-    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, MODE, VP>(p, L, st, base, e1);
-    if (full_end < e1) edge_step<true, T, OutT, NV, MODE, VP>(p, L, st, full_end, e1);
+    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, MODE, VP, LPH>(p, L, st, base, e1);
+    if (full_end < e1) edge_step<true, T, OutT, NV, MODE, VP, LPH>(p, L, st, full_end, e1);
 
     // merge the lane groups (fixed butterfly order)
     for (int off = L.gsize; off < 32; off <<= 1) {
@@ -458,7 +463,7 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 // L2 keeps serving the sources near them).  Each item's result depends only
 // on its own data, so the dynamic order does not change any output.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, int MODE>
+template <typename T, typename OutT, int NV, int MODE, int LPH>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : 1)
     core_kernel(const CoreParams p) {
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
@@ -473,13 +478,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
         for (unsigned long long it = first; it < last; ++it) {
             if (it < n_chunks) {
                 const int32_t* c = p.chunks + 3 * it;
-                process_item<T, OutT, NV, MODE>(p, L, c[0], c[1], c[2], (long long)it);
+                process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
             } else {
                 const int row = (int)(it - n_chunks);
                 const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
                 if (e1 - e0 > p.heavy_threshold) continue;  // done by chunks + merge
                 if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) continue;  // tile path
-                process_item<T, OutT, NV, MODE>(p, L, row, e0, e1, -1);
+                process_item<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1, -1);
             }
         }
     }
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
-template <typename T, typename OutT, int NV, int MODE>
+template <typename T, typename OutT, int NV, int MODE, int LPH>
 cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
     const long long items = p.n_chunks + p.N;
     if (items <= 0) return cudaSuccess;
@@ -538,7 +543,8 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE>, kWarpsPerCta * 32, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE, LPH>, kWarpsPerCta * 32,
+                                                          0);
         if (e != cudaSuccess) return e;
         cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
         cached_dev = dev;
@@ -547,18 +553,27 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
     const int ctas = (int)(need < cached_ctas ? need : cached_ctas);
     e = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned long long), st);
     if (e != cudaSuccess) return e;
-    core_kernel<T, OutT, NV, MODE><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
+    core_kernel<T, OutT, NV, MODE, LPH><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 template <typename T, typename OutT, int MODE>
 cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
     const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
+    if (nv == 1) {  // one vector per lane: the head-lane reduction is unrolled
+        switch (p.lph) {
+            case 2: return launch_core_nv<T, OutT, 1, MODE, 2>(p, st);
+            case 4: return launch_core_nv<T, OutT, 1, MODE, 4>(p, st);
+            case 8: return launch_core_nv<T, OutT, 1, MODE, 8>(p, st);
+            case 16: return launch_core_nv<T, OutT, 1, MODE, 16>(p, st);
+            case 32: return launch_core_nv<T, OutT, 1, MODE, 32>(p, st);
+            default: return launch_core_nv<T, OutT, 1, MODE, 0>(p, st);
+        }
+    }
     switch (nv) {
-        case 1: return launch_core_nv<T, OutT, 1, MODE>(p, st);
-        case 2: return launch_core_nv<T, OutT, 2, MODE>(p, st);
-        case 4: return launch_core_nv<T, OutT, 4, MODE>(p, st);
-        case 8: return launch_core_nv<T, OutT, 8, MODE>(p, st);
+        case 2: return launch_core_nv<T, OutT, 2, MODE, 0>(p, st);
+        case 4: return launch_core_nv<T, OutT, 4, MODE, 0>(p, st);
+        case 8: return launch_core_nv<T, OutT, 8, MODE, 0>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }
