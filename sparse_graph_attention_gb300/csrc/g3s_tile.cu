@@ -22,9 +22,12 @@
 //   3. thread i reads row i of S, masks entries outside its own window's
 //      tiles or absent from the bitmap, updates its running max / sum and
 //      writes P = 2^(s - m) in the input type to shared memory;
-//   4. O_chunk = P V (M=128, N=64, K=64; V read as an MN-major operand) into
-//      TMEM columns [64, 128), added by each thread to its fp32 row of O.
-// Rows are normalised and stored at the end.  Every wait on an mbarrier is
+//   4. O += P V (M=128, N=64, K=64; V read as an MN-major operand) accumulates
+//      in TMEM columns [64, 128); it is issued together with the next chunk's
+//      S = Q K^T under one commit, so each chunk costs one MMA round trip.
+//      When a row's reference max moves (rarely: only by more than 2^8), the
+//      thread rescales its row of O in TMEM before the next accumulation.
+// Rows are read back from TMEM, normalised and stored at the end.  Every wait on an mbarrier is
 // bounded (about one second of %globaltimer); on expiry the CTA sets the
 // plan's status word, frees its TMEM and returns.
 #include <cuda_bf16.h>
@@ -57,6 +60,7 @@ struct TileSmem {
     int tile_g[kMaxGroupTiles];     // global tile index of each group tile
     int8_t tile_j[kMaxGroupTiles];  // window slot of each group tile
     int win[kGroupWindows];
+    int win_t0[kGroupWindows], win_t1[kGroupWindows];  // group-tile range of each window
     unsigned long long mbar;
     uint32_t tmem_base;
     int nw, tt;
@@ -149,6 +153,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// store 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};\n"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -276,6 +293,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
                 sm.tile_g[start + k] = t0 + k;
                 sm.tile_j[start + k] = (int8_t)lane;
             }
+            sm.win_t0[lane] = start;
+            sm.win_t1[lane] = start + cnt;
         }
         const int nw = __popc(__ballot_sync(0xffffffffu, w >= 0));
         const int tt = __shfl_sync(0xffffffffu, start + cnt, kGroupWindows - 1);
@@ -306,8 +325,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
                 cp_async16(smem_u32(&sm.bits[ms][slot][0]), p.tile_bits + g * 4, valid ? 16u : 0u);
         }
     };
-    // chunk `ch`'s K and V rows (64 rows x 8 pieces of 16 B) into stage `ks`
-    auto issue_gather = [&](int ch, int ks, int ms) {
+    // chunk `ch`'s K or V rows (64 rows x 8 pieces of 16 B) into stage `st`
+    auto issue_gather = [&](const T* src, uint8_t* dst_base, int ch, int ms) {
 #pragma unroll
         for (int it = 0; it < (kNC * 8) / kThreads; ++it) {
             const int piece = tid + kThreads * it;
@@ -315,8 +334,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
             const int col = (ch * 8 + (c >> 3)) < tt ? sm.cols[ms][c] : -1;
             const long long off = col >= 0 ? ((long long)col * p.H + h) * kD + x * 8 : 0;
             const uint32_t d = (uint32_t)(c * 128 + ((x ^ (c & 7)) << 4));
-            cp_async16(smem_u32(sm.k[ks]) + d, K + off, col >= 0 ? 16u : 0u);
-            cp_async16(smem_u32(sm.v[ks]) + d, V + off, col >= 0 ? 16u : 0u);
+            cp_async16(smem_u32(dst_base) + d, src + off, col >= 0 ? 16u : 0u);
         }
     };
 
@@ -327,6 +345,12 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         const long long n = (long long)sm.win[j] * kWinRows + r;
         if (n < p.N) node = n;
     }
+    const int my_t0 = j < sm.nw ? sm.win_t0[j] : 0;  // this row's window: group tiles [my_t0, my_t1)
+    const int my_t1 = j < sm.nw ? sm.win_t1[j] : 0;
+    const uint32_t tmem_S = tmem;             // S chunk, columns [0, 64)
+    const uint32_t tmem_O = tmem + kNC;       // O accumulator, columns [64, 128)
+    const uint32_t row_S = tmem_row;          // this warp's lanes of S
+    const uint32_t row_O = tmem_row + kNC;    // and of O
 
     // ---- prologue: Q, chunk 0's metadata, then chunk 0's rows + chunk 1's metadata
     {
@@ -339,13 +363,13 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    if (nchunks > 0) issue_gather(0, 0, 0);
+    if (nchunks > 0) {
+        issue_gather(K, sm.k[0], 0, 0);
+        issue_gather(V, sm.v[0], 0, 0);
+    }
     if (nchunks > 1) issue_meta(1, 1);
     cp_async_commit();
 
-    float o[kD];
-#pragma unroll
-    for (int i = 0; i < kD; ++i) o[i] = 0.f;
     float m = kNegBig, l = 0.f;
     uint32_t phase = 0;
     bool failed = false;
@@ -353,40 +377,49 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
 
     for (int ch = 0; ch < nchunks; ++ch) {
         const int ks = ch & 1, ms = ch % 3;
-        cp_async_wait_all();  // chunk ch's rows and chunk ch+1's metadata
-        fence_async_smem();
+        cp_async_wait_all();  // this chunk's K and V rows, the next chunk's metadata
+        fence_async_smem();   // ... and the previous chunk's P: visible to the tensor core
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
 
-        // S = Q K^T
+        // O += P_{ch-1} V_{ch-1} (accumulated in TMEM), then S = Q K_ch^T; one commit covers both
         if (tid == 0) {
+            if (ch > 0) {
+#pragma unroll
+                for (int kk = 0; kk < kNC / 16; ++kk)
+                    mma_f16(tmem_O, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
+                            sdesc_sw128(smem_u32(sm.v[ks ^ 1]) + kk * 16 * 128, kNC * 128, 1024), kIdescO,
+                            (ch > 1 || kk > 0) ? 1u : 0u);
+            }
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-                mma_f16(tmem, sdesc_sw128(smem_u32(sm.q) + kk * 32, 16, 1024),
+                mma_f16(tmem_S, sdesc_sw128(smem_u32(sm.q) + kk * 32, 16, 1024),
                         sdesc_sw128(smem_u32(sm.k[ks]) + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
             mma_commit(&sm.mbar);
         }
-        // next chunk's rows (into the other stage, free since the last chunk's MMAs
-        // completed) and the metadata two chunks ahead, in flight during this chunk
-        if (ch + 1 < nchunks) issue_gather(ch + 1, ks ^ 1, (ch + 1) % 3);
+        // the next chunk's K rows (that stage was last read by S_{ch-1}, complete) and
+        // the metadata two chunks ahead
+        if (ch + 1 < nchunks) issue_gather(K, sm.k[ks ^ 1], ch + 1, (ch + 1) % 3);
         if (ch + 2 < nchunks) issue_meta(ch + 2, (ch + 2) % 3);
-        cp_async_commit();
 
-        bool ok = mbar_wait_bounded(&sm.mbar, phase);
+        const bool ok = mbar_wait_bounded(&sm.mbar, phase);
         phase ^= 1u;
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
         }
         tc_fence_after();
+        // the next chunk's V rows (that stage was last read by P_{ch-1} V_{ch-1}, now complete)
+        if (ch + 1 < nchunks) issue_gather(V, sm.v[ks ^ 1], ch + 1, (ch + 1) % 3);
+        cp_async_commit();
 
-        // masked online softmax of this row
+        // masked online softmax of this row of S_ch
         float s[kNC];
 #pragma unroll
         for (int q4 = 0; q4 < kNC / 16; ++q4) {
             float v16[16];
-            tmem_ld16(tmem_row + q4 * 16, v16);
+            tmem_ld16(row_S + q4 * 16, v16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) s[q4 * 16 + i] = v16[i];
         }
@@ -395,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         for (int slot = 0; slot < 8; ++slot) {
             const int t = ch * 8 + slot;
             uint32_t mask8 = 0;
-            if (node >= 0 && t < tt && sm.tile_j[t] == j) mask8 = (sm.bits[ms][slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
+            if (node >= 0 && t >= my_t0 && t < my_t1) mask8 = (sm.bits[ms][slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float x = ((mask8 >> c) & 1u) ? s[slot * 8 + c] * scale : -INFINITY;
@@ -403,12 +436,29 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
                 cmax = fmaxf(cmax, x);
             }
         }
+        // Move the reference max when a logit exceeds it by more than the slack.
+        // The row of O in TMEM then needs the same factor -- unless nothing has
+        // been accumulated for this row yet (l == 0: its O row is still zero).
+        float corr = 1.f;
+        bool rescale = false;
         if (cmax > m + kRescaleSlack) {
-            const float corr = ex2(m - cmax);
+            corr = ex2(m - cmax);
+            rescale = l > 0.f;
             l *= corr;
-#pragma unroll
-            for (int i = 0; i < kD; ++i) o[i] *= corr;
             m = cmax;
+        }
+        // tcgen05.ld / st are warp-collective: every thread takes part, the
+        // ones that need no rescale multiply by 1.
+        if (__syncthreads_or(rescale)) {  // rare; O_{ch-1} is complete, nothing is in flight on O
+            const float f = rescale ? corr : 1.f;
+#pragma unroll
+            for (int q4 = 0; q4 < kD / 16; ++q4) {
+                float v16[16];
+                tmem_ld16(row_O + q4 * 16, v16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v16[i] *= f;
+                tmem_st16(row_O + q4 * 16, v16);
+            }
         }
         {
             const uint32_t pdst = smem_u32(sm.p) + tid * 128;
@@ -426,39 +476,47 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
                              : "memory");
             }
         }
+    }
+
+    // the last chunk's P V
+    if (!failed && nchunks > 0) {
+        cp_async_wait_all();
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-
-        // O_chunk = P V
         if (tid == 0) {
 #pragma unroll
             for (int kk = 0; kk < kNC / 16; ++kk)
-                mma_f16(tmem + kNC, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
-                        sdesc_sw128(smem_u32(sm.v[ks]) + kk * 16 * 128, kNC * 128, 1024), kIdescO, kk > 0 ? 1u : 0u);
+                mma_f16(tmem_O, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
+                        sdesc_sw128(smem_u32(sm.v[(nchunks - 1) & 1]) + kk * 16 * 128, kNC * 128, 1024), kIdescO,
+                        (nchunks > 1 || kk > 0) ? 1u : 0u);
             mma_commit(&sm.mbar);
         }
-        ok = mbar_wait_bounded(&sm.mbar, phase);
+        const bool ok = mbar_wait_bounded(&sm.mbar, phase);
         phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
+        if (__syncthreads_or(!ok)) failed = true;
         tc_fence_after();
-#pragma unroll
-        for (int q4 = 0; q4 < kD / 16; ++q4) {
-            float v16[16];
-            tmem_ld16(tmem_row + kNC + q4 * 16, v16);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[q4 * 16 + i] += v16[i];
-        }
-        tc_fence_before();
-        __syncthreads();  // TMEM, P and this chunk's stages are reused next
     }
     cp_async_wait_all();
 
-    if (!failed && node >= 0) store_row<OutT>(p.O, (node * p.H + h) * kD, o, l > 0.f ? 1.0f / l : 0.f);
+    if (!failed) {  // uniform over the CTA
+        float o[kD];
+        if (nchunks > 0) {
+            // warp-collective read of every row, padding rows included
+#pragma unroll
+            for (int q4 = 0; q4 < kD / 16; ++q4) {
+                float v16[16];
+                tmem_ld16(row_O + q4 * 16, v16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[q4 * 16 + i] = v16[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kD; ++i) o[i] = 0.f;
+        }
+        if (node >= 0) store_row<OutT>(p.O, (node * p.H + h) * kD, o, l > 0.f ? 1.0f / l : 0.f);
+    }
     if (failed && tid == 0) atomicOr(p.status, kErrTimeout);
     tc_fence_before();
     __syncthreads();

@@ -96,6 +96,33 @@ def test_tile_many_chunks_per_window():
     assert st["tiles"] > 20 * st["tile_windows"]
 
 
+def test_tile_rescale_of_accumulated_rows():
+    """Windows spanning four 64-column chunks whose later columns carry much larger
+    logits: each row's reference max moves after O has been accumulated in TMEM,
+    so the rows are rescaled in place before the next accumulation."""
+    rng = np.random.default_rng(29)
+    n = 16 * 8
+    cols, deg = [], np.zeros(n, np.int64)
+    for i in range(n):
+        s = np.sort(rng.choice(256, size=rng.integers(80, 140), replace=False))  # sources 0..255, sorted
+        cols.append(s)
+        deg[i] = s.size
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    nn = 256
+    rp = np.concatenate([rp, np.full(nn - n, rp[-1], np.int32)])  # nodes 128..255: no in-edges
+    g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
+    vals = graphgen.make_values(nn, g.num_edges, 2, 64, False, seed=30)
+    ramp = np.linspace(0.2, 6.0, nn, dtype=np.float32)[:, None, None]  # logits grow with the column id
+    vals["K"] = vals["K"] * ramp
+    vals["Q"] = np.abs(vals["Q"]) * 2.0
+    vals["K"] = np.abs(vals["K"])
+    plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard",
+                          plan_kw=dict(tile_path=1, tile_density_milli=0, heavy_threshold=512))
+    plan.check()
+    assert plan.stats()["tile_windows"] == 8
+
+
 def test_tile_multigraph_windows_stay_on_core():
     g = graphgen.random_csr(200, 30, seed=17, multigraph=True)
     plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=0))
