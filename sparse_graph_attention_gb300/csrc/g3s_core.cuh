@@ -8,7 +8,9 @@
 // gathers a different in-edge, so one warp load instruction covers G edges;
 // wider rows give each lane NV = row_vecs/32 vectors of a single edge.  The
 // lanes of one head (lph = d*sizeof(T)/16 of them) reduce the dot product
-// with xor shuffles.  Every group keeps its own online-softmax state (running
+// with xor shuffles (for 16-bit inputs the per-lane dot products take the
+// stored 16-bit values directly into fp32 FMAs, and the 1/sqrt(d) scale is
+// applied after the reduction).  Every group keeps its own online-softmax state (running
 // max m, denominator l, fp32 accumulator) in registers; the groups are merged
 // with a fixed butterfly at the end, so the result does not depend on timing.
 //
@@ -137,6 +139,45 @@ struct Vec<__half> {
 
 __device__ __forceinline__ uint4 ldg16(const uint4* p) { return __ldg(p); }
 
+// Dot product of two 16-byte vectors of 16-bit values with fp32 FMAs that
+// take the 16-bit operands directly (fma.rn.f32.bf16 / .f16: the product of
+// two 16-bit values is exact in fp32, so this equals unpacking to fp32 and
+// using fp32 FMAs in the same order).  Even and odd elements form two chains.
+template <typename T>
+struct MixedDot;
+template <>
+struct MixedDot<__nv_bfloat16> {
+    __device__ static float run(const uint4& q, const uint4& k) {
+        float a = 0.f, b = 0.f;
+        asm("{\n .reg .b16 q0,q1,q2,q3,q4,q5,q6,q7,k0,k1,k2,k3,k4,k5,k6,k7;\n"
+            " mov.b32 {q0,q1}, %2;\n mov.b32 {q2,q3}, %3;\n mov.b32 {q4,q5}, %4;\n mov.b32 {q6,q7}, %5;\n"
+            " mov.b32 {k0,k1}, %6;\n mov.b32 {k2,k3}, %7;\n mov.b32 {k4,k5}, %8;\n mov.b32 {k6,k7}, %9;\n"
+            " fma.rn.f32.bf16 %0, q0, k0, %0;\n fma.rn.f32.bf16 %1, q1, k1, %1;\n"
+            " fma.rn.f32.bf16 %0, q2, k2, %0;\n fma.rn.f32.bf16 %1, q3, k3, %1;\n"
+            " fma.rn.f32.bf16 %0, q4, k4, %0;\n fma.rn.f32.bf16 %1, q5, k5, %1;\n"
+            " fma.rn.f32.bf16 %0, q6, k6, %0;\n fma.rn.f32.bf16 %1, q7, k7, %1;\n}"
+            : "+f"(a), "+f"(b)
+            : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w), "r"(k.x), "r"(k.y), "r"(k.z), "r"(k.w));
+        return a + b;
+    }
+};
+template <>
+struct MixedDot<__half> {
+    __device__ static float run(const uint4& q, const uint4& k) {
+        float a = 0.f, b = 0.f;
+        asm("{\n .reg .b16 q0,q1,q2,q3,q4,q5,q6,q7,k0,k1,k2,k3,k4,k5,k6,k7;\n"
+            " mov.b32 {q0,q1}, %2;\n mov.b32 {q2,q3}, %3;\n mov.b32 {q4,q5}, %4;\n mov.b32 {q6,q7}, %5;\n"
+            " mov.b32 {k0,k1}, %6;\n mov.b32 {k2,k3}, %7;\n mov.b32 {k4,k5}, %8;\n mov.b32 {k6,k7}, %9;\n"
+            " fma.rn.f32.f16 %0, q0, k0, %0;\n fma.rn.f32.f16 %1, q1, k1, %1;\n"
+            " fma.rn.f32.f16 %0, q2, k2, %0;\n fma.rn.f32.f16 %1, q3, k3, %1;\n"
+            " fma.rn.f32.f16 %0, q4, k4, %0;\n fma.rn.f32.f16 %1, q5, k5, %1;\n"
+            " fma.rn.f32.f16 %0, q6, k6, %0;\n fma.rn.f32.f16 %1, q7, k7, %1;\n}"
+            : "+f"(a), "+f"(b)
+            : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w), "r"(k.x), "r"(k.y), "r"(k.z), "r"(k.w));
+        return a + b;
+    }
+};
+
 __device__ __forceinline__ float clamp5(float x) { return fminf(fmaxf(x, -5.0f), 5.0f); }
 
 // Store VE fp32 values as OutT at element offset `elem` (16-byte aligned).
@@ -193,6 +234,7 @@ struct Lanes {
 template <int NV, int VP>
 struct ItemState {
     float2 q[NV][VP];    // query, pre-scaled (pairs of features)
+    uint4 qr[NV];        // query as stored (16-bit inputs, standard form)
     float2 acc[NV][VP];  // sum of weight * value
     float m[NV], l[NV];  // reference max (log2 units) and sum of weights
     int cbase, idx_lo, idx_hi;  // window of 64 source indices held one per lane
@@ -209,6 +251,7 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
     constexpr bool RTM = MODE == kModeRtm;
     constexpr bool AGG = MODE == kModeAgg;
+    constexpr bool MIXED = MODE == kModeStd && VE == 8;  // 16-bit inputs
     const int rv = L.rv, g = L.g, lph = LPH > 0 ? LPH : L.lph;
     const int S = L.G * U;
     if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
@@ -272,10 +315,12 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
                 lg[u][j] = 0.f;
                 continue;
             }
-            float2 kf[VP];
-            VT::to_float2(kr[u][j], kf);
             float s;
-            if constexpr (RTM) {
+            if constexpr (MIXED) {
+                s = MixedDot<T>::run(st.qr[j], kr[u][j]);
+            } else if constexpr (RTM) {
+                float2 kf[VP];
+                VT::to_float2(kr[u][j], kf);
                 float2 ef[VP];
                 VT::to_float2(er[u][j], ef);
                 float uo[VE];
@@ -295,6 +340,8 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
                 if (p.Eout != nullptr && ok[u])
                     Store<OutT, VE>::run(p.Eout, ((long long)eid[u] * rv + L.sub + 32 * j) * VE, uo);
             } else {
+                float2 kf[VP];
+                VT::to_float2(kr[u][j], kf);
                 float2 s2 = make_float2(0.f, 0.f);  // packed fp32 FMA
 #pragma unroll
                 for (int k = 0; k < VP; ++k) s2 = __ffma2_rn(st.q[j][k], kf[k], s2);
@@ -306,7 +353,7 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
             } else {
                 for (int o2 = 1; o2 < lph; o2 <<= 1) s += __shfl_xor_sync(kFull, s, o2);
             }
-            lg[u][j] = s;
+            lg[u][j] = MIXED ? s * p.qscale : s;  // logit in log2 units
         }
     }
 
@@ -369,12 +416,14 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
     st.idx_hi = (e0 + 32 + L.lane < e1) ? __ldg(p.col_idx + e0 + 32 + L.lane) : 0;
     const uint4* Q4 = static_cast<const uint4*>(p.Q);
     const float2 qs = make_float2(p.qscale, p.qscale);
+    constexpr bool MIXED = MODE == kModeStd && VE == 8;  // dot products on the stored 16-bit query
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-        if constexpr (MODE != kModeAgg) VT::to_float2(ldg16(Q4 + (long long)row * rv + sub + 32 * j), st.q[j]);
+        if constexpr (MIXED) st.qr[j] = ldg16(Q4 + (long long)row * rv + sub + 32 * j);
+        else if constexpr (MODE != kModeAgg) VT::to_float2(ldg16(Q4 + (long long)row * rv + sub + 32 * j), st.q[j]);
 #pragma unroll
         for (int k = 0; k < VP; ++k) {
-            if constexpr (MODE != kModeAgg) st.q[j][k] = __fmul2_rn(st.q[j][k], qs);
+            if constexpr (MODE != kModeAgg && !MIXED) st.q[j][k] = __fmul2_rn(st.q[j][k], qs);
             st.acc[j][k] = make_float2(0.f, 0.f);
         }
         st.m[j] = kNegBig;
