@@ -210,6 +210,8 @@ def parse_args():
                     help="density cutoff of the tile path in 1/1000 (default: the library's)")
     ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
                     help="element type of O (default fp32)")
+    ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
+                    help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -284,6 +286,8 @@ def main():
         plan_kw["out_dtype"] = args.out_dtype
     if args.tile_density_milli is not None:
         plan_kw["tile_density_milli"] = args.tile_density_milli
+    if args.tma_gather is not None:
+        plan_kw["tma_gather"] = args.tma_gather
     plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)
     torch.cuda.synchronize(dev)
     plan_ms = 1000.0 * (time.perf_counter() - t0)
@@ -427,7 +431,8 @@ def main():
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms,
-            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tile_windows": st["tile_windows"],
+            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
+                     "tile_windows": st["tile_windows"],
                      "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},
         }
         print(json.dumps(line), flush=True)

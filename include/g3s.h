@@ -102,6 +102,13 @@ typedef enum g3s_variant {
  *  out_dtype       element type of O and Eout: G3S_F32 (default) or the input
  *                  dtype.  fp32 keeps the fp32 accumulation; a 16-bit store adds
  *                  up to one half-ulp of rounding (2^-8 relative for bf16)
+ *  tma_gather      1: where supported (standard form, fp16/bf16 inputs,
+ *                  H*d*2 = 128, 256 or 512 bytes per node row) the CUDA-core
+ *                  kernel receives its K and V rows through TMA gathers into a
+ *                  per-warp shared-memory ring; 0 (default): plain global
+ *                  loads.  Both compute the same arithmetic in the same order.
+ *                  The ring costs resident warps (shared memory, registers),
+ *                  and on the measured workloads the plain loads are faster.
  */
 typedef struct g3s_plan_options {
     int32_t bucket_bounds[G3S_NUM_BUCKETS - 2];
@@ -116,11 +123,13 @@ typedef struct g3s_plan_options {
     float rtm_epsilon;
     int32_t validate_graph;
     int32_t out_dtype;
+    int32_t tma_gather;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {
     int64_t num_nodes, num_edges;
-    int32_t heads, head_dim, dtype, variant, out_dtype, reserved0;
+    int32_t heads, head_dim, dtype, variant, out_dtype;
+    int32_t tma_gather; /* 1 when forward feeds the CUDA-core kernel through TMA gathers */
     int64_t bucket_count[G3S_NUM_BUCKETS];
     int64_t heavy_rows, chunks;
     int32_t has_bsb, tile_path;

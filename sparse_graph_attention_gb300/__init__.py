@@ -62,6 +62,7 @@ class PlanOptions(ctypes.Structure):
         ("rtm_epsilon", ctypes.c_float),
         ("validate_graph", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32),
+        ("tma_gather", ctypes.c_int32),
     ]
 
 
@@ -70,7 +71,7 @@ class PlanStats(ctypes.Structure):
         ("num_nodes", ctypes.c_int64), ("num_edges", ctypes.c_int64),
         ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("variant", ctypes.c_int32),
-        ("out_dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32), ("tma_gather", ctypes.c_int32),
         ("bucket_count", ctypes.c_int64 * NUM_BUCKETS),
         ("heavy_rows", ctypes.c_int64), ("chunks", ctypes.c_int64),
         ("has_bsb", ctypes.c_int32), ("tile_path", ctypes.c_int32),

@@ -71,6 +71,7 @@ void default_options(g3s_plan_options* o) {
     o->rtm_epsilon = 1e-6f;
     o->validate_graph = 1;
     o->out_dtype = G3S_F32;
+    o->tma_gather = 0;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -104,6 +105,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (!(o.rtm_epsilon >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "rtm_epsilon must be >= 0");
     if (o.out_dtype != G3S_F32 && o.out_dtype != dtype)
         return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
+    if (o.tma_gather != 0 && o.tma_gather != 1) return fail(G3S_ERR_INVALID_ARG, "tma_gather must be 0 or 1");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -218,10 +220,10 @@ g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int hea
         o = *opts;
     else
         default_options(&o);
-    PlanShape s;
+    PlanShape s{};
     g3s_status st = check_shape(num_nodes, num_edges, heads, head_dim, dtype, variant, o, &s);
     if (st != G3S_OK) return st;
-    PlanArrays a;
+    PlanArrays a{};
     *bytes = carve(s, &a, nullptr);
     return G3S_OK;
 }
@@ -237,14 +239,14 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
         o = *opts;
     else
         default_options(&o);
-    PlanShape s;
+    PlanShape s{};
     g3s_status st = check_shape(num_nodes, num_edges, heads, head_dim, dtype, variant, o, &s);
     if (st != G3S_OK) return st;
     if (!row_ptr_d) return fail(G3S_ERR_INVALID_ARG, "row_ptr is NULL");
     if (num_edges > 0 && !col_idx_d) return fail(G3S_ERR_INVALID_ARG, "col_idx is NULL with E > 0");
     if ((reinterpret_cast<uintptr_t>(row_ptr_d) & 3u) || (reinterpret_cast<uintptr_t>(col_idx_d) & 3u))
         return fail(G3S_ERR_INVALID_ARG, "row_ptr / col_idx must be 4-byte aligned");
-    PlanArrays a;
+    PlanArrays a{};
     const size_t need = carve(s, &a, nullptr);
     if (!workspace_d) return fail(G3S_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
     if (reinterpret_cast<uintptr_t>(workspace_d) % kAlign)
@@ -306,6 +308,10 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->dtype = p->dtype;
     st->variant = p->variant;
     st->out_dtype = p->opts.out_dtype;
+    st->tma_gather = (p->opts.tma_gather && core_tma_supported(p->dtype, p->variant == G3S_RTMSCORE ? 1 : 0,
+                                                                p->shape.H * p->shape.D * dtype_size(p->dtype) / 16))
+                         ? 1
+                         : 0;
     for (int b = 0; b < G3S_NUM_BUCKETS; ++b) st->bucket_count[b] = p->counts.bucket_count[b];
     st->heavy_rows = p->counts.n_heavy;
     st->chunks = p->counts.n_chunks;
@@ -372,7 +378,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
     const int esz = dtype_size(p->dtype);
-    CoreParams cp;
+    CoreParams cp{};
     cp.W = nullptr;
     cp.normalize = 0;
     cp.edge_id = p->edge_id;
@@ -400,8 +406,9 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.qscale = rtm ? inv_sqrt_d : inv_sqrt_d * 1.4426950408889634f;
     cp.eps = p->opts.rtm_epsilon;
     cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
+    cp.status = p->arr.fwd_status;
     if (p->counts.n_tile_windows > 0) {
-        TileParams tp;
+        TileParams tp{};
         tp.Q = Q;
         tp.K = K;
         tp.V = V;
@@ -417,9 +424,10 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.status = p->arr.fwd_status;
         CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
     }
-    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream), "fused kernel launch");
+    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, stream),
+                 "fused kernel launch");
     if (p->counts.n_chunks > 0) {
-        MergeParams mp;
+        MergeParams mp{};
         mp.heavy_rows = p->arr.heavy_rows;
         mp.heavy_chunk_ptr = p->arr.heavy_chunk_ptr;
         mp.part_acc = p->arr.part_acc;
@@ -450,7 +458,7 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     if (dev != p->device) return fail(G3S_ERR_INVALID_ARG, "plan was built on device %d, current is %d", p->device, dev);
     if (s.N == 0) return G3S_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    CoreParams cp;
+    CoreParams cp{};
     cp.row_ptr = p->row_ptr;
     cp.col_idx = p->col_idx;
     cp.Q = nullptr;
@@ -477,9 +485,10 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     cp.eps = eps;
     cp.elementwise_clamp = 0;
     cp.normalize = normalize ? 1 : 0;
-    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, cp, stream), "aggregation kernel launch");
+    cp.status = p->arr.fwd_status;
+    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, false, cp, stream), "aggregation kernel launch");
     if (p->counts.n_chunks > 0) {
-        MergeParams mp;
+        MergeParams mp{};
         mp.heavy_rows = p->arr.heavy_rows;
         mp.heavy_chunk_ptr = p->arr.heavy_chunk_ptr;
         mp.part_acc = p->arr.part_acc;

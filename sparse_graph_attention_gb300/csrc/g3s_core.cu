@@ -1,8 +1,60 @@
 // Dispatch of the fused CUDA-core kernel and the heavy-row merge by input and
-// output element type.  The kernels themselves are in g3s_core.cuh.
+// output element type.  The kernels themselves are in g3s_core.cuh and
+// g3s_core_tma.cuh.
+#include <mutex>
+
 #include "g3s_internal.h"
 
 namespace g3s {
+
+namespace {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library does
+// not link the driver API).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// A 2-D map over n node rows of row_vecs 16-byte vectors (16-bit elements),
+// box one row high and one row wide, for tile::gather4.
+bool encode_rows(EncodeTiledFn enc, CUtensorMap* m, const void* base, long long n, int row_vecs) {
+    const cuuint64_t dims[2] = {(cuuint64_t)row_vecs * 8, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_vecs * 16};
+    const cuuint32_t box[2] = {(cuuint32_t)row_vecs * 8, 1};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The maps of the last K and V seen by this host thread (encoding is host
+// work of a few microseconds; repeated forwards on the same tensors reuse it).
+struct MapCache {
+    const void* K = nullptr;
+    const void* V = nullptr;
+    long long n = -1;
+    int row_vecs = 0;
+    CUtensorMap tk, tv;
+};
+thread_local MapCache map_cache;
+
+}  // namespace
 
 bool core_supported(int dtype, int row_vecs) {
     if (dtype < 0 || dtype > 2) return false;
@@ -10,9 +62,30 @@ bool core_supported(int dtype, int row_vecs) {
     return true;
 }
 
-cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st) {
+bool core_tma_supported(int dtype, int mode, int row_vecs) {
+    return mode == 0 && (dtype == 1 || dtype == 2) && (row_vecs == 8 || row_vecs == 16 || row_vecs == 32);
+}
+
+cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const CoreParams& p, cudaStream_t st) {
     const bool out_f32 = out_dtype == 0;
     if (!out_f32 && out_dtype != dtype) return cudaErrorInvalidValue;
+    if (tma && p.N > 0 && p.status != nullptr && core_tma_supported(dtype, mode, p.row_vecs)) {
+        EncodeTiledFn enc = tensor_map_encoder();
+        if (enc != nullptr) {
+            MapCache& c = map_cache;
+            if (c.K != p.K || c.V != p.V || c.n != p.N || c.row_vecs != p.row_vecs) {
+                c.K = nullptr;
+                if (!encode_rows(enc, &c.tk, p.K, p.N, p.row_vecs) || !encode_rows(enc, &c.tv, p.V, p.N, p.row_vecs))
+                    return cudaErrorInvalidValue;
+                c.K = p.K;
+                c.V = p.V;
+                c.n = p.N;
+                c.row_vecs = p.row_vecs;
+            }
+            return dtype == 1 ? core_tma_launch_f16(out_f32, p, c.tk, c.tv, st)
+                              : core_tma_launch_bf16(out_f32, p, c.tk, c.tv, st);
+        }
+    }
     switch (dtype) {
         case 0: return core_launch_f32(true, mode, p, st);
         case 1: return core_launch_f16(out_f32, mode, p, st);

@@ -240,72 +240,23 @@ struct ItemState {
     int cbase, idx_lo, idx_hi;  // window of 64 source indices held one per lane
 };
 
-// One step of S = G * U edges starting at CSR position `base`.  TAIL: the
-// step runs past the row's end; slots beyond it re-read the row's last edge
-// (a valid, cached address) and get weight 0, so no load is branched.
-template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
-__device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
-                                          const int e1) {
+// The arithmetic of one step on fetched rows: logits, softmax weights and the
+// weighted sum of values (kr/vr/er: the lane's 16-byte vectors of K, V and E
+// for its U edges; ok: the slot holds a real edge; eid: its physical slot).
+template <int U, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
+__device__ __forceinline__ void edge_math(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st,
+                                          const uint4 (&kr)[MODE == kModeAgg ? 1 : U][MODE == kModeAgg ? 1 : NV],
+                                          const uint4 (&vr)[U][NV],
+                                          const uint4 (&er)[MODE == kModeRtm ? U : 1][MODE == kModeRtm ? NV : 1],
+                                          const float (&wg)[MODE == kModeAgg ? U : 1][MODE == kModeAgg ? NV : 1],
+                                          const bool (&ok)[U],
+                                          const int (&eid)[(MODE == kModeRtm || MODE == kModeAgg) ? U : 1]) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
-    constexpr int U = NV >= 4 ? 1 : 4 / NV;
     constexpr bool RTM = MODE == kModeRtm;
     constexpr bool AGG = MODE == kModeAgg;
     constexpr bool MIXED = MODE == kModeStd && VE == 8;  // 16-bit inputs
-    const int rv = L.rv, g = L.g, lph = LPH > 0 ? LPH : L.lph;
-    const int S = L.G * U;
-    if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
-        st.cbase += 64;
-        st.idx_lo = (st.cbase + L.lane < e1) ? __ldg(p.col_idx + st.cbase + L.lane) : 0;
-        st.idx_hi = (st.cbase + 32 + L.lane < e1) ? __ldg(p.col_idx + st.cbase + 32 + L.lane) : 0;
-    }
-    const int off = base - st.cbase;  // 0, S, 2S, ... < 64
-    const int last = e1 - 1 - st.cbase;
-    int src[U];
-    bool ok[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        int pos = off + g * U + u;
-        ok[u] = !TAIL || pos <= last;
-        if (TAIL) pos = ok[u] ? pos : last;
-        if (S <= 32) {
-            const int v = (off & 32) ? st.idx_hi : st.idx_lo;  // warp-uniform choice
-            src[u] = __shfl_sync(kFull, v, pos & 31);
-        } else {
-            const int a = __shfl_sync(kFull, st.idx_lo, pos & 31);
-            const int b = __shfl_sync(kFull, st.idx_hi, pos & 31);
-            src[u] = pos < 32 ? a : b;
-        }
-    }
-
-    const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
-    const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
-    // physical slot of each edge's features (RTMScore) or weights (aggregation)
-    int eid[(RTM || AGG) ? U : 1];
-    if constexpr (RTM || AGG) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = ok[u] ? base + g * U + u : e1 - 1;
-            eid[u] = p.edge_id != nullptr ? __ldg(p.edge_id + e) : e;
-        }
-    }
-    uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
-    uint4 er[RTM ? U : 1][RTM ? NV : 1];
-    float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const long long o = (long long)src[u] * rv;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
-            vr[u][j] = ldg16(V4 + o + 32 * j);
-            if constexpr (AGG) wg[u][j] = Vec<T>::load1(p.W, (long long)eid[u] * p.H + (L.sub + 32 * j) / lph);
-            if constexpr (RTM) {
-                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)eid[u] * rv + 32 * j);
-            }
-        }
-    }
-
+    const int rv = L.rv, lph = LPH > 0 ? LPH : L.lph;
     float lg[U][NV];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -394,23 +345,80 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
     }
 }
 
-// ---------------------------------------------------------------------------
-// One work item: destination `row`, CSR positions [e0, e1).  chunk >= 0 means
-// this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
-// otherwise normalise and write O.
-// ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, int MODE, int LPH>
-__device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
-                                             const int e1, const long long chunk) {
-    using VT = Vec<T>;
-    constexpr int VE = VT::N;  // elements per 16-byte vector
-    constexpr int VP = VE / 2;
+// One step of S = G * U edges starting at CSR position `base`.  TAIL: the
+// step runs past the row's end; slots beyond it re-read the row's last edge
+// (a valid, cached address) and get weight 0, so no load is branched.
+template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
+__device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
+                                          const int e1) {
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
-    constexpr bool PLAIN = MODE != kModeStd;  // weights need no running max
-    const int rv = L.rv, g = L.g, sub = L.sub, lph = LPH > 0 ? LPH : L.lph;
+    constexpr bool RTM = MODE == kModeRtm;
+    constexpr bool AGG = MODE == kModeAgg;
+    const int rv = L.rv, g = L.g, lph = LPH > 0 ? LPH : L.lph;
     const int S = L.G * U;
+    if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
+        st.cbase += 64;
+        st.idx_lo = (st.cbase + L.lane < e1) ? __ldg(p.col_idx + st.cbase + L.lane) : 0;
+        st.idx_hi = (st.cbase + 32 + L.lane < e1) ? __ldg(p.col_idx + st.cbase + 32 + L.lane) : 0;
+    }
+    const int off = base - st.cbase;  // 0, S, 2S, ... < 64
+    const int last = e1 - 1 - st.cbase;
+    int src[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        int pos = off + g * U + u;
+        ok[u] = !TAIL || pos <= last;
+        if (TAIL) pos = ok[u] ? pos : last;
+        if (S <= 32) {
+            const int v = (off & 32) ? st.idx_hi : st.idx_lo;  // warp-uniform choice
+            src[u] = __shfl_sync(kFull, v, pos & 31);
+        } else {
+            const int a = __shfl_sync(kFull, st.idx_lo, pos & 31);
+            const int b = __shfl_sync(kFull, st.idx_hi, pos & 31);
+            src[u] = pos < 32 ? a : b;
+        }
+    }
 
-    ItemState<NV, VP> st;
+    const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
+    const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
+    // physical slot of each edge's features (RTMScore) or weights (aggregation)
+    int eid[(RTM || AGG) ? U : 1];
+    if constexpr (RTM || AGG) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = ok[u] ? base + g * U + u : e1 - 1;
+            eid[u] = p.edge_id != nullptr ? __ldg(p.edge_id + e) : e;
+        }
+    }
+    uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
+    uint4 er[RTM ? U : 1][RTM ? NV : 1];
+    float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const long long o = (long long)src[u] * rv;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
+            vr[u][j] = ldg16(V4 + o + 32 * j);
+            if constexpr (AGG) wg[u][j] = Vec<T>::load1(p.W, (long long)eid[u] * p.H + (L.sub + 32 * j) / lph);
+            if constexpr (RTM) {
+                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)eid[u] * rv + 32 * j);
+            }
+        }
+    }
+
+    edge_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, kr, vr, er, wg, ok, eid);
+}
+
+// Start of a work item: the query, an empty softmax state, and the first 64
+// source indices.
+template <typename T, int NV, int MODE, int VP>
+__device__ __forceinline__ void init_item(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int row,
+                                          const int e0, const int e1) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    const int rv = L.rv, sub = L.sub;
     st.cbase = e0;
     st.idx_lo = (e0 + L.lane < e1) ? __ldg(p.col_idx + e0 + L.lane) : 0;
     st.idx_hi = (e0 + 32 + L.lane < e1) ? __ldg(p.col_idx + e0 + 32 + L.lane) : 0;
@@ -430,10 +438,17 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
         st.l[j] = 0.f;
     }
 
-    const int full_end = e0 + ((e1 - e0) & ~(S - 1));  // S is a power of two
-    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, MODE, VP, LPH>(p, L, st, base, e1);
-    if (full_end < e1) edge_step<true, T, OutT, NV, MODE, VP, LPH>(p, L, st, full_end, e1);
+}
 
+// End of a work item: merge the lane groups, then write the partial result of
+// a heavy-row chunk (chunk >= 0) or the normalised output row.
+template <typename T, typename OutT, int NV, int MODE, int VP, int LPH>
+__device__ __forceinline__ void finish_item(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int row,
+                                            const long long chunk) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    constexpr bool PLAIN = MODE != kModeStd;  // weights need no running max
+    const int rv = L.rv, g = L.g, sub = L.sub, lph = LPH > 0 ? LPH : L.lph;
     // merge the lane groups (fixed butterfly order)
     for (int off = L.gsize; off < 32; off <<= 1) {
 #pragma unroll
@@ -499,6 +514,26 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
             Store<OutT, VE>::run(p.O, ((long long)row * rv + sub + 32 * j) * VE, o);
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// One work item: destination `row`, CSR positions [e0, e1).  chunk >= 0 means
+// this is chunk `chunk` of a heavy row: write the partial (m, l, acc) there;
+// otherwise normalise and write O.
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT, int NV, int MODE, int LPH>
+__device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
+                                             const int e1, const long long chunk) {
+    constexpr int VP = Vec<T>::N / 2;
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    const int S = L.G * U;
+    ItemState<NV, VP> st;
+    init_item<T, NV, MODE, VP>(p, L, st, row, e0, e1);
+    const int full_end = e0 + ((e1 - e0) & ~(S - 1));  // S is a power of two
+    for (int base = e0; base < full_end; base += S) edge_step<false, T, OutT, NV, MODE, VP, LPH>(p, L, st, base, e1);
+    if (full_end < e1) edge_step<true, T, OutT, NV, MODE, VP, LPH>(p, L, st, full_end, e1);
+
+    finish_item<T, OutT, NV, MODE, VP, LPH>(p, L, st, row, chunk);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libg3s translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the type only; driver entry points are looked up at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -116,6 +117,7 @@ struct CoreParams {
     float eps;
     int elementwise_clamp;
     int normalize;  // aggregation: divide by (sum of weights + eps)
+    int32_t* status;  // forward status word: kErrTimeout is OR-ed in when a bounded wait gives up
 };
 
 struct MergeParams {
@@ -134,7 +136,11 @@ struct MergeParams {
 // mode: 0 standard softmax, 1 RTMScore, 2 weighted aggregation.
 // Launchers return cudaErrorInvalidValue for shapes without a kernel.
 bool core_supported(int dtype, int row_vecs);
-cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st);
+// The TMA-fed form (g3s_core_tma.cuh): standard mode, 16-bit inputs, row_vecs 8, 16 or 32.
+bool core_tma_supported(int dtype, int mode, int row_vecs);
+// tma: use the TMA-fed form where core_tma_supported (and the driver offers
+// tensor-map encoding); otherwise the plain-load kernel.
+cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const CoreParams& p, cudaStream_t st);
 cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
@@ -142,6 +148,10 @@ cudaError_t core_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaSt
 cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st);
+cudaError_t core_tma_launch_f16(bool out_f32, const CoreParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t st);
+cudaError_t core_tma_launch_bf16(bool out_f32, const CoreParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 cudaStream_t st);
 
 // ---- tensor-core tile kernel (g3s_tile.cu) -------------------------------
 struct TileParams {

@@ -71,10 +71,10 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     default_options(&o);
     o.bsb = 0;
     o.tile_path = 0;
-    PlanShape s;
+    PlanShape s{};
     g3s_status st = check_shape(num_nodes, num_edges, heads, head_dim, dtype, variant, o, &s);
     if (st != G3S_OK) return st;
-    PlanArrays a;
+    PlanArrays a{};
     const size_t need = carve(s, &a, nullptr);
     if (need > (size_t)G3S_NOALLOC_SCRATCH_BYTES)
         return fail(G3S_ERR_WORKSPACE,
@@ -116,9 +116,10 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
 
     // the fused forward, heavy-row partials in the static scratch
     const int esz = dtype_size(dtype);
-    CoreParams cp;
+    CoreParams cp{};
     cp.W = nullptr;
     cp.normalize = 0;
+    cp.edge_id = nullptr;  // E / Eout by CSR position
     cp.row_ptr = row_ptr_d;
     cp.col_idx = col_idx_d;
     cp.Q = Q;
@@ -143,9 +144,10 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     cp.qscale = rtm ? inv_sqrt_d : inv_sqrt_d * 1.4426950408889634f;
     cp.eps = o.rtm_epsilon;
     cp.elementwise_clamp = o.rtm_elementwise_clamp ? 1 : 0;
-    NOALLOC_CUDA(core_launch(dtype, o.out_dtype, rtm, cp, stream), "fused kernel launch");
+    cp.status = a.fwd_status;
+    NOALLOC_CUDA(core_launch(dtype, o.out_dtype, rtm, o.tma_gather != 0, cp, stream), "fused kernel launch");
     if (hc.n_chunks > 0) {
-        MergeParams mp;
+        MergeParams mp{};
         mp.heavy_rows = a.heavy_rows;
         mp.heavy_chunk_ptr = a.heavy_chunk_ptr;
         mp.part_acc = a.part_acc;
