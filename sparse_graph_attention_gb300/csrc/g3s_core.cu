@@ -31,18 +31,6 @@ EncodeTiledFn tensor_map_encoder() {
     return fn;
 }
 
-// A 2-D map over n node rows of row_vecs 16-byte vectors (16-bit elements),
-// box one row high and one row wide, for tile::gather4.
-bool encode_rows(EncodeTiledFn enc, CUtensorMap* m, const void* base, long long n, int row_vecs) {
-    const cuuint64_t dims[2] = {(cuuint64_t)row_vecs * 8, (cuuint64_t)n};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_vecs * 16};
-    const cuuint32_t box[2] = {(cuuint32_t)row_vecs * 8, 1};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The maps of the last K and V seen by this host thread (encoding is host
 // work of a few microseconds; repeated forwards on the same tensors reuse it).
 struct MapCache {
@@ -55,6 +43,20 @@ struct MapCache {
 thread_local MapCache map_cache;
 
 }  // namespace
+
+bool tensor_maps_available() { return tensor_map_encoder() != nullptr; }
+
+bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr || rows < 1) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_elems, 1};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool core_supported(int dtype, int row_vecs) {
     if (dtype < 0 || dtype > 2) return false;
@@ -70,12 +72,13 @@ cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const Core
     const bool out_f32 = out_dtype == 0;
     if (!out_f32 && out_dtype != dtype) return cudaErrorInvalidValue;
     if (tma && p.N > 0 && p.status != nullptr && core_tma_supported(dtype, mode, p.row_vecs)) {
-        EncodeTiledFn enc = tensor_map_encoder();
-        if (enc != nullptr) {
+        if (tensor_maps_available()) {
             MapCache& c = map_cache;
             if (c.K != p.K || c.V != p.V || c.n != p.N || c.row_vecs != p.row_vecs) {
                 c.K = nullptr;
-                if (!encode_rows(enc, &c.tk, p.K, p.N, p.row_vecs) || !encode_rows(enc, &c.tv, p.V, p.N, p.row_vecs))
+                // one node row per box: row_vecs * 8 16-bit elements
+                const int re = p.row_vecs * 8;
+                if (!encode_rows16(&c.tk, p.K, p.N, re, re, false) || !encode_rows16(&c.tv, p.V, p.N, re, re, false))
                     return cudaErrorInvalidValue;
                 c.K = p.K;
                 c.V = p.V;

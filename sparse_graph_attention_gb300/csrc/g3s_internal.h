@@ -135,6 +135,14 @@ struct MergeParams {
 // dtype / out_dtype: 0 f32, 1 f16, 2 bf16; out_dtype is f32 or the input dtype.
 // mode: 0 standard softmax, 1 RTMScore, 2 weighted aggregation.
 // Launchers return cudaErrorInvalidValue for shapes without a kernel.
+// Tensor maps for TMA, encoded through the driver entry point looked up at
+// run time (g3s_core.cu).  encode_rows16: a 2-D map over `rows` rows of
+// `row_elems` 16-bit elements (row stride row_elems * 2 bytes), box of
+// box_elems x 1 row (the shape tile::gather4 needs); swizzle128 selects the
+// 128-byte swizzle (box_elems * 2 must then be 128).
+bool tensor_maps_available();
+bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128);
+
 bool core_supported(int dtype, int row_vecs);
 // The TMA-fed form (g3s_core_tma.cuh): standard mode, 16-bit inputs, row_vecs 8, 16 or 32.
 bool core_tma_supported(int dtype, int mode, int row_vecs);
@@ -172,6 +180,7 @@ struct TileParams {
 bool tile_supported(int dtype, int variant, int head_dim);
 cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st);
 cudaError_t tile_launch(int dtype, int out_dtype, const TileParams& p, cudaStream_t st);
+
 
 // ---- host helpers shared by the ABI translation units (g3s_api.cu) ---------
 namespace api {

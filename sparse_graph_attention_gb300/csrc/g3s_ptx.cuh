@@ -50,15 +50,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
-// TMA gather of four rows (row indices r0..r3, column 0) of a 2-D tensor map
-// whose box is one row high, into consecutive rows of shared memory at dst;
-// completion is counted on the mbarrier in bytes.
+// TMA gather of four rows (row indices r0..r3, starting at element column x,
+// which must be a multiple of 16 bytes) of a 2-D tensor map whose box is one
+// row high, into consecutive rows of shared memory at dst; completion is
+// counted on the mbarrier in bytes.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
+                                            uint32_t bar, int x = 0) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
         : "memory");
 }
 
