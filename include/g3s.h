@@ -258,6 +258,42 @@ g3s_status g3s_aggregate(const g3s_plan *plan, const void *W, const void *X, voi
                          g3s_stream_t stream);
 
 /*
+ * Dense projection on the tensor cores: Y = X W^T with fp32 accumulation.
+ * The projection of node (or edge) features into the attention's inputs; the
+ * Triton article (stondelli.it/articles/gattn-triton, closing section) notes
+ * that once the attention is fused these GEMMs dominate the layer.  No
+ * counterpart on the pages beyond that remark: the layout is this library's.
+ *   X  device (M, Kin) row-major, 16-bit (dtype G3S_F16 or G3S_BF16)
+ *   W  device (Nout, Kin) row-major (a linear layer's weight), same dtype
+ *   Y  host array of Nout / seg_cols device pointers (1 to 3): output i holds
+ *      columns [i * seg_cols, (i + 1) * seg_cols) of Y as an (M, seg_cols)
+ *      row-major array in out_dtype (G3S_F32 or dtype), fully overwritten
+ *   status_d  optional device int32: the bit 0x10 is OR-ed in if a bounded
+ *      device wait gives up (the outputs are then incomplete); may be NULL
+ * Kin must be a positive multiple of 8 and seg_cols a positive multiple of
+ * 64 (Nout = 1, 2 or 3 times seg_cols); all pointers 16-byte aligned.
+ * INVALID_ARG otherwise; UNSUPPORTED for other dtypes or when the driver
+ * offers no tensor-map encoding; CUDA when the launch fails.
+ */
+g3s_status g3s_linear(const void *X, const void *W, int64_t M, int Kin, int Nout, g3s_dtype dtype,
+                      void *const *Y, int seg_cols, g3s_dtype out_dtype, int32_t *status_d, g3s_stream_t stream);
+
+/*
+ * One attention layer on the plan's graph: Q | K | V = X Wqkv^T with
+ * g3s_linear (Wqkv is (3 H d, Kin), rows for Q, then K, then V), then
+ * g3s_forward.  For an RTMScore plan also Eproj = Xe We^T (Xe (edge slots,
+ * Ke), We (H d, Ke)) feeds the edge term; NULL Xe/We on a standard plan.
+ * Q, K, V (each (N, H, d)) and Eproj ((edge slots, H, d)) are caller device
+ * buffers of the plan's dtype that receive the projections; O and Eout as in
+ * g3s_forward.  The plan's dtype must be 16-bit and H d a multiple of 64.
+ * Uses the plan's workspace and status word.  Errors as g3s_linear and
+ * g3s_forward.
+ */
+g3s_status g3s_layer_forward(const g3s_plan *plan, const void *X, const void *Wqkv, int Kin, const void *Xe,
+                             const void *We, int Ke, void *Q, void *K, void *V, void *Eproj, void *O, void *Eout,
+                             g3s_stream_t stream);
+
+/*
  * Bytes of device staging g3s_forward_host needs for this plan: room for
  * Q, K, V, O (and Eproj, Eout for RTMScore), each 256-byte aligned.
  */

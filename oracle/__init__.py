@@ -7,6 +7,9 @@ product library never loads it, and it never loads the product library.
 * ``forward``   -- the attention definitions, in C (``g3s_oracle.c``), fp64,
                    OpenMP over rows.
 * ``aggregate`` -- the weighted (optionally normalised) aggregation, same file.
+* ``linear``    -- the projection Y = X W^T in fp64 (numpy matmul on the
+                   exactly widened inputs), and ``round_to`` for storing a
+                   projection in a 16-bit type (round to nearest even).
 * ``decode``    -- the exact widening of stored fp32 / fp16 / bf16 values.
 * ``planner``   -- numpy reference of the degree buckets, heavy-row chunks and
                    BSB tiles (``planner.py``).
@@ -182,3 +185,26 @@ def aggregate(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, W, X, rows=No
     if rc:
         raise ValueError("bad oracle arguments")
     return O
+
+
+def linear(X, W, dtype: str) -> np.ndarray:
+    """fp64 projection Y = X W^T of the stored values: X (M, Kin), W (Nout, Kin).
+
+    The dense projection in front of the attention (the Triton article,
+    stondelli.it/articles/gattn-triton, closing section: the GEMMs that remain
+    once the attention is fused).  The inputs are widened exactly, the
+    product is numpy's fp64 matmul."""
+    x = decode(dtype, X)
+    w = decode(dtype, W)
+    if x.ndim != 2 or w.ndim != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("need X (M, Kin) and W (Nout, Kin)")
+    return x @ w.T
+
+
+def round_to(y, dtype: str) -> np.ndarray:
+    """Values of fp64 ``y`` once stored in ``dtype`` (round to nearest even), as fp64."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float64))
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    return t.to(tdt).to(torch.float64).numpy()

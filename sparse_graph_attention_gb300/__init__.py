@@ -89,7 +89,7 @@ EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_opti
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
             "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
             "g3s_forward_noalloc", "g3s_forward_check", "g3s_aggregate", "g3s_selftest_wait_timeout",
-            "g3s_plan_set_edge_ids"]
+            "g3s_plan_set_edge_ids", "g3s_linear", "g3s_layer_forward"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -131,6 +131,10 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_selftest_wait_timeout.restype = I
         lib.g3s_plan_set_edge_ids.argtypes = [P, P, I64, P]
         lib.g3s_plan_set_edge_ids.restype = I
+        lib.g3s_linear.argtypes = [P, P, I64, I, I, I, ctypes.POINTER(P), I, I, P, P]
+        lib.g3s_linear.restype = I
+        lib.g3s_layer_forward.argtypes = [P, P, P, I, P, P, I, P, P, P, P, P, P, P]
+        lib.g3s_layer_forward.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -341,6 +345,42 @@ class Plan:
             _check(self._lib.g3s_forward(self.handle, q, k, v, e, o, eo, _stream_handle(stream)))
         return (O, Eout) if want_eout else O
 
+    def layer_forward(self, X, Wqkv, Xe=None, We=None, O=None, Eout=None, want_eout: bool = False,
+                      stream=None):
+        """``g3s_layer_forward``: Q|K|V = X Wqkv^T (and, for RTMScore, Eproj = Xe We^T),
+        then the fused forward.  Returns (O, (Q, K, V, Eproj)) or, with
+        ``want_eout``, ((O, Eout), (Q, K, V, Eproj))."""
+        torch = _torch()
+        tdt = torch_dtype(self.dtype)
+        odt = torch_dtype(self.out_dtype)
+        hd = self.heads * self.head_dim
+        kin = int(X.shape[-1])
+        x = _dev_ptr(X, "X", tdt, self.num_nodes * kin, self.device)
+        wqkv = _dev_ptr(Wqkv, "Wqkv", tdt, 3 * hd * kin, self.device)
+        Q, K, V = (torch.empty((self.num_nodes, self.heads, self.head_dim), dtype=tdt, device=self.device)
+                   for _ in range(3))
+        E = xe = we = ep = None
+        ke = 0
+        if self.variant == "rtmscore":
+            ke = int(Xe.shape[-1])
+            xe = _dev_ptr(Xe, "Xe", tdt, self.edge_slots * ke, self.device)
+            we = _dev_ptr(We, "We", tdt, hd * ke, self.device)
+            E = torch.empty((self.edge_slots, self.heads, self.head_dim), dtype=tdt, device=self.device)
+            ep = E.data_ptr()
+            if want_eout and Eout is None:
+                Eout = torch.empty((self.edge_slots, self.heads, self.head_dim), dtype=odt, device=self.device)
+        elif Xe is not None or We is not None:
+            raise ValueError("Xe / We are only valid for an RTMScore plan")
+        if O is None:
+            O = torch.empty((self.num_nodes, self.heads, self.head_dim), dtype=odt, device=self.device)
+        o = _dev_ptr(O, "O", odt, self._node_numel(), self.device)
+        eo = Eout.data_ptr() if Eout is not None else None
+        with torch.cuda.device(self.device):
+            _check(self._lib.g3s_layer_forward(self.handle, x, wqkv, kin, xe, we, ke, Q.data_ptr(), K.data_ptr(),
+                                               V.data_ptr(), ep, o, eo, _stream_handle(stream)))
+        out = (O, Eout) if want_eout else O
+        return out, (Q, K, V, E)
+
     def aggregate(self, W, X, O=None, normalize: bool = False, eps: float = 1e-6, stream=None):
         """``g3s_aggregate``: O_i = sum_e W[e] X[src(e)] (optionally / (sum_e W[e] + eps))."""
         torch = _torch()
@@ -390,6 +430,32 @@ class Plan:
         return staging
 
 
+def linear(X, W, seg_cols: Optional[int] = None, out_dtype: Optional[str] = None, outs=None, status=None,
+           stream=None):
+    """``g3s_linear``: Y = X W^T for X (M, Kin) and W (Nout, Kin), 16-bit, on
+    the tensor cores.  Returns a list of Nout / seg_cols outputs of shape
+    (M, seg_cols) (default seg_cols = Nout)."""
+    torch = _torch()
+    lib = load_library()
+    names = {torch.float16: "f16", torch.bfloat16: "bf16"}
+    if X.dtype not in names:
+        raise TypeError("X must be fp16 or bf16")
+    dt = names[X.dtype]
+    M, kin = int(X.shape[0]), int(X.shape[-1])
+    nout = int(W.shape[0])
+    seg = int(seg_cols or nout)
+    odt = out_dtype or dt
+    if outs is None:
+        outs = [torch.empty((M, seg), dtype=torch_dtype(odt), device=X.device) for _ in range(nout // seg)]
+    ptrs = (ctypes.c_void_p * len(outs))(*[_dev_ptr(o, "Y", torch_dtype(odt), M * seg, X.device) for o in outs])
+    st = _dev_ptr(status, "status", torch.int32, 1, X.device) if status is not None else None
+    with torch.cuda.device(X.device):
+        _check(lib.g3s_linear(_dev_ptr(X, "X", X.dtype, M * kin, X.device), _dev_ptr(W, "W", X.dtype, nout * kin,
+                                                                                  X.device),
+                              M, kin, nout, DTYPES[dt], ptrs, seg, DTYPES[odt], st, _stream_handle(stream)))
+    return outs
+
+
 def forward_noalloc(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant, Q, K, V, E=None, O=None,
                     Eout=None, stream=None):
     """``g3s_forward_noalloc``: plan + forward in one call using the library's
@@ -415,5 +481,5 @@ def forward_noalloc(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant
     return (O, Eout) if Eout is not None else O
 
 
-__all__ = ["forward_noalloc","Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
+__all__ = ["forward_noalloc", "linear", "Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
            "DTYPES", "VARIANTS", "ARRAYS", "EXPORTED", "LIB_PATH"]

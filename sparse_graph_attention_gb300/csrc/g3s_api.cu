@@ -602,6 +602,58 @@ g3s_status g3s_selftest_wait_timeout(const g3s_plan* p, uint64_t limit_ns, g3s_s
     return g3s_forward_check(p, stream_);
 }
 
+g3s_status g3s_linear(const void* X, const void* W, int64_t M, int Kin, int Nout, g3s_dtype dtype, void* const* Y,
+                      int seg_cols, g3s_dtype out_dtype, int32_t* status_d, g3s_stream_t stream_) {
+    if (M < 0 || Kin <= 0 || Nout <= 0 || seg_cols <= 0) return fail(G3S_ERR_INVALID_ARG, "negative or zero size");
+    if (dtype != G3S_F16 && dtype != G3S_BF16) return fail(G3S_ERR_UNSUPPORTED, "g3s_linear takes fp16 or bf16 inputs");
+    if (out_dtype != G3S_F32 && out_dtype != dtype)
+        return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
+    if (Kin % 8 != 0 || seg_cols % 64 != 0 || Nout % seg_cols != 0 || Nout / seg_cols > 3)
+        return fail(G3S_ERR_INVALID_ARG, "need Kin %% 8 == 0, seg_cols %% 64 == 0, Nout = 1..3 x seg_cols");
+    if (M > 0x7fffffffLL) return fail(G3S_ERR_INVALID_ARG, "M must fit in int32");
+    if (M == 0) return G3S_OK;
+    if (!X || !W || !Y) return fail(G3S_ERR_INVALID_ARG, "X, W and Y must be non-NULL");
+    const int nseg = Nout / seg_cols;
+    LinearParams lp{};
+    lp.A = X;
+    lp.W = W;
+    for (int i = 0; i < nseg; ++i) {
+        if (!Y[i] || !aligned16(Y[i])) return fail(G3S_ERR_INVALID_ARG, "output %d is NULL or not 16-byte aligned", i);
+        lp.out[i] = Y[i];
+    }
+    if (!aligned16(X) || !aligned16(W)) return fail(G3S_ERR_INVALID_ARG, "X and W must be 16-byte aligned");
+    if (!linear_supported(dtype, out_dtype, Kin, seg_cols)) return fail(G3S_ERR_UNSUPPORTED, "shape without a kernel");
+    if (!tensor_maps_available()) return fail(G3S_ERR_UNSUPPORTED, "the driver offers no tensor-map encoding");
+    lp.seg_cols = seg_cols;
+    lp.M = M;
+    lp.Kin = Kin;
+    lp.Nout = Nout;
+    lp.status = status_d;
+    CUDA_OR_FAIL(linear_launch(dtype, out_dtype, lp, reinterpret_cast<cudaStream_t>(stream_)), "projection launch");
+    return G3S_OK;
+}
+
+g3s_status g3s_layer_forward(const g3s_plan* p, const void* X, const void* Wqkv, int Kin, const void* Xe,
+                             const void* We, int Ke, void* Q, void* K, void* V, void* Eproj, void* O, void* Eout,
+                             g3s_stream_t stream_) {
+    if (!p) return fail(G3S_ERR_INVALID_ARG, "NULL plan");
+    const bool rtm = p->variant == G3S_RTMSCORE;
+    if (p->dtype != G3S_F16 && p->dtype != G3S_BF16) return fail(G3S_ERR_UNSUPPORTED, "layer needs a 16-bit plan");
+    const int hd = p->shape.H * p->shape.D;
+    if (rtm != (Xe != nullptr || We != nullptr))
+        return fail(G3S_ERR_INVALID_ARG, "Xe / We are needed for an RTMScore plan and only then");
+    const g3s_dtype dt = (g3s_dtype)p->dtype;
+    void* qkv[3] = {Q, K, V};
+    g3s_status st = g3s_linear(X, Wqkv, p->shape.N, Kin, 3 * hd, dt, qkv, hd, dt, p->arr.fwd_status, stream_);
+    if (st != G3S_OK) return st;
+    if (rtm) {
+        void* e1[1] = {Eproj};
+        st = g3s_linear(Xe, We, p->edge_slots, Ke, hd, dt, e1, hd, dt, p->arr.fwd_status, stream_);
+        if (st != G3S_OK) return st;
+    }
+    return g3s_forward(p, Q, K, V, rtm ? Eproj : nullptr, O, rtm ? Eout : nullptr, stream_);
+}
+
 void g3s_plan_destroy(g3s_plan* p) { delete p; }
 
 }  // extern "C"

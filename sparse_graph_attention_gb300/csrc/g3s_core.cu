@@ -58,6 +58,18 @@ bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_ele
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tile16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_rows, int box_elems) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr || rows < 1) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_elems, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool core_supported(int dtype, int row_vecs) {
     if (dtype < 0 || dtype > 2) return false;
     if (row_vecs < 1 || row_vecs > 256 || (row_vecs & (row_vecs - 1))) return false;

@@ -142,6 +142,9 @@ struct MergeParams {
 // 128-byte swizzle (box_elems * 2 must then be 128).
 bool tensor_maps_available();
 bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128);
+// A 2-D map over `rows` rows of `row_elems` 16-bit elements with a box of
+// box_rows x box_elems and the 128-byte swizzle (box_elems * 2 == 128).
+bool encode_tile16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_rows, int box_elems);
 
 bool core_supported(int dtype, int row_vecs);
 // The TMA-fed form (g3s_core_tma.cuh): standard mode, 16-bit inputs, row_vecs 8, 16 or 32.
@@ -181,6 +184,19 @@ bool tile_supported(int dtype, int variant, int head_dim);
 cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st);
 cudaError_t tile_launch(int dtype, int out_dtype, const TileParams& p, cudaStream_t st);
 
+
+// ---- dense projection on the tensor cores (g3s_linear.cu) -------------------
+struct LinearParams {
+    const void* A;    // X (M, Kin) row-major
+    const void* W;    // W (Nout, Kin) row-major
+    void* out[3];     // output segments, each (M, seg_cols) row-major
+    int seg_cols;
+    long long M;
+    int Kin, Nout;
+    int32_t* status;  // kErrTimeout is OR-ed in when a bounded wait gives up (may be null)
+};
+bool linear_supported(int dtype, int out_dtype, int kin, int seg_cols);
+cudaError_t linear_launch(int dtype, int out_dtype, const LinearParams& p, cudaStream_t st);
 
 // ---- host helpers shared by the ABI translation units (g3s_api.cu) ---------
 namespace api {

@@ -1,0 +1,347 @@
+// Dense projection Y = X W^T on the tensor cores (tcgen05.mma, TMEM
+// accumulators, TMA tiles).
+//
+// This is the projection of node (or edge) features into the queries, keys
+// and values that the attention consumes (the Triton article,
+// stondelli.it/articles/gattn-triton, notes that once the attention is fused
+// these GEMMs take most of the time).  X is (M, Kin) row-major, W is
+// (Nout, Kin) row-major -- the layout of a linear layer's weight -- so both
+// operands are K-major.  The Nout output columns are written to up to three
+// row-major outputs of seg_cols columns each (Q | K | V of a layer).
+//
+// Kernel: persistent CTAs over 128 x BN output tiles (BN = 128, or 64 when
+// seg_cols is not a multiple of 128), tiles in row-block-major order so the
+// CTAs in flight share X row blocks through L2.  Six warps:
+//   warp 0, one thread: TMA loads of the X and W tiles of each 64-wide K
+//     step (128-byte swizzle) into a ring of 4 stages;
+//   warp 1, one thread: tcgen05.mma (M = 128, N = BN, K = 16 per
+//     instruction) into one of two TMEM accumulators, alternating by tile so
+//     the epilogue of a tile overlaps the MMAs of the next;
+//   warps 2-5: the epilogue, one output row per thread (tcgen05.ld of the
+//     accumulator row, conversion, 16-byte stores).
+// Every mbarrier wait is bounded (1 s of %globaltimer, or until another role
+// has given up); on expiry the kernel records kErrTimeout in the status word,
+// lets the copies and MMAs in flight finish, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "g3s_internal.h"
+#include "g3s_ptx.cuh"
+
+namespace g3s {
+namespace {
+
+constexpr int kBM = 128;        // output rows per tile (MMA M)
+constexpr int kBK = 64;         // K per stage: 64 16-bit elements = one 128-byte swizzle row
+constexpr int kStagesL = 4;
+constexpr int kWarpsL = 6;
+constexpr uint64_t kLimitL = 1000000000ull;
+
+template <int BN>
+struct __align__(1024) LinSmem {
+    uint8_t a[kStagesL][kBM * 128];  // X tile: 128 rows x 64 K (K-major, 128-byte swizzle)
+    uint8_t b[kStagesL][BN * 128];   // W tile: BN rows x 64 K
+    uint64_t full[kStagesL], empty[kStagesL];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void mbar_arrive_l(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 2-D TMA tile load of the box at element coordinates (x, y) into dst.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_l(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                      uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void commit_l(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t sdesc_l(uint32_t saddr) {  // K-major, 128-byte swizzle, 8-row groups 1024 B apart
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+__host__ __device__ constexpr uint32_t idesc_l(bool bf16, int M, int N) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+template <int BN>
+__device__ __forceinline__ bool wait_l(LinSmem<BN>& sm, uint32_t bar, uint32_t parity) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int*>(&sm.abort)) return false;
+        if (ptx::globaltimer() - t0 > kLimitL) {
+            *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+            return false;
+        }
+    }
+}
+
+// 32 fp32 values -> out type, stored at dst (16-byte aligned)
+template <typename OutT>
+__device__ __forceinline__ void store32(OutT* dst, const uint32_t (&r)[32]) {
+    if constexpr (std::is_same<OutT, float>::value) {
+        float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                               __uint_as_float(r[4 * i + 3]));
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a = __uint_as_float(r[8 * i + 2 * k]), b = __uint_as_float(r[8 * i + 2 * k + 1]);
+                if constexpr (std::is_same<OutT, __half>::value) {
+                    __half2 h = __floats2half2_rn(a, b);
+                    w[k] = *reinterpret_cast<uint32_t*>(&h);
+                } else {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+                    w[k] = *reinterpret_cast<uint32_t*>(&h);
+                }
+            }
+            d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+template <typename T, typename OutT, int BN>
+__global__ void __launch_bounds__(kWarpsL * 32, 1)
+    linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb) {
+    extern __shared__ uint8_t lin_smem_raw[];
+    LinSmem<BN>& sm =
+        *reinterpret_cast<LinSmem<BN>*>((reinterpret_cast<uintptr_t>(lin_smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr bool kBf16 = !std::is_same<T, __half>::value;
+    constexpr uint32_t kId = idesc_l(kBf16, kBM, BN);
+    constexpr uint32_t kStageBytes = (kBM + BN) * 128;
+    const long long m_tiles = (p.M + kBM - 1) / kBM;
+    const int n_tiles = (p.Nout + BN - 1) / BN;
+    const long long tiles = m_tiles * n_tiles;
+    const int k_steps = (p.Kin + kBK - 1) / kBK;
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         ptx::smem_u32(&sm.tmem_base)),
+                     "r"(2 * BN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesL; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&sm.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sm.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&sm.acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sm.acc_empty[b]), 128);
+        }
+        ptx::mbar_init(ptx::smem_u32(&sm.mma_done), 1);
+        sm.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {  // loads
+            uint32_t it = 0;  // stage uses
+            bool ok = true;
+            for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int m0 = (int)(t / n_tiles) * kBM, n0 = (int)(t % n_tiles) * BN;
+                for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                    const int s = (int)(it % kStagesL);
+                    const uint32_t u = it / kStagesL;
+                    if (u >= 1 && !wait_l(sm, ptx::smem_u32(&sm.empty[s]), (u - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = ptx::smem_u32(&sm.full[s]);
+                    ptx::mbar_arrive_expect_tx(bar, kStageBytes);
+                    tma_load_2d(ptx::smem_u32(sm.a[s]), &ta, ks * kBK, m0, bar);
+                    tma_load_2d(ptx::smem_u32(sm.b[s]), &tb, ks * kBK, n0, bar);
+                }
+            }
+            // every armed copy lands before the CTA may exit
+            for (int s = 0; s < kStagesL; ++s) {
+                const uint32_t uses = it / kStagesL + ((uint32_t)s < it % kStagesL ? 1u : 0u);
+                if (uses > 0) ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full[s]), (uses - 1) & 1, kLimitL);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMAs
+            uint32_t it = 0, tl = 0;  // stage uses, local tiles
+            bool ok = true;
+            for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tl) {
+                const uint32_t buf = tl & 1, use = tl >> 1;
+                if (use >= 1 && !wait_l(sm, ptx::smem_u32(&sm.acc_empty[buf]), (use - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_after();
+                const uint32_t d = tmem + buf * BN;
+                for (int ks = 0; ks < k_steps; ++ks, ++it) {
+                    const int s = (int)(it % kStagesL);
+                    if (!wait_l(sm, ptx::smem_u32(&sm.full[s]), (it / kStagesL) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_after();
+                    const uint32_t a = ptx::smem_u32(sm.a[s]), b = ptx::smem_u32(sm.b[s]);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_l(d, sdesc_l(a + kk * 32), sdesc_l(b + kk * 32), kId, (ks > 0 || kk > 0) ? 1u : 0u);
+                    commit_l(ptx::smem_u32(&sm.empty[s]));  // the stage is free once these MMAs are done
+                }
+                if (ok) commit_l(ptx::smem_u32(&sm.acc_full[buf]));
+            }
+            commit_l(ptx::smem_u32(&sm.mma_done));
+            ptx::mbar_wait_bounded(ptx::smem_u32(&sm.mma_done), 0, kLimitL);
+        }
+        __syncwarp();
+    } else {  // epilogue: warps 2-5, TMEM lane quarter warp % 4
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        uint32_t tl = 0;
+        for (long long t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
+            const uint32_t buf = tl & 1, use = tl >> 1;
+            if (!__all_sync(0xffffffffu, wait_l(sm, ptx::smem_u32(&sm.acc_full[buf]), use & 1))) break;
+            tc_after();
+            const long long m = (t / n_tiles) * kBM + row;
+            const int n0 = (int)(t % n_tiles) * BN;
+            const int seg = n0 / p.seg_cols, c0 = n0 - seg * p.seg_cols;
+            OutT* out = static_cast<OutT*>(p.out[seg]);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + buf * BN + c, r);  // warp-collective: every row takes part
+                if (m < p.M && n0 + c < p.Nout) store32<OutT>(out + m * p.seg_cols + c0 + c, r);
+            }
+            tc_before();
+            mbar_arrive_l(ptx::smem_u32(&sm.acc_empty[buf]));
+        }
+    }
+
+    tc_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && sm.abort && p.status != nullptr) atomicOr(p.status, (int32_t)kErrTimeout);
+    if (warp == 1) {
+        tc_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
+    }
+}
+
+struct LinMaps {
+    const void* A = nullptr;
+    const void* B = nullptr;
+    long long M = -1;
+    int Kin = 0, Nout = 0, BN = 0;
+    CUtensorMap a, b;
+};
+thread_local LinMaps lin_maps;
+
+// A 2-D K-major map: rows x kin 16-bit elements, box of box_rows x 64, 128-byte swizzle.
+bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, int kin, int box_rows);
+
+template <typename T, typename OutT, int BN>
+cudaError_t launch_lin(const LinearParams& p, cudaStream_t st) {
+    LinMaps& mp = lin_maps;
+    if (mp.A != p.A || mp.B != p.W || mp.M != p.M || mp.Kin != p.Kin || mp.Nout != p.Nout || mp.BN != BN) {
+        mp.A = nullptr;
+        if (!encode_kmajor(&mp.a, p.A, p.M, p.Kin, kBM) || !encode_kmajor(&mp.b, p.W, p.Nout, p.Kin, BN))
+            return cudaErrorInvalidValue;
+        mp.A = p.A;
+        mp.B = p.W;
+        mp.M = p.M;
+        mp.Kin = p.Kin;
+        mp.Nout = p.Nout;
+        mp.BN = BN;
+    }
+    const int smem = (int)sizeof(LinSmem<BN>) + 1024;
+    static int cached_dev = -1, sms = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != cached_dev) {
+        e = cudaFuncSetAttribute(linear_kernel<T, OutT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cached_dev = dev;
+    }
+    const long long tiles = ((p.M + kBM - 1) / kBM) * ((p.Nout + BN - 1) / BN);
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    linear_kernel<T, OutT, BN><<<grid, kWarpsL * 32, smem, st>>>(p, mp.a, mp.b);
+    return cudaGetLastError();
+}
+
+template <typename T, typename OutT>
+cudaError_t launch_lin_bn(const LinearParams& p, cudaStream_t st) {
+    if (p.seg_cols % 128 == 0) return launch_lin<T, OutT, 128>(p, st);
+    return launch_lin<T, OutT, 64>(p, st);
+}
+
+bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, int kin, int box_rows) {
+    return encode_tile16(m, base, rows, kin, box_rows, kBK);
+}
+
+}  // namespace
+
+bool linear_supported(int dtype, int out_dtype, int kin, int seg_cols) {
+    if (dtype != G3S_F16 && dtype != G3S_BF16) return false;
+    if (out_dtype != G3S_F32 && out_dtype != dtype) return false;
+    // rows of X and W must be 16-byte multiples for TMA; output segments of whole 64-column tiles
+    return kin >= 8 && kin % 8 == 0 && seg_cols >= 64 && seg_cols % 64 == 0;
+}
+
+cudaError_t linear_launch(int dtype, int out_dtype, const LinearParams& p, cudaStream_t st) {
+    if (p.M <= 0) return cudaSuccess;
+    if (!tensor_maps_available()) return cudaErrorNotSupported;
+    if (dtype == G3S_BF16) {
+        if (out_dtype == G3S_F32) return launch_lin_bn<__nv_bfloat16, float>(p, st);
+        return launch_lin_bn<__nv_bfloat16, __nv_bfloat16>(p, st);
+    }
+    if (out_dtype == G3S_F32) return launch_lin_bn<__half, float>(p, st);
+    return launch_lin_bn<__half, __half>(p, st);
+}
+
+}  // namespace g3s

@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 import torch
 
+import graphgen
 import oracle
 import pins
 
@@ -61,3 +62,46 @@ def test_bad_index_is_reported():
     x = np.zeros((2, 1, 4), np.float32)
     with pytest.raises(ValueError):
         oracle.forward(rp, col, 2, 1, 4, "f32", "standard", x, x, x)
+
+
+# ---------------------------------------------------------------------------
+# the projection Y = X W^T and the 16-bit store
+# ---------------------------------------------------------------------------
+def test_linear_matches_brute_force():
+    """oracle.linear against a triple loop on the widened values, rectangular
+    and square (a transposed weight would fail the square case)."""
+    rng = np.random.default_rng(7)
+    for dt in ("bf16", "f16"):
+        for (m, nout, kin) in ((5, 7, 12), (6, 6, 6)):
+            X = graphgen.to_dtype(rng.standard_normal((m, kin)).astype(np.float32), dt)
+            W = graphgen.to_dtype(rng.standard_normal((nout, kin)).astype(np.float32), dt)
+            Y = oracle.linear(X, W, dt)
+            x, w = oracle.decode(dt, X), oracle.decode(dt, W)
+            for i in range(m):
+                for j in range(nout):
+                    acc = 0.0
+                    for k in range(kin):
+                        acc += x[i, k] * w[j, k]
+                    assert abs(Y[i, j] - acc) <= 1e-12 * (1.0 + abs(acc))
+
+
+def test_linear_selects_rows_of_w():
+    """W with one 1 per row picks columns of X exactly (Y[:, j] = X[:, perm[j]])."""
+    rng = np.random.default_rng(8)
+    kin, nout = 16, 10
+    perm = rng.integers(0, kin, nout)
+    Wn = np.zeros((nout, kin), np.float32)
+    Wn[np.arange(nout), perm] = 1.0
+    X = graphgen.to_dtype(rng.standard_normal((9, kin)).astype(np.float32), "bf16")
+    Y = oracle.linear(X, graphgen.to_dtype(Wn, "bf16"), "bf16")
+    assert np.array_equal(Y, oracle.decode("bf16", X)[:, perm])
+
+
+def test_round_to_ties_and_ranges():
+    """Round to nearest even at the bf16 / fp16 half-ulp points."""
+    one = 1.0
+    assert oracle.round_to(np.array([one + 2.0 ** -8]), "bf16")[0] == 1.0          # tie -> even
+    assert oracle.round_to(np.array([one + 3 * 2.0 ** -9]), "bf16")[0] == one + 2.0 ** -7
+    assert oracle.round_to(np.array([one + 2.0 ** -11]), "f16")[0] == 1.0          # tie -> even
+    assert oracle.round_to(np.array([one + 3 * 2.0 ** -12]), "f16")[0] == one + 2.0 ** -10
+    assert oracle.round_to(np.array([-2.5]), "bf16")[0] == -2.5
