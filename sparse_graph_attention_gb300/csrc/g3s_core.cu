@@ -58,15 +58,17 @@ bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_ele
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_tile16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_rows, int box_elems) {
+bool encode_tile(CUtensorMap* m, const void* base, long long rows, int row_elems, int elem_bytes, int box_rows,
+                 int box_elems) {
     EncodeTiledFn enc = tensor_map_encoder();
-    if (enc == nullptr || rows < 1) return false;
+    if (enc == nullptr || rows < 1 || (elem_bytes != 2 && elem_bytes != 4)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem_bytes};
     const cuuint32_t box[2] = {(cuuint32_t)box_elems, (cuuint32_t)box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+               const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -142,9 +142,11 @@ struct MergeParams {
 // 128-byte swizzle (box_elems * 2 must then be 128).
 bool tensor_maps_available();
 bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128);
-// A 2-D map over `rows` rows of `row_elems` 16-bit elements with a box of
-// box_rows x box_elems and the 128-byte swizzle (box_elems * 2 == 128).
-bool encode_tile16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_rows, int box_elems);
+// A 2-D map over `rows` rows of `row_elems` elements of elem_bytes (2 or 4)
+// with a box of box_rows x box_elems and the 128-byte swizzle
+// (box_elems * elem_bytes == 128).
+bool encode_tile(CUtensorMap* m, const void* base, long long rows, int row_elems, int elem_bytes, int box_rows,
+                 int box_elems);
 
 bool core_supported(int dtype, int row_vecs);
 // The TMA-fed form (g3s_core_tma.cuh): standard mode, 16-bit inputs, row_vecs 8, 16 or 32.

@@ -9,16 +9,17 @@
 // operands are K-major.  The Nout output columns are written to up to three
 // row-major outputs of seg_cols columns each (Q | K | V of a layer).
 //
-// Kernel: persistent CTAs over 128 x BN output tiles (BN = 128, or 64 when
-// seg_cols is not a multiple of 128), tiles in row-block-major order so the
+// Kernel: persistent CTAs over 128 x BN output tiles (BN = 256, 128 or 64 by
+// what seg_cols allows), tiles in row-block-major order so the
 // CTAs in flight share X row blocks through L2.  Six warps:
 //   warp 0, one thread: TMA loads of the X and W tiles of each 64-wide K
 //     step (128-byte swizzle) into a ring of 4 stages;
 //   warp 1, one thread: tcgen05.mma (M = 128, N = BN, K = 16 per
 //     instruction) into one of two TMEM accumulators, alternating by tile so
 //     the epilogue of a tile overlaps the MMAs of the next;
-//   warps 2-5: the epilogue, one output row per thread (tcgen05.ld of the
-//     accumulator row, conversion, 16-byte stores).
+//   warps 2-5: the epilogue, one output row per thread: tcgen05.ld of the
+//     accumulator row, conversion into a 128-byte-swizzled staging block in
+//     shared memory, and a TMA tile store of each 128 x 128-byte block.
 // Every mbarrier wait is bounded (1 s of %globaltimer, or until another role
 // has given up); on expiry the kernel records kErrTimeout in the status word,
 // lets the copies and MMAs in flight finish, frees TMEM and returns.
@@ -43,6 +44,7 @@ template <int BN>
 struct __align__(1024) LinSmem {
     uint8_t a[kStagesL][kBM * 128];  // X tile: 128 rows x 64 K (K-major, 128-byte swizzle)
     uint8_t b[kStagesL][BN * 128];   // W tile: BN rows x 64 K
+    uint8_t o[2][kBM * 128];         // output staging: 128 rows x 128 bytes (128-byte swizzle), two buffers
     uint64_t full[kStagesL], empty[kStagesL];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
@@ -63,6 +65,33 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
             "r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// 2-D TMA tile store of the box at (x, y) from shared memory src.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of all but the newest `n` committed stores have been read
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// the 128 epilogue threads
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the same barrier, returning whether `ok` holds on all 128 threads (so that
+// they all leave the loop together: a named barrier has no timeout)
+__device__ __forceinline__ bool epi_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void mma_l(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -111,23 +140,22 @@ __device__ __forceinline__ bool wait_l(LinSmem<BN>& sm, uint32_t bar, uint32_t p
     }
 }
 
-// 32 fp32 values -> out type, stored at dst (16-byte aligned)
+// One row of a 128-byte output block into the staging buffer (128-byte
+// swizzle: 16-byte chunk x of row r at r * 128 + ((x ^ (r & 7)) << 4)) from
+// 128 / sizeof(OutT) fp32 accumulator values.
 template <typename OutT>
-__device__ __forceinline__ void store32(OutT* dst, const uint32_t (&r)[32]) {
-    if constexpr (std::is_same<OutT, float>::value) {
-        float4* d = reinterpret_cast<float4*>(dst);
+__device__ __forceinline__ void stage_row(uint32_t buf, int row, const uint32_t* r) {
+    const uint32_t base = buf + row * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
-                               __uint_as_float(r[4 * i + 3]));
-    } else {
-        uint4* d = reinterpret_cast<uint4*>(dst);
+    for (int x = 0; x < 8; ++x) {
+        uint32_t w[4];
+        if constexpr (std::is_same<OutT, float>::value) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t w[4];
+            for (int k = 0; k < 4; ++k) w[k] = r[4 * x + k];
+        } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float a = __uint_as_float(r[8 * i + 2 * k]), b = __uint_as_float(r[8 * i + 2 * k + 1]);
+                const float a = __uint_as_float(r[8 * x + 2 * k]), b = __uint_as_float(r[8 * x + 2 * k + 1]);
                 if constexpr (std::is_same<OutT, __half>::value) {
                     __half2 h = __floats2half2_rn(a, b);
                     w[k] = *reinterpret_cast<uint32_t*>(&h);
@@ -136,14 +164,18 @@ __device__ __forceinline__ void store32(OutT* dst, const uint32_t (&r)[32]) {
                     w[k] = *reinterpret_cast<uint32_t*>(&h);
                 }
             }
-            d[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + ((x ^ (row & 7)) << 4)), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
     }
 }
 
 template <typename T, typename OutT, int BN>
 __global__ void __launch_bounds__(kWarpsL * 32, 1)
-    linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb) {
+    linear_kernel(const LinearParams p, const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                  const __grid_constant__ CUtensorMap to0, const __grid_constant__ CUtensorMap to1,
+                  const __grid_constant__ CUtensorMap to2) {
     extern __shared__ uint8_t lin_smem_raw[];
     LinSmem<BN>& sm =
         *reinterpret_cast<LinSmem<BN>*>((reinterpret_cast<uintptr_t>(lin_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -239,26 +271,46 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
         }
         __syncwarp();
     } else {  // epilogue: warps 2-5, TMEM lane quarter warp % 4
+        // A tile leaves in blocks of 128 bytes per row (64 16-bit or 32 fp32
+        // columns): every thread converts its row of the block into a staging
+        // buffer, then one thread stores the block with TMA.  Two buffers: a
+        // buffer is rewritten only after the store two blocks back has read it.
+        constexpr int kBC = 128 / (int)sizeof(OutT);  // output columns per block
         const int row = 32 * (warp & 3) + lane;
+        const bool leader = threadIdx.x == 64;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        uint32_t tl = 0;
+        const CUtensorMap* maps[3] = {&to0, &to1, &to2};
+        uint32_t tl = 0, blocks = 0;
         for (long long t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
-            if (!__all_sync(0xffffffffu, wait_l(sm, ptx::smem_u32(&sm.acc_full[buf]), use & 1))) break;
+            if (!epi_all(wait_l(sm, ptx::smem_u32(&sm.acc_full[buf]), use & 1))) break;
             tc_after();
-            const long long m = (t / n_tiles) * kBM + row;
+            const int m0 = (int)(t / n_tiles) * kBM;
             const int n0 = (int)(t % n_tiles) * BN;
             const int seg = n0 / p.seg_cols, c0 = n0 - seg * p.seg_cols;
-            OutT* out = static_cast<OutT*>(p.out[seg]);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + buf * BN + c, r);  // warp-collective: every row takes part
-                if (m < p.M && n0 + c < p.Nout) store32<OutT>(out + m * p.seg_cols + c0 + c, r);
+            for (int j = 0; j < BN / kBC; ++j, ++blocks) {
+                const uint32_t sb = ptx::smem_u32(sm.o[blocks & 1]);
+                if (leader && blocks >= 2) bulk_wait_read<1>();
+                epi_sync();  // the staging buffer is free
+                uint32_t r[32 * (kBC / 32)];
+#pragma unroll
+                for (int q = 0; q < kBC / 32; ++q)
+                    tmem_ld32(tmem + lane_off + buf * BN + j * kBC + q * 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * q));
+                if (j == BN / kBC - 1) {  // the accumulator is read: the MMAs may reuse it
+                    tc_before();
+                    mbar_arrive_l(ptx::smem_u32(&sm.acc_empty[buf]));
+                }
+                stage_row<OutT>(sb, row, r);
+                ptx::fence_proxy_async_smem();
+                epi_sync();  // the block is staged
+                if (leader) {
+                    tma_store_2d(maps[seg], c0 + j * kBC, m0, sb);
+                    bulk_commit();
+                }
             }
-            tc_before();
-            mbar_arrive_l(ptx::smem_u32(&sm.acc_empty[buf]));
         }
+        if (leader) bulk_wait_all();  // the stores have completed before the CTA exits
     }
 
     tc_before();
@@ -273,9 +325,10 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
 struct LinMaps {
     const void* A = nullptr;
     const void* B = nullptr;
+    const void* O[3] = {nullptr, nullptr, nullptr};
     long long M = -1;
-    int Kin = 0, Nout = 0, BN = 0;
-    CUtensorMap a, b;
+    int Kin = 0, Nout = 0, BN = 0, seg = 0, esz = 0;
+    CUtensorMap a, b, o[3];
 };
 thread_local LinMaps lin_maps;
 
@@ -285,16 +338,28 @@ bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, int kin, in
 template <typename T, typename OutT, int BN>
 cudaError_t launch_lin(const LinearParams& p, cudaStream_t st) {
     LinMaps& mp = lin_maps;
-    if (mp.A != p.A || mp.B != p.W || mp.M != p.M || mp.Kin != p.Kin || mp.Nout != p.Nout || mp.BN != BN) {
+    constexpr int esz = (int)sizeof(OutT);
+    const int nseg = p.Nout / p.seg_cols;
+    bool same = mp.A == p.A && mp.B == p.W && mp.M == p.M && mp.Kin == p.Kin && mp.Nout == p.Nout && mp.BN == BN &&
+                mp.seg == p.seg_cols && mp.esz == esz;
+    for (int i = 0; i < 3; ++i) same = same && mp.O[i] == (i < nseg ? p.out[i] : nullptr);
+    if (!same) {
         mp.A = nullptr;
         if (!encode_kmajor(&mp.a, p.A, p.M, p.Kin, kBM) || !encode_kmajor(&mp.b, p.W, p.Nout, p.Kin, BN))
             return cudaErrorInvalidValue;
+        for (int i = 0; i < 3; ++i) {  // unused segments get a copy of the first map (never stored through)
+            if (!encode_tile(&mp.o[i], p.out[i < nseg ? i : 0], p.M, p.seg_cols, esz, kBM, 128 / esz))
+                return cudaErrorInvalidValue;
+            mp.O[i] = i < nseg ? p.out[i] : nullptr;
+        }
         mp.A = p.A;
         mp.B = p.W;
         mp.M = p.M;
         mp.Kin = p.Kin;
         mp.Nout = p.Nout;
         mp.BN = BN;
+        mp.seg = p.seg_cols;
+        mp.esz = esz;
     }
     const int smem = (int)sizeof(LinSmem<BN>) + 1024;
     static int cached_dev = -1, sms = 0;
@@ -310,18 +375,22 @@ cudaError_t launch_lin(const LinearParams& p, cudaStream_t st) {
     }
     const long long tiles = ((p.M + kBM - 1) / kBM) * ((p.Nout + BN - 1) / BN);
     const int grid = (int)(tiles < sms ? tiles : sms);
-    linear_kernel<T, OutT, BN><<<grid, kWarpsL * 32, smem, st>>>(p, mp.a, mp.b);
+    linear_kernel<T, OutT, BN><<<grid, kWarpsL * 32, smem, st>>>(p, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2]);
     return cudaGetLastError();
 }
 
+// Tile width: 256 columns where the segments allow it and K is long enough
+// for the MMAs to matter (the operand reads of an N = 128 MMA alone fill the
+// shared-memory bandwidth), else 128, else 64.
 template <typename T, typename OutT>
 cudaError_t launch_lin_bn(const LinearParams& p, cudaStream_t st) {
+    if (p.seg_cols % 256 == 0 && p.Kin >= 256) return launch_lin<T, OutT, 256>(p, st);
     if (p.seg_cols % 128 == 0) return launch_lin<T, OutT, 128>(p, st);
     return launch_lin<T, OutT, 64>(p, st);
 }
 
 bool encode_kmajor(CUtensorMap* m, const void* base, long long rows, int kin, int box_rows) {
-    return encode_tile16(m, base, rows, kin, box_rows, kBK);
+    return encode_tile(m, base, rows, kin, 2, box_rows, kBK);
 }
 
 }  // namespace
