@@ -53,6 +53,17 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
 
 
+def measured_bf16_peak(sustained: bool):
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d[key]), "measured (MEASURED_PEAKS.json %s)" % key
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
 def kernel_sources_hash() -> str:
     csrc = os.path.join(ROOT, "sparse_graph_attention_gb300", "csrc")
     h = hashlib.sha256()
@@ -210,6 +221,9 @@ def parse_args():
                     help="density cutoff of the tile path in 1/1000 (default: the library's)")
     ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
                     help="element type of O (default fp32)")
+    ap.add_argument("--layer", type=int, default=0, metavar="KIN",
+                    help="also time one attention layer on 16-bit workloads: Q|K|V = X Wqkv^T for X of KIN "
+                         "features (the tcgen05 projection), then the forward; adds a 'layer' object")
     ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
                     help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -246,6 +260,69 @@ def run_reference(args, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def time_layer(args, g, w, plan, O, Eout, stream, dev):
+    """One attention layer: Q|K|V = X Wqkv^T (g3s_linear, tensor cores) then the
+    fused forward, on seeded synthetic features and weights of the workload's
+    shape; the projection alone is timed too and set against its roofline."""
+    import torch
+    import sparse_graph_attention_gb300 as g3s
+    if w.dtype not in ("bf16", "f16"):
+        return {"unavailable": "the projection takes 16-bit inputs; this workload is %s" % w.dtype}
+    kin = int(args.layer)
+    hd = w.heads * w.head_dim
+    tdt = g3s.torch_dtype(w.dtype)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + w.number)
+    X = torch.randn(g.num_nodes, kin, device=dev, generator=gen).to(tdt)
+    Wqkv = (torch.randn(3 * hd, kin, device=dev, generator=gen) * kin ** -0.5).to(tdt)
+    Xe = We = None
+    if w.variant == "rtmscore":
+        Xe = torch.randn(g.num_edges, kin, device=dev, generator=gen).to(tdt)
+        We = (torch.randn(hd, kin, device=dev, generator=gen) * kin ** -0.5).to(tdt)
+    qkv = [torch.empty(g.num_nodes, hd, dtype=tdt, device=dev) for _ in range(3)]
+
+    def layer_step():
+        plan.layer_forward(X, Wqkv, Xe, We, O=O, Eout=Eout)
+
+    def proj_step():
+        g3s.linear(X, Wqkv, seg_cols=hd, outs=qkv, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    n = max(3, min(args.steps, 50))
+    layer_ms = timed(layer_step, n)
+    proj_ms = timed(proj_step, n)
+    flops = 2.0 * g.num_nodes * kin * 3 * hd
+    nbytes = 2.0 * (g.num_nodes * kin + 3 * hd * kin + g.num_nodes * 3 * hd)
+    hbm, hbm_src = measured_hbm_peak()
+    tf, tf_src = measured_bf16_peak(sustained=False)
+    if w.dtype == "f16":
+        tf_src += " (fp16 dense rate equals bf16's)"
+    t_mem, t_math = nbytes / (hbm * 1e9), flops / (tf * 1e12)
+    if t_mem >= t_math:
+        roof = {"bound": "hbm", "achieved": nbytes / (proj_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": hbm_src}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (proj_ms / 1e3) / 1e12, "peak": tf, "unit": "TFLOP/s",
+                "peak_source": tf_src}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    return {"kin": kin, "ms_per_layer": layer_ms, "edges_per_s": g.num_edges / (layer_ms / 1e3),
+            "projection": {"ms": proj_ms, "shape": [g.num_nodes, kin, 3 * hd], "tflops": flops / (proj_ms / 1e3) / 1e12,
+                           "gbs": nbytes / (proj_ms / 1e3) / 1e9, "roofline": roof,
+                           "bytes_model": "X read once, Wqkv once, Q|K|V written once (16-bit)"},
+            "data": "seeded synthetic features and weights (torch generator), not trained"}
 
 
 def main():
@@ -356,6 +433,11 @@ def main():
         roofline["tile_windows"] = st["tile_windows"]
         roofline["tile_window_nnz"] = st["tile_window_nnz"]
 
+    # ---- optional: a whole layer (projection on the tensor cores + forward) ----
+    layer = None
+    if args.layer:
+        layer = time_layer(args, g, w, plan, O, Eout, stream, dev)
+
     # ---- end to end through the C ABI on host buffers --------------------
     # Every step uploads its Q, K, V (and E) from pinned host memory and
     # downloads its O (and Eout) through g3s_forward_host.  Two plans (each
@@ -430,7 +512,7 @@ def main():
                        "parallelism": "replica per GPU" if world > 1 else "single GPU"},
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms,
+            "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
             "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
                      "tile_windows": st["tile_windows"],
                      "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},
