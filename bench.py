@@ -221,6 +221,8 @@ def parse_args():
                     help="density cutoff of the tile path in 1/1000 (default: the library's)")
     ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
                     help="element type of O (default fp32)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of the forward captured in a CUDA graph (no per-call launch overhead)")
     ap.add_argument("--layer", type=int, default=0, metavar="KIN",
                     help="also time one attention layer on 16-bit workloads: Q|K|V = X Wqkv^T for X of KIN "
                          "features (the tcgen05 projection), then the forward; adds a 'layer' object")
@@ -384,6 +386,19 @@ def main():
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
+    if args.graph:  # capture one forward, then time replays of it
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        fwd_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fwd_graph):
+            step()
+        step = fwd_graph.replay
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
 
     # ---- timed region: K forwards, inputs resident ----------------------
     if dist:
@@ -509,7 +524,8 @@ def main():
                        "num_edges": g.num_edges, "heads": w.heads, "head_dim": w.head_dim, "variant": w.variant,
                        "out_dtype": plan.out_dtype, "accumulation": "f32",
                        "l2": "no flush: inputs larger than L2 (%.2f GB touched per step)" % (compulsory / 1e9),
-                       "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+                       "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                       "launch": "CUDA graph replay" if args.graph else "one g3s_forward call per step"},
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,

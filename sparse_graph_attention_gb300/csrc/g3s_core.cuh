@@ -545,7 +545,10 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 // time from an atomic counter, so a warp that drew a short row is never idle
 // behind a long one, and the rows in flight stay a narrow band of ids (the
 // L2 keeps serving the sources near them).  Each item's result depends only
-// on its own data, so the dynamic order does not change any output.
+// on its own data, so the dynamic order does not change any output.  When all
+// items fit one resident wave of warps the launcher instead gives every warp
+// exactly one item by its id (no counter, no memset launch): small graphs are
+// bound by one row's latency chain, not by balance.
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT, int NV, int MODE, int LPH>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : 1)
@@ -553,24 +556,30 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
     const unsigned long long total = n_chunks + (unsigned long long)p.N;
+    auto run = [&](unsigned long long it) {
+        if (it < n_chunks) {
+            const int32_t* c = p.chunks + 3 * it;
+            process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
+        } else {
+            const int row = (int)(it - n_chunks);
+            const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
+            if (e1 - e0 > p.heavy_threshold) return;                                       // chunks + merge
+            if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) return;  // tile path
+            process_item<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1, -1);
+        }
+    };
+    if (p.static_items) {  // at most one item per warp: item = global warp id, no counter
+        const unsigned long long it = (unsigned long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+        if (it < total) run(it);
+        return;
+    }
     for (;;) {
         unsigned long long first = 0;
         if (L.lane == 0) first = atomicAdd(p.work_counter, (unsigned long long)kItemsPerGrab);
         first = __shfl_sync(kFull, first, 0);
         if (first >= total) break;
         const unsigned long long last = first + kItemsPerGrab < total ? first + kItemsPerGrab : total;
-        for (unsigned long long it = first; it < last; ++it) {
-            if (it < n_chunks) {
-                const int32_t* c = p.chunks + 3 * it;
-                process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
-            } else {
-                const int row = (int)(it - n_chunks);
-                const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
-                if (e1 - e0 > p.heavy_threshold) continue;  // done by chunks + merge
-                if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) continue;  // tile path
-                process_item<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1, -1);
-            }
-        }
+        for (unsigned long long it = first; it < last; ++it) run(it);
     }
 }
 
@@ -632,6 +641,15 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
         cached_dev = dev;
+    }
+    if (items <= (long long)cached_ctas * kWarpsPerCta) {
+        // Every item fits one resident wave of warps: one item per warp, no
+        // work counter (no memset launch, no atomic round trip).
+        CoreParams q = p;
+        q.static_items = 1;
+        const int ctas = (int)((items + kWarpsPerCta - 1) / kWarpsPerCta);
+        core_kernel<T, OutT, NV, MODE, LPH><<<ctas, kWarpsPerCta * 32, 0, st>>>(q);
+        return cudaGetLastError();
     }
     const long long need = (items + (long long)kWarpsPerCta * kItemsPerGrab - 1) / ((long long)kWarpsPerCta * kItemsPerGrab);
     const int ctas = (int)(need < cached_ctas ? need : cached_ctas);

@@ -118,6 +118,7 @@ struct CoreParams {
     int elementwise_clamp;
     int normalize;  // aggregation: divide by (sum of weights + eps)
     int32_t* status;  // forward status word: kErrTimeout is OR-ed in when a bounded wait gives up
+    int static_items;  // set by the launcher: one item per warp, by warp id (no work counter)
 };
 
 struct MergeParams {
