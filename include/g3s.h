@@ -87,9 +87,11 @@ typedef enum g3s_variant {
  *                  is the standard form with fp16/bf16 inputs and d = 64,
  *                  unless bsb = 0)
  *  tile_density_milli  a window takes the tile path when
- *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 500:
- *                  on the batched 20-60-node graphs, density about 0.25, the
- *                  CUDA-core kernel is faster)
+ *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 400:
+ *                  the tile kernel's time follows its tiles, the CUDA-core
+ *                  kernel's its edges; measured on batched 20-60-node graphs
+ *                  they cross near a window density of 0.4-0.5, and on
+ *                  complete graphs the tile path is about twice as fast)
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 32)
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
@@ -185,6 +187,10 @@ g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int hea
  *                         owned by the caller, must outlive the plan
  *   stream                all planner kernels run here; synchronised before return
  *   out                   receives the plan; free with g3s_plan_destroy
+ * Besides its host struct, a plan with tile-path windows holds one CUDA
+ * stream and two events: g3s_forward runs the tile kernel on that stream,
+ * forked from and joined back into the caller's stream (so both kernels
+ * overlap and the call stays capturable in a CUDA graph).
  * Returns BAD_GRAPH when validation finds row_ptr[0] != 0, a decreasing
  * row_ptr, row_ptr[N] != E or a source outside [0, N).  With validation off
  * a malformed CSR is undefined behaviour.
@@ -328,7 +334,7 @@ g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
  */
 g3s_status g3s_selftest_wait_timeout(const g3s_plan *plan, uint64_t limit_ns, g3s_stream_t stream);
 
-/* Release the plan's host struct (the caller still owns the workspace). NULL is a no-op. */
+/* Release the plan's host struct, stream and events (the caller still owns the workspace). NULL is a no-op. */
 void g3s_plan_destroy(g3s_plan *plan);
 
 /*

@@ -64,7 +64,7 @@ void default_options(g3s_plan_options* o) {
     o->chunk_edges = 256;
     o->bsb = -1;
     o->tile_path = -1;
-    o->tile_density_milli = 500;
+    o->tile_density_milli = 400;
     o->tile_max_tiles = 32;
     o->bsb_smem_edges = 2048;
     o->rtm_elementwise_clamp = 1;
@@ -187,6 +187,11 @@ struct g3s_plan {
     size_t ws_used;
     const int32_t* edge_id;  // optional CSR position -> physical edge slot
     long long edge_slots;    // rows of E / Eout / W (E without edge ids)
+    // With tile windows, the tile kernel runs on this side stream beside the
+    // CUDA-core kernel (forked from and joined back into the caller's stream
+    // with the two events); created with the plan, destroyed with it.
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 extern "C" {
@@ -294,6 +299,15 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
     p->ws_used = need;
     p->edge_id = nullptr;
     p->edge_slots = num_edges;
+    if (hc.n_tile_windows > 0) {
+        cudaError_t e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            g3s_plan_destroy(p);
+            return cuda_fail(e, "side stream / events of the tile path");
+        }
+    }
     *out = p;
     return G3S_OK;
 }
@@ -422,10 +436,16 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.tile_bits = p->arr.tile_bits;
         tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;
         tp.status = p->arr.fwd_status;
-        CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
+        // the tile kernel on the side stream, the CUDA-core kernel on the caller's, overlapping
+        CUDA_OR_FAIL(cudaEventRecord(p->ev_fork, stream), "cudaEventRecord(fork)");
+        CUDA_OR_FAIL(cudaStreamWaitEvent(p->side, p->ev_fork, 0), "cudaStreamWaitEvent(fork)");
+        CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, p->side), "tile kernel launch");
+        CUDA_OR_FAIL(cudaEventRecord(p->ev_join, p->side), "cudaEventRecord(join)");
     }
     CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, stream),
                  "fused kernel launch");
+    if (p->counts.n_tile_windows > 0)
+        CUDA_OR_FAIL(cudaStreamWaitEvent(stream, p->ev_join, 0), "cudaStreamWaitEvent(join)");
     if (p->counts.n_chunks > 0) {
         MergeParams mp{};
         mp.heavy_rows = p->arr.heavy_rows;
@@ -654,6 +674,12 @@ g3s_status g3s_layer_forward(const g3s_plan* p, const void* X, const void* Wqkv,
     return g3s_forward(p, Q, K, V, rtm ? Eproj : nullptr, O, rtm ? Eout : nullptr, stream_);
 }
 
-void g3s_plan_destroy(g3s_plan* p) { delete p; }
+void g3s_plan_destroy(g3s_plan* p) {
+    if (!p) return;
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->side) cudaStreamDestroy(p->side);
+    delete p;
+}
 
 }  // extern "C"

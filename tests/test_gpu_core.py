@@ -31,7 +31,7 @@ def test_small_workload(name):
     run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant)
 
 
-@pytest.mark.parametrize("name", ["tiny_poisson", "rtmscore_batch64", "batched_dense", "powerlaw"])
+@pytest.mark.parametrize("name", ["tiny_poisson", "rtmscore_batch64", "batched_dense", "powerlaw", "batched_complete"])
 def test_full_workload_all_rows(name):
     g, vals, w = graphgen.make_workload(name, "full")
     run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant)

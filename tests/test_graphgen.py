@@ -24,7 +24,7 @@ def test_small_workloads_are_valid_and_seeded(name):
     g2, v2, _ = graphgen.make_workload(name, "small")
     assert np.array_equal(g1.row_ptr, g2.row_ptr) and np.array_equal(g1.col_idx, g2.col_idx)
     assert all(np.array_equal(v1[k], v2[k]) for k in v1)
-    _check_csr(g1, self_loops_allowed=(name == "batched_dense"))
+    _check_csr(g1, self_loops_allowed=name in ("batched_dense", "batched_complete"))
     assert v1["Q"].shape == (g1.num_nodes, w.heads, w.head_dim)
     if w.variant == "rtmscore":
         assert v1["E"].shape == (g1.num_edges, w.heads, w.head_dim)
@@ -48,6 +48,21 @@ def test_batched_dense_full():
     assert np.sum(rows == c) == g.num_nodes  # one self loop per node
     # off-diagonal density close to 0.3 within graphs of U[20,60] nodes
     assert 12 < g.degrees().mean() < 16
+
+
+def test_batched_complete_is_complete():
+    """Every graph of the batch is complete with self loops: each row lists all
+    nodes of its own graph."""
+    g = graphgen.make_workload("batched_complete", "small")[0]
+    rows, c = _check_csr(g, self_loops_allowed=True)
+    deg = g.degrees()
+    start = 0
+    while start < g.num_nodes:  # a graph is a run of rows with the same degree = its size
+        n = int(deg[start])
+        assert np.all(deg[start:start + n] == n)
+        for r in range(start, start + n):
+            assert np.array_equal(c[g.row_ptr[r]:g.row_ptr[r + 1]], np.arange(start, start + n))
+        start += n
 
 
 def test_lognormal_local_small_structure():
