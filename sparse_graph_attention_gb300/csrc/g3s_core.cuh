@@ -584,42 +584,50 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
 }
 
 // ---------------------------------------------------------------------------
-// Merge of heavy-row partials: one warp per heavy row, chunks combined in
-// ascending order (m = max m_c, l = sum l_c 2^(m_c - m), O = sum acc_c 2^(m_c - m) / l;
+// Merge of heavy-row partials: one warp per heavy row and 32-column block,
+// chunks combined in ascending order (m = max m_c, l = sum l_c 2^(m_c - m), O = sum acc_c 2^(m_c - m) / l;
 // RTMScore: plain sums, epsilon added once).
 // ---------------------------------------------------------------------------
 template <typename OutT, bool PLAIN>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergeParams p) {
+    // one warp per (heavy row, block of 32 output columns); the chunk loops
+    // are unrolled so several chunks' loads are in flight at once
     const int lane = threadIdx.x & 31;
-    const long long k = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (k >= p.n_heavy) return;
+    const int HD = p.H * p.D;
+    const int col_blocks = (HD + 31) / 32;
+    const long long w = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (w >= (long long)p.n_heavy * col_blocks) return;
+    const long long k = w / col_blocks;
+    const int x = (int)(w - k * col_blocks) * 32 + lane;
+    if (x >= HD) return;
     const int row = p.heavy_rows[k];
     const int c0 = p.heavy_chunk_ptr[k], c1 = p.heavy_chunk_ptr[k + 1];
-    const int HD = p.H * p.D;
-    for (int x = lane; x < HD; x += 32) {
-        const int h = x / p.D;
-        float o;
-        if constexpr (PLAIN) {
-            float a = 0.f, s = 0.f;
-            for (int c = c0; c < c1; ++c) {
-                a += p.part_acc[(long long)c * HD + x];
-                s += p.part_ml[((long long)c * p.H + h) * 2 + 1];
-            }
-            o = p.normalize ? a / (s + p.eps) : a;
-        } else {
-            float mx = kNegBig;
-            for (int c = c0; c < c1; ++c) mx = fmaxf(mx, p.part_ml[((long long)c * p.H + h) * 2]);
-            float a = 0.f, s = 0.f;
-            for (int c = c0; c < c1; ++c) {
-                const float* ml = p.part_ml + ((long long)c * p.H + h) * 2;
-                const float f = ex2(ml[0] - mx);
-                s += ml[1] * f;
-                a += p.part_acc[(long long)c * HD + x] * f;
-            }
-            o = s > 0.f ? a / s : 0.f;
+    const int h = x / p.D;
+    const float* ml = p.part_ml + (long long)h * 2;     // chunk c: ml[c * 2H], ml[c * 2H + 1]
+    const float* acc = p.part_acc + x;                  // chunk c: acc[c * HD]
+    float o;
+    if constexpr (PLAIN) {
+        float a = 0.f, s = 0.f;
+#pragma unroll 8
+        for (int c = c0; c < c1; ++c) {
+            a += acc[(long long)c * HD];
+            s += ml[(long long)c * 2 * p.H + 1];
         }
-        Vec<OutT>::store1(p.O, (long long)row * HD + x, o);
+        o = p.normalize ? a / (s + p.eps) : a;
+    } else {
+        float mx = kNegBig;
+#pragma unroll 8
+        for (int c = c0; c < c1; ++c) mx = fmaxf(mx, ml[(long long)c * 2 * p.H]);
+        float a = 0.f, s = 0.f;
+#pragma unroll 8
+        for (int c = c0; c < c1; ++c) {
+            const float f = ex2(ml[(long long)c * 2 * p.H] - mx);
+            s += ml[(long long)c * 2 * p.H + 1] * f;
+            a += acc[(long long)c * HD] * f;
+        }
+        o = s > 0.f ? a / s : 0.f;
     }
+    Vec<OutT>::store1(p.O, (long long)row * HD + x, o);
 }
 
 
@@ -693,7 +701,8 @@ cudaError_t launch_core_mode(int mode, const CoreParams& p, cudaStream_t st) {
 template <typename OutT>
 cudaError_t launch_merge(bool plain, const MergeParams& p, cudaStream_t st) {
     if (p.n_heavy <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((p.n_heavy + kWarpsPerCta - 1) / kWarpsPerCta)), block(kWarpsPerCta * 32);
+    const long long warps = (long long)p.n_heavy * ((p.H * p.D + 31) / 32);
+    dim3 grid((unsigned)((warps + kWarpsPerCta - 1) / kWarpsPerCta)), block(kWarpsPerCta * 32);
     if (plain)
         merge_kernel<OutT, true><<<grid, block, 0, st>>>(p);
     else
