@@ -229,6 +229,8 @@ def parse_args():
     ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
                     help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="plans (each with its own staging) taking e2e steps in turn, one stream each")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -455,23 +457,26 @@ def main():
 
     # ---- end to end through the C ABI on host buffers --------------------
     # Every step uploads its Q, K, V (and E) from pinned host memory and
-    # downloads its O (and Eout) through g3s_forward_host.  Two plans (each
-    # with its own workspace and device staging) alternate on two streams, so
-    # one step's copies overlap the neighbouring step's kernels, as a caller
-    # streaming feature batches over one graph would run it.  The serialised
-    # single-stream time is reported beside it.
+    # downloads its O (and Eout) through g3s_forward_host.  Three plans (each
+    # with its own workspace and device staging) take the steps in turn, one
+    # stream each, so one step's upload overlaps the others' kernels and
+    # downloads, as a caller streaming feature batches over one graph would
+    # run it (with two, a stream's next upload waited behind its own
+    # download).  The serialised single-stream time is reported beside it.
     e2e = None
     if not args.no_e2e:
         pin = {k: t[k].pin_memory() for k in t}
-        plans = [plan, g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)]
-        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        ns = max(1, args.e2e_streams)
+        plans = [plan] + [g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)
+                          for _ in range(ns - 1)]
+        streams = [torch.cuda.Stream(dev) for _ in range(ns)]
         stagings = [torch.empty(pl.staging_size(), dtype=torch.uint8, device=dev) for pl in plans]
-        Ohs = [torch.empty(pin["Q"].shape, dtype=odt).pin_memory() for _ in range(2)]
+        Ohs = [torch.empty(pin["Q"].shape, dtype=odt).pin_memory() for _ in range(ns)]
         Eohs = [torch.empty(pin["E"].shape, dtype=odt).pin_memory() if w.variant == "rtmscore" else None
-                for _ in range(2)]
+                for _ in range(ns)]
 
         def host_step(i, k=None):
-            k = i % 2 if k is None else k
+            k = i % ns if k is None else k
             plans[k].forward_host(pin["Q"], pin["K"], pin["V"], Ohs[k], pin.get("E"), Eohs[k], staging=stagings[k],
                                   stream=streams[k])
 
@@ -507,7 +512,7 @@ def main():
         e2e = {"value": whole_job_rate(g.num_edges, n_e2e, world, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": e2e_ms / n_e2e, "serial_ms_per_step": serial_ms,
-               "path": "g3s_forward_host, pinned host buffers, two plans alternating on two streams"}
+               "path": "g3s_forward_host, pinned host buffers, %d plans in turn on %d streams" % (ns, ns)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
