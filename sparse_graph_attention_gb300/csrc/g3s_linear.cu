@@ -52,34 +52,8 @@ struct __align__(1024) LinSmem {
     int abort;
 };
 
-__device__ __forceinline__ void mbar_arrive_l(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+using namespace ptx;
 
-// 2-D TMA tile load of the box at element coordinates (x, y) into dst.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// 2-D TMA tile store of the box at (x, y) from shared memory src.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
-                 "r"(x), "r"(y), "r"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the shared-memory sources of all but the newest `n` committed stores have been read
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // the 128 epilogue threads
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // the same barrier, returning whether `ok` holds on all 128 threads (so that
@@ -94,46 +68,17 @@ __device__ __forceinline__ bool epi_all(bool ok) {
     return r != 0;
 }
 
-__device__ __forceinline__ void mma_l(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                      uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void commit_l(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ uint64_t sdesc_l(uint32_t saddr) {  // K-major, 128-byte swizzle, 8-row groups 1024 B apart
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           (1ull << 46) | (2ull << 61);
-}
-__host__ __device__ constexpr uint32_t idesc_l(bool bf16, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
+// K-major operand with the 128-byte swizzle: 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t sdesc_l(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
 template <int BN>
 __device__ __forceinline__ bool wait_l(LinSmem<BN>& sm, uint32_t bar, uint32_t parity) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
     for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*reinterpret_cast<volatile int*>(&sm.abort)) return false;
-        if (ptx::globaltimer() - t0 > kLimitL) {
+        if (globaltimer() - t0 > kLimitL) {
             *reinterpret_cast<volatile int*>(&sm.abort) = 1;
             return false;
         }
@@ -181,36 +126,30 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
         *reinterpret_cast<LinSmem<BN>*>((reinterpret_cast<uintptr_t>(lin_smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr bool kBf16 = !std::is_same<T, __half>::value;
-    constexpr uint32_t kId = idesc_l(kBf16, kBM, BN);
+    constexpr uint32_t kId = idesc_f16(kBf16, false, kBM, BN);
     constexpr uint32_t kStageBytes = (kBM + BN) * 128;
     const long long m_tiles = (p.M + kBM - 1) / kBM;
     const int n_tiles = (p.Nout + BN - 1) / BN;
     const long long tiles = m_tiles * n_tiles;
     const int k_steps = (p.Kin + kBK - 1) / kBK;
 
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         ptx::smem_u32(&sm.tmem_base)),
-                     "r"(2 * BN)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), 2 * BN);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStagesL; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&sm.full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.empty[s]), 1);
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&sm.acc_full[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sm.acc_empty[b]), 128);
+            mbar_init(smem_u32(&sm.acc_full[b]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[b]), 128);
         }
-        ptx::mbar_init(ptx::smem_u32(&sm.mma_done), 1);
+        mbar_init(smem_u32(&sm.mma_done), 1);
         sm.abort = 0;
-        ptx::fence_mbar_init();
+        fence_mbar_init();
     }
-    tc_before();
+    tc_fence_before();
     __syncthreads();
-    tc_after();
+    tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
@@ -222,20 +161,20 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
                 for (int ks = 0; ks < k_steps; ++ks, ++it) {
                     const int s = (int)(it % kStagesL);
                     const uint32_t u = it / kStagesL;
-                    if (u >= 1 && !wait_l(sm, ptx::smem_u32(&sm.empty[s]), (u - 1) & 1)) {
+                    if (u >= 1 && !wait_l(sm, smem_u32(&sm.empty[s]), (u - 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = ptx::smem_u32(&sm.full[s]);
-                    ptx::mbar_arrive_expect_tx(bar, kStageBytes);
-                    tma_load_2d(ptx::smem_u32(sm.a[s]), &ta, ks * kBK, m0, bar);
-                    tma_load_2d(ptx::smem_u32(sm.b[s]), &tb, ks * kBK, n0, bar);
+                    const uint32_t bar = smem_u32(&sm.full[s]);
+                    mbar_arrive_expect_tx(bar, kStageBytes);
+                    tma_load_2d(smem_u32(sm.a[s]), &ta, ks * kBK, m0, bar);
+                    tma_load_2d(smem_u32(sm.b[s]), &tb, ks * kBK, n0, bar);
                 }
             }
             // every armed copy lands before the CTA may exit
             for (int s = 0; s < kStagesL; ++s) {
                 const uint32_t uses = it / kStagesL + ((uint32_t)s < it % kStagesL ? 1u : 0u);
-                if (uses > 0) ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full[s]), (uses - 1) & 1, kLimitL);
+                if (uses > 0) mbar_wait_bounded(smem_u32(&sm.full[s]), (uses - 1) & 1, kLimitL);
             }
         }
         __syncwarp();
@@ -245,29 +184,29 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
             bool ok = true;
             for (long long t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tl) {
                 const uint32_t buf = tl & 1, use = tl >> 1;
-                if (use >= 1 && !wait_l(sm, ptx::smem_u32(&sm.acc_empty[buf]), (use - 1) & 1)) {
+                if (use >= 1 && !wait_l(sm, smem_u32(&sm.acc_empty[buf]), (use - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_after();
+                tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
                 for (int ks = 0; ks < k_steps; ++ks, ++it) {
                     const int s = (int)(it % kStagesL);
-                    if (!wait_l(sm, ptx::smem_u32(&sm.full[s]), (it / kStagesL) & 1)) {
+                    if (!wait_l(sm, smem_u32(&sm.full[s]), (it / kStagesL) & 1)) {
                         ok = false;
                         break;
                     }
-                    tc_after();
-                    const uint32_t a = ptx::smem_u32(sm.a[s]), b = ptx::smem_u32(sm.b[s]);
+                    tc_fence_after();
+                    const uint32_t a = smem_u32(sm.a[s]), b = smem_u32(sm.b[s]);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_l(d, sdesc_l(a + kk * 32), sdesc_l(b + kk * 32), kId, (ks > 0 || kk > 0) ? 1u : 0u);
-                    commit_l(ptx::smem_u32(&sm.empty[s]));  // the stage is free once these MMAs are done
+                        mma_f16(d, sdesc_l(a + kk * 32), sdesc_l(b + kk * 32), kId, (ks > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&sm.empty[s]));  // the stage is free once these MMAs are done
                 }
-                if (ok) commit_l(ptx::smem_u32(&sm.acc_full[buf]));
+                if (ok) mma_commit(smem_u32(&sm.acc_full[buf]));
             }
-            commit_l(ptx::smem_u32(&sm.mma_done));
-            ptx::mbar_wait_bounded(ptx::smem_u32(&sm.mma_done), 0, kLimitL);
+            mma_commit(smem_u32(&sm.mma_done));
+            mbar_wait_bounded(smem_u32(&sm.mma_done), 0, kLimitL);
         }
         __syncwarp();
     } else {  // epilogue: warps 2-5, TMEM lane quarter warp % 4
@@ -283,14 +222,14 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
         uint32_t tl = 0, blocks = 0;
         for (long long t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
             const uint32_t buf = tl & 1, use = tl >> 1;
-            if (!epi_all(wait_l(sm, ptx::smem_u32(&sm.acc_full[buf]), use & 1))) break;
-            tc_after();
+            if (!epi_all(wait_l(sm, smem_u32(&sm.acc_full[buf]), use & 1))) break;
+            tc_fence_after();
             const int m0 = (int)(t / n_tiles) * kBM;
             const int n0 = (int)(t % n_tiles) * BN;
             const int seg = n0 / p.seg_cols, c0 = n0 - seg * p.seg_cols;
 #pragma unroll 1
             for (int j = 0; j < BN / kBC; ++j, ++blocks) {
-                const uint32_t sb = ptx::smem_u32(sm.o[blocks & 1]);
+                const uint32_t sb = smem_u32(sm.o[blocks & 1]);
                 if (leader && blocks >= 2) bulk_wait_read<1>();
                 epi_sync();  // the staging buffer is free
                 uint32_t r[32 * (kBC / 32)];
@@ -298,11 +237,11 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
                 for (int q = 0; q < kBC / 32; ++q)
                     tmem_ld32(tmem + lane_off + buf * BN + j * kBC + q * 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * q));
                 if (j == BN / kBC - 1) {  // the accumulator is read: the MMAs may reuse it
-                    tc_before();
-                    mbar_arrive_l(ptx::smem_u32(&sm.acc_empty[buf]));
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&sm.acc_empty[buf]));
                 }
                 stage_row<OutT>(sb, row, r);
-                ptx::fence_proxy_async_smem();
+                fence_proxy_async_smem();
                 epi_sync();  // the block is staged
                 if (leader) {
                     tma_store_2d(maps[seg], c0 + j * kBC, m0, sb);
@@ -313,12 +252,12 @@ __global__ void __launch_bounds__(kWarpsL * 32, 1)
         if (leader) bulk_wait_all();  // the stores have completed before the CTA exits
     }
 
-    tc_before();
+    tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && sm.abort && p.status != nullptr) atomicOr(p.status, (int32_t)kErrTimeout);
     if (warp == 1) {
-        tc_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * BN);
     }
 }
 

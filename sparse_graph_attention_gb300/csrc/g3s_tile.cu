@@ -36,6 +36,7 @@
 #include <type_traits>
 
 #include "g3s_internal.h"
+#include "g3s_ptx.cuh"
 
 namespace g3s {
 namespace {
@@ -66,128 +67,12 @@ struct TileSmem {
     int nw, tt;
 };
 
-// ---- PTX wrappers ----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-// make this thread's generic-proxy shared-memory writes visible to the tensor core (async proxy)
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_init(unsigned long long* m, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(m)), "r"(count) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* m, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(m)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
-}
-// bounded wait: false when the phase did not complete within limit_ns
-__device__ bool mbar_wait_bounded(unsigned long long* m, uint32_t parity,
-                                  unsigned long long limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(m, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait(m, parity)) return true;
-        if (globaltimer() - t0 > limit_ns) return false;
-    }
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16 or bf16 in, fp32 accumulate)
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(unsigned long long* mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(mbar))
-                 : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];\n"
-        "tcgen05.wait::ld.sync.aligned;\n"  // same statement: the outputs exist only after the wait
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// store 16 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16};\n"
-        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
-        : "memory");
-}
+using namespace ptx;
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle.  Start address and the
-// two byte offsets are stored in 16-byte units; bits 46-47 hold the
-// descriptor version (1), bits 61-63 the swizzle mode (2 = 128 B).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1),
-// A/B type (bits 7-9 and 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0),
-// B major (bit 16: 0 K, 1 MN), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 template <typename T>
@@ -266,8 +151,11 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kD);
 
     // ---- set-up: TMEM, mbarrier, the group's windows and tiles ---------------
-    if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
-    if (tid == 0) mbar_init(&sm.mbar, 1);
+    if (warp == 0) tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    if (tid == 0) {
+        mbar_init(smem_u32(&sm.mbar), 1);
+        fence_mbar_init();
+    }
     // windows of the group and their tile ranges, read in parallel by the first warp
     if (warp == 0) {
         const int lane = tid;
@@ -378,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     for (int ch = 0; ch < nchunks; ++ch) {
         const int ks = ch & 1, ms = ch % 3;
         cp_async_wait_all();  // this chunk's K and V rows, the next chunk's metadata
-        fence_async_smem();   // ... and the previous chunk's P: visible to the tensor core
+        fence_proxy_async_smem();   // ... and the previous chunk's P: visible to the tensor core
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -396,14 +284,14 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
             for (int kk = 0; kk < kD / 16; ++kk)
                 mma_f16(tmem_S, sdesc_sw128(smem_u32(sm.q) + kk * 32, 16, 1024),
                         sdesc_sw128(smem_u32(sm.k[ks]) + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-            mma_commit(&sm.mbar);
+            mma_commit(smem_u32(&sm.mbar));
         }
         // the next chunk's K rows (that stage was last read by S_{ch-1}, complete) and
         // the metadata two chunks ahead
         if (ch + 1 < nchunks) issue_gather(K, sm.k[ks ^ 1], ch + 1, (ch + 1) % 3);
         if (ch + 2 < nchunks) issue_meta(ch + 2, (ch + 2) % 3);
 
-        const bool ok = mbar_wait_bounded(&sm.mbar, phase);
+        const bool ok = mbar_wait_bounded(smem_u32(&sm.mbar), phase, kWaitLimitNs);
         phase ^= 1u;
         if (__syncthreads_or(!ok)) {
             failed = true;
@@ -481,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     // the last chunk's P V
     if (!failed && nchunks > 0) {
         cp_async_wait_all();
-        fence_async_smem();
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -491,9 +379,9 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
                 mma_f16(tmem_O, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
                         sdesc_sw128(smem_u32(sm.v[(nchunks - 1) & 1]) + kk * 16 * 128, kNC * 128, 1024), kIdescO,
                         (nchunks > 1 || kk > 0) ? 1u : 0u);
-            mma_commit(&sm.mbar);
+            mma_commit(smem_u32(&sm.mbar));
         }
-        const bool ok = mbar_wait_bounded(&sm.mbar, phase);
+        const bool ok = mbar_wait_bounded(smem_u32(&sm.mbar), phase, kWaitLimitNs);
         phase ^= 1u;
         if (__syncthreads_or(!ok)) failed = true;
         tc_fence_after();
@@ -528,9 +416,12 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
 // the tile kernel does.
 __global__ void wait_selftest_kernel(unsigned long long limit_ns, int32_t* status) {
     __shared__ unsigned long long mbar;
-    if (threadIdx.x == 0) mbar_init(&mbar, 1);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&mbar), 1);
+        fence_mbar_init();
+    }
     __syncthreads();
-    const bool ok = mbar_wait_bounded(&mbar, 0, limit_ns);
+    const bool ok = mbar_wait_bounded(smem_u32(&mbar), 0, limit_ns);
     if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(status, kErrTimeout);
 }
 
