@@ -228,6 +228,8 @@ def parse_args():
                          "features (the tcgen05 projection), then the forward; adds a 'layer' object")
     ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
                     help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
+    ap.add_argument("--pack-rows", type=int, default=None, choices=[0, 1],
+                    help="short-row packs, one row per lane group (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-streams", type=int, default=3,
                     help="plans (each with its own staging) taking e2e steps in turn, one stream each")
@@ -369,6 +371,8 @@ def main():
         plan_kw["tile_density_milli"] = args.tile_density_milli
     if args.tma_gather is not None:
         plan_kw["tma_gather"] = args.tma_gather
+    if args.pack_rows is not None:
+        plan_kw["pack_rows"] = args.pack_rows
     plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)
     torch.cuda.synchronize(dev)
     plan_ms = 1000.0 * (time.perf_counter() - t0)
@@ -535,6 +539,7 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
             "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
+                     "pack_rows": plan.options.pack_rows,
                      "tile_windows": st["tile_windows"],
                      "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},
         }

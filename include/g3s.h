@@ -111,6 +111,17 @@ typedef enum g3s_variant {
  *                  loads.  Both compute the same arithmetic in the same order.
  *                  The ring costs resident warps (shared memory, registers),
  *                  and on the measured workloads the plain loads are faster.
+ *  pack_rows       short-row packs, where a node row is at most 256 bytes
+ *                  (G = 32 * 16 / row bytes >= 2 lane groups per warp): a warp
+ *                  takes G consecutive rows together, one per lane group,
+ *                  when each has at most min(4 G, 2 * 32 / G, heavy_threshold)
+ *                  entries (stats.pack_limit), else one row at a time.  The
+ *                  kernel with packs needs more registers, so it is a second
+ *                  flavour: -1 (default) uses it when at least a quarter of
+ *                  the rows are that short (stats.short_rows), 1 whenever the
+ *                  row width packs, 0 never.  Same arithmetic per row; a
+ *                  packed row's terms are summed in CSR order by one lane
+ *                  group (no lane-group merge).
  */
 typedef struct g3s_plan_options {
     int32_t bucket_bounds[G3S_NUM_BUCKETS - 2];
@@ -126,6 +137,7 @@ typedef struct g3s_plan_options {
     int32_t validate_graph;
     int32_t out_dtype;
     int32_t tma_gather;
+    int32_t pack_rows;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {
@@ -137,6 +149,9 @@ typedef struct g3s_plan_stats {
     int32_t has_bsb, tile_path;
     int64_t windows, tiles, tile_windows, dup_windows, large_windows;
     int64_t tile_window_nnz; /* CSR entries handled by the tile path */
+    int32_t pack_rows;       /* 1 when forwards use short-row packs */
+    int32_t pack_limit;      /* most entries of a packed row (0: this row width does not pack) */
+    int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
 } g3s_plan_stats;
 

@@ -63,6 +63,7 @@ class PlanOptions(ctypes.Structure):
         ("validate_graph", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32),
         ("tma_gather", ctypes.c_int32),
+        ("pack_rows", ctypes.c_int32),
     ]
 
 
@@ -78,6 +79,7 @@ class PlanStats(ctypes.Structure):
         ("windows", ctypes.c_int64), ("tiles", ctypes.c_int64), ("tile_windows", ctypes.c_int64),
         ("dup_windows", ctypes.c_int64), ("large_windows", ctypes.c_int64),
         ("tile_window_nnz", ctypes.c_int64),
+        ("pack_rows", ctypes.c_int32), ("pack_limit", ctypes.c_int32), ("short_rows", ctypes.c_int64),
         ("workspace_used", ctypes.c_size_t),
     ]
 

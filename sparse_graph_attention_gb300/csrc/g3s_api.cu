@@ -72,6 +72,7 @@ void default_options(g3s_plan_options* o) {
     o->validate_graph = 1;
     o->out_dtype = G3S_F32;
     o->tma_gather = 0;
+    o->pack_rows = -1;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -106,6 +107,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (o.out_dtype != G3S_F32 && o.out_dtype != dtype)
         return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
     if (o.tma_gather != 0 && o.tma_gather != 1) return fail(G3S_ERR_INVALID_ARG, "tma_gather must be 0 or 1");
+    if (o.pack_rows < -1 || o.pack_rows > 1) return fail(G3S_ERR_INVALID_ARG, "pack_rows takes -1, 0 or 1");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -115,6 +117,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->H = heads;
     s->D = head_dim;
     s->heavy_threshold = o.heavy_threshold;
+    s->pack_limit = pack_limit_for((int)row_vecs, o.heavy_threshold);
     s->chunk_edges = o.chunk_edges;
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
@@ -337,6 +340,9 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->dup_windows = p->counts.n_dup_windows;
     st->large_windows = p->counts.n_large_windows;
     st->tile_window_nnz = p->counts.tile_window_nnz;
+    st->pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
+    st->pack_limit = p->shape.pack_limit;
+    st->short_rows = p->counts.n_short;
     st->workspace_used = p->ws_used;
     return G3S_OK;
 }
@@ -421,6 +427,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.eps = p->opts.rtm_epsilon;
     cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
     cp.status = p->arr.fwd_status;
+    cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
     if (p->counts.n_tile_windows > 0) {
         TileParams tp{};
         tp.Q = Q;
@@ -506,6 +513,7 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     cp.elementwise_clamp = 0;
     cp.normalize = normalize ? 1 : 0;
     cp.status = p->arr.fwd_status;
+    cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
     CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, false, cp, stream), "aggregation kernel launch");
     if (p->counts.n_chunks > 0) {
         MergeParams mp{};

@@ -103,6 +103,14 @@ cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const Core
                               : core_tma_launch_bf16(out_f32, p, c.tk, c.tv, st);
         }
     }
+    if (p.pack_rows && mode != 1 && p.row_vecs <= 16) {  // the short-row pack flavour
+        switch (dtype) {
+            case 0: return core_launch_pack_f32(true, mode, p, st);
+            case 1: return core_launch_pack_f16(out_f32, mode, p, st);
+            case 2: return core_launch_pack_bf16(out_f32, mode, p, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (dtype) {
         case 0: return core_launch_f32(true, mode, p, st);
         case 1: return core_launch_f16(out_f32, mode, p, st);

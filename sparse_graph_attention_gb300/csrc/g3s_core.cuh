@@ -345,6 +345,42 @@ __device__ __forceinline__ void edge_math(const CoreParams& p, const Lanes& L, I
     }
 }
 
+// Gather the rows of U source nodes (K, V; E or the given weights through
+// the slots' CSR positions) for this lane and run the step's arithmetic.
+template <int U, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
+__device__ __forceinline__ void fetch_math(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st,
+                                           const int (&src)[U], const bool (&ok)[U], const int (&epos)[U]) {
+    constexpr bool RTM = MODE == kModeRtm;
+    constexpr bool AGG = MODE == kModeAgg;
+    const int rv = L.rv, lph = LPH > 0 ? LPH : L.lph;
+    const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
+    const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
+    // physical slot of each edge's features (RTMScore) or weights (aggregation)
+    int eid[(RTM || AGG) ? U : 1];
+    if constexpr (RTM || AGG) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) eid[u] = p.edge_id != nullptr ? __ldg(p.edge_id + epos[u]) : epos[u];
+    }
+    uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
+    uint4 er[RTM ? U : 1][RTM ? NV : 1];
+    float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const long long o = (long long)src[u] * rv;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
+            vr[u][j] = ldg16(V4 + o + 32 * j);
+            if constexpr (AGG) wg[u][j] = Vec<T>::load1(p.W, (long long)eid[u] * p.H + (L.sub + 32 * j) / lph);
+            if constexpr (RTM) {
+                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)eid[u] * rv + 32 * j);
+            }
+        }
+    }
+
+    edge_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, kr, vr, er, wg, ok, eid);
+}
+
 // One step of S = G * U edges starting at CSR position `base`.  TAIL: the
 // step runs past the row's end; slots beyond it re-read the row's last edge
 // (a valid, cached address) and get weight 0, so no load is branched.
@@ -352,9 +388,7 @@ template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP, int LP
 __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
                                           const int e1) {
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
-    constexpr bool RTM = MODE == kModeRtm;
-    constexpr bool AGG = MODE == kModeAgg;
-    const int rv = L.rv, g = L.g, lph = LPH > 0 ? LPH : L.lph;
+    const int g = L.g;
     const int S = L.G * U;
     if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
         st.cbase += 64;
@@ -380,35 +414,10 @@ __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, I
         }
     }
 
-    const uint4* K4 = static_cast<const uint4*>(p.K) + L.sub;
-    const uint4* V4 = static_cast<const uint4*>(p.V) + L.sub;
-    // physical slot of each edge's features (RTMScore) or weights (aggregation)
-    int eid[(RTM || AGG) ? U : 1];
-    if constexpr (RTM || AGG) {
+    int epos[U];  // CSR position of each slot's edge (a valid one for masked slots)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = ok[u] ? base + g * U + u : e1 - 1;
-            eid[u] = p.edge_id != nullptr ? __ldg(p.edge_id + e) : e;
-        }
-    }
-    uint4 kr[AGG ? 1 : U][AGG ? 1 : NV], vr[U][NV];
-    uint4 er[RTM ? U : 1][RTM ? NV : 1];
-    float wg[AGG ? U : 1][AGG ? NV : 1];  // given weights (aggregation)
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const long long o = (long long)src[u] * rv;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if constexpr (!AGG) kr[u][j] = ldg16(K4 + o + 32 * j);
-            vr[u][j] = ldg16(V4 + o + 32 * j);
-            if constexpr (AGG) wg[u][j] = Vec<T>::load1(p.W, (long long)eid[u] * p.H + (L.sub + 32 * j) / lph);
-            if constexpr (RTM) {
-                er[u][j] = ldg16(static_cast<const uint4*>(p.E) + L.sub + (long long)eid[u] * rv + 32 * j);
-            }
-        }
-    }
-
-    edge_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, kr, vr, er, wg, ok, eid);
+    for (int u = 0; u < U; ++u) epos[u] = ok[u] ? base + g * U + u : e1 - 1;
+    fetch_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, src, ok, epos);
 }
 
 // Start of a work item: the query, an empty softmax state, and the first 64
@@ -442,15 +451,16 @@ __device__ __forceinline__ void init_item(const CoreParams& p, const Lanes& L, I
 
 // End of a work item: merge the lane groups, then write the partial result of
 // a heavy-row chunk (chunk >= 0) or the normalised output row.
-template <typename T, typename OutT, int NV, int MODE, int VP, int LPH>
+template <typename T, typename OutT, int NV, int MODE, int VP, int LPH, bool MERGE = true>
 __device__ __forceinline__ void finish_item(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int row,
                                             const long long chunk) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
     constexpr bool PLAIN = MODE != kModeStd;  // weights need no running max
     const int rv = L.rv, g = L.g, sub = L.sub, lph = LPH > 0 ? LPH : L.lph;
-    // merge the lane groups (fixed butterfly order)
-    for (int off = L.gsize; off < 32; off <<= 1) {
+    // merge the lane groups (fixed butterfly order); a packed item's groups
+    // each hold their own row and skip this
+    for (int off = L.gsize; MERGE && off < 32; off <<= 1) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             if constexpr (PLAIN) {
@@ -477,7 +487,7 @@ __device__ __forceinline__ void finish_item(const CoreParams& p, const Lanes& L,
             }
         }
     }
-    if (g != 0) return;
+    if (MERGE && g != 0) return;
 
     if (chunk >= 0) {
         const long long HD = (long long)rv * VE;
@@ -537,6 +547,43 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 }
 
 // ---------------------------------------------------------------------------
+// A pack of G consecutive short rows, one per lane group (G = 32 / row_vecs
+// >= 2): every group walks its own row U edges per step, so a warp covers G
+// rows at once and no lane-group merge is needed.  Used when every row of the
+// pack has at most pack_max_deg <= 2 * group-size entries, held two per lane
+// of the group.  deg: this group's row length; maxdeg: the largest in the pack.
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT, int NV, int MODE, int LPH>
+__device__ __forceinline__ void process_pack(const CoreParams& p, const Lanes& L, const int row, const int e0,
+                                             const int deg, const int maxdeg) {
+    constexpr int VP = Vec<T>::N / 2;
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    const int gs = L.gsize;
+    const bool live = row < p.N;
+    ItemState<NV, VP> st;
+    // the query of this group's row (row 0 stands in past the end) and an empty state
+    init_item<T, NV, MODE, VP>(p, L, st, live ? row : 0, 0, 0);
+    const int w0 = L.sub < deg ? __ldg(p.col_idx + e0 + L.sub) : 0;
+    const int w1 = gs + L.sub < deg ? __ldg(p.col_idx + e0 + gs + L.sub) : 0;
+    const int last = deg > 0 ? deg - 1 : 0;
+    for (int base = 0; base < maxdeg; base += U) {
+        int src[U], epos[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            ok[u] = base + u < deg;
+            const int slot = ok[u] ? base + u : last;  // the same on every lane of the group
+            // the group's lane holding `slot` offers the word that has it
+            const int w = slot >= gs ? w1 : w0;
+            src[u] = __shfl_sync(kFull, w, L.g * gs + (slot & (gs - 1)));
+            epos[u] = deg > 0 ? e0 + slot : 0;  // an empty row's slots: any valid position
+        }
+        fetch_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, src, ok, epos);
+    }
+    if (live) finish_item<T, OutT, NV, MODE, VP, LPH, false>(p, L, st, row, -1);
+}
+
+// ---------------------------------------------------------------------------
 // The fused kernel.  T: input element type; OutT: type of O and Eout (fp32
 // or T); NV: 16-byte vectors per lane per edge; RTM: edge-modulated variant.
 //
@@ -550,22 +597,46 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 // exactly one item by its id (no counter, no memset launch): small graphs are
 // bound by one row's latency chain, not by balance.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, int MODE, int LPH>
+template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : 1)
     core_kernel(const CoreParams p) {
+    static_assert(!PACK || (NV == 1 && MODE != kModeRtm), "packs: one vector per lane, no edge outputs");
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
-    const unsigned long long total = n_chunks + (unsigned long long)p.N;
+    const int pack = PACK ? p.pack : 1;  // rows per item: 1, or G (the pack flavour; 16 % G == 0)
+    const unsigned long long total = n_chunks + (unsigned long long)((p.N + pack - 1) / pack);
     auto run = [&](unsigned long long it) {
         if (it < n_chunks) {
             const int32_t* c = p.chunks + 3 * it;
             process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
+            return;
+        }
+        const int r0 = (int)(it - n_chunks) * pack;
+        if (p.win_flags != nullptr && (p.win_flags[r0 >> 4] & kFlagTile)) return;  // tile path (whole window)
+        if constexpr (!PACK) {
+            const int e0 = p.row_ptr[r0], e1 = p.row_ptr[r0 + 1];
+            if (e1 - e0 > p.heavy_threshold) return;  // chunks + merge
+            process_item<T, OutT, NV, MODE, LPH>(p, L, r0, e0, e1, -1);
         } else {
-            const int row = (int)(it - n_chunks);
-            const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
-            if (e1 - e0 > p.heavy_threshold) return;                                       // chunks + merge
-            if (p.win_flags != nullptr && (p.win_flags[row >> 4] & kFlagTile)) return;  // tile path
-            process_item<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1, -1);
+            // this group's row, then the pack's longest
+            const int row = r0 + L.g;
+            int e0 = 0, e1 = 0;
+            if (row < p.N) {
+                e0 = p.row_ptr[row];
+                e1 = p.row_ptr[row + 1];
+            }
+            const int maxdeg = __reduce_max_sync(kFull, e1 - e0);
+            if (maxdeg <= p.pack_max_deg) {
+                process_pack<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1 - e0, maxdeg);
+                return;
+            }
+            // a long row in the pack: each row on the whole warp, in order
+            const int n_sub = pack < p.N - r0 ? pack : (int)(p.N - r0);
+            for (int j = 0; j < n_sub; ++j) {
+                const int a = __shfl_sync(kFull, e0, j * L.gsize), b = __shfl_sync(kFull, e1, j * L.gsize);
+                if (b - a > p.heavy_threshold) continue;  // chunks + merge
+                process_item<T, OutT, NV, MODE, LPH>(p, L, r0 + j, a, b, -1);
+            }
         }
     };
     if (p.static_items) {  // at most one item per warp: item = global warp id, no counter
@@ -631,9 +702,22 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
-template <typename T, typename OutT, int NV, int MODE, int LPH>
-cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
-    const long long items = p.n_chunks + p.N;
+template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK>
+cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
+    CoreParams p = p_in;
+    // Short-row packs: one row per lane group, where a row is narrower than
+    // 16 vectors (G >= 2 groups) and its entries fit two per group lane.
+    const int gsize = p.row_vecs < 32 ? p.row_vecs : 32, G = 32 / gsize;
+    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    p.pack = 1;
+    p.pack_max_deg = 0;
+    if (PACK && G >= 2 && G <= 16) {
+        int t = G * U < 2 * gsize ? G * U : 2 * gsize;
+        if (t > p.heavy_threshold) t = p.heavy_threshold;
+        p.pack = G;
+        p.pack_max_deg = t;
+    }
+    const long long items = p.n_chunks + (p.N + p.pack - 1) / p.pack;
     if (items <= 0) return cudaSuccess;
     // one resident wave of CTAs (cached per instantiation and device)
     static int cached_dev = -1, cached_ctas = 0;
@@ -644,7 +728,7 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE, LPH>, kWarpsPerCta * 32,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE, LPH, PACK>, kWarpsPerCta * 32,
                                                           0);
         if (e != cudaSuccess) return e;
         cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
@@ -656,14 +740,14 @@ cudaError_t launch_core_nv(const CoreParams& p, cudaStream_t st) {
         CoreParams q = p;
         q.static_items = 1;
         const int ctas = (int)((items + kWarpsPerCta - 1) / kWarpsPerCta);
-        core_kernel<T, OutT, NV, MODE, LPH><<<ctas, kWarpsPerCta * 32, 0, st>>>(q);
+        core_kernel<T, OutT, NV, MODE, LPH, PACK><<<ctas, kWarpsPerCta * 32, 0, st>>>(q);
         return cudaGetLastError();
     }
     const long long need = (items + (long long)kWarpsPerCta * kItemsPerGrab - 1) / ((long long)kWarpsPerCta * kItemsPerGrab);
     const int ctas = (int)(need < cached_ctas ? need : cached_ctas);
     e = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned long long), st);
     if (e != cudaSuccess) return e;
-    core_kernel<T, OutT, NV, MODE, LPH><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
+    core_kernel<T, OutT, NV, MODE, LPH, PACK><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -672,18 +756,18 @@ cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
     const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
     if (nv == 1) {  // one vector per lane: the head-lane reduction is unrolled
         switch (p.lph) {
-            case 2: return launch_core_nv<T, OutT, 1, MODE, 2>(p, st);
-            case 4: return launch_core_nv<T, OutT, 1, MODE, 4>(p, st);
-            case 8: return launch_core_nv<T, OutT, 1, MODE, 8>(p, st);
-            case 16: return launch_core_nv<T, OutT, 1, MODE, 16>(p, st);
-            case 32: return launch_core_nv<T, OutT, 1, MODE, 32>(p, st);
-            default: return launch_core_nv<T, OutT, 1, MODE, 0>(p, st);
+            case 2: return launch_core_nv<T, OutT, 1, MODE, 2, false>(p, st);
+            case 4: return launch_core_nv<T, OutT, 1, MODE, 4, false>(p, st);
+            case 8: return launch_core_nv<T, OutT, 1, MODE, 8, false>(p, st);
+            case 16: return launch_core_nv<T, OutT, 1, MODE, 16, false>(p, st);
+            case 32: return launch_core_nv<T, OutT, 1, MODE, 32, false>(p, st);
+            default: return launch_core_nv<T, OutT, 1, MODE, 0, false>(p, st);
         }
     }
     switch (nv) {
-        case 2: return launch_core_nv<T, OutT, 2, MODE, 0>(p, st);
-        case 4: return launch_core_nv<T, OutT, 4, MODE, 0>(p, st);
-        case 8: return launch_core_nv<T, OutT, 8, MODE, 0>(p, st);
+        case 2: return launch_core_nv<T, OutT, 2, MODE, 0, false>(p, st);
+        case 4: return launch_core_nv<T, OutT, 4, MODE, 0, false>(p, st);
+        case 8: return launch_core_nv<T, OutT, 8, MODE, 0, false>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -694,6 +778,29 @@ cudaError_t launch_core_mode(int mode, const CoreParams& p, cudaStream_t st) {
         case kModeStd: return launch_core<T, OutT, kModeStd>(p, st);
         case kModeRtm: return launch_core<T, OutT, kModeRtm>(p, st);
         case kModeAgg: return launch_core<T, OutT, kModeAgg>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// The pack flavour: node rows of at most 16 vectors (two or more lane groups),
+// standard and aggregation modes.
+template <typename T, typename OutT, int MODE>
+cudaError_t launch_core_packed(const CoreParams& p, cudaStream_t st) {
+    if (p.row_vecs > 16) return cudaErrorInvalidValue;
+    switch (p.lph) {
+        case 2: return launch_core_nv<T, OutT, 1, MODE, 2, true>(p, st);
+        case 4: return launch_core_nv<T, OutT, 1, MODE, 4, true>(p, st);
+        case 8: return launch_core_nv<T, OutT, 1, MODE, 8, true>(p, st);
+        case 16: return launch_core_nv<T, OutT, 1, MODE, 16, true>(p, st);
+        default: return launch_core_nv<T, OutT, 1, MODE, 0, true>(p, st);
+    }
+}
+
+template <typename T, typename OutT>
+cudaError_t launch_core_packed_mode(int mode, const CoreParams& p, cudaStream_t st) {
+    switch (mode) {
+        case kModeStd: return launch_core_packed<T, OutT, kModeStd>(p, st);
+        case kModeAgg: return launch_core_packed<T, OutT, kModeAgg>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -37,7 +37,7 @@ struct PlanCounts {
     int32_t n_tile_windows;
     int32_t n_dup_windows;
     int32_t n_large_windows;
-    int32_t pad0;
+    int32_t n_short;  // rows with at most PlanShape::pack_limit entries
     long long tile_window_nnz;
 };
 
@@ -81,7 +81,27 @@ struct PlanShape {
     bool build_bsb, tile_enabled;
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
     int64_t scan_blocks;
+    int pack_limit;  // most entries of a row a short-row pack takes (0: the row width does not pack)
 };
+
+// Most CSR entries of a row that a short-row pack takes, for node rows of
+// row_vecs 16-byte vectors: packs exist where a row is at most 16 vectors
+// (G = 32 / row_vecs >= 2 lane groups); a group walks its row 4 entries a
+// step and holds its indices two per lane; never above the heavy threshold.
+inline int pack_limit_for(int row_vecs, int heavy_threshold) {
+    if (row_vecs < 1 || row_vecs > 16) return 0;
+    const int G = 32 / row_vecs;
+    int t = 4 * G < 2 * row_vecs ? 4 * G : 2 * row_vecs;
+    return t < heavy_threshold ? t : heavy_threshold;
+}
+
+// Whether forwards run the short-row pack flavour: option 1 forces it where
+// the row width packs, -1 (auto) takes it when at least a quarter of the rows
+// are short, 0 never.
+inline bool use_packs(int option, const PlanShape& s, const PlanCounts& c) {
+    if (s.pack_limit <= 0 || option == 0) return false;
+    return option == 1 || 4LL * c.n_short >= s.N;
+}
 
 // ---- planner (g3s_planner.cu) --------------------------------------------
 cudaError_t plan_validate(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s,
@@ -119,6 +139,9 @@ struct CoreParams {
     int normalize;  // aggregation: divide by (sum of weights + eps)
     int32_t* status;  // forward status word: kErrTimeout is OR-ed in when a bounded wait gives up
     int static_items;  // set by the launcher: one item per warp, by warp id (no work counter)
+    int pack_rows;     // run the short-row pack flavour (the plan's choice)
+    int pack;          // set by the launcher: rows per item (1, or the lane-group count)
+    int pack_max_deg;  // set by the launcher: a pack runs packed when no row has more entries
 };
 
 struct MergeParams {
@@ -159,6 +182,10 @@ cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaSt
 cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+// the short-row pack flavour: p.row_vecs <= 16, mode 0 or 2
+cudaError_t core_launch_pack_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_pack_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch_pack_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st);

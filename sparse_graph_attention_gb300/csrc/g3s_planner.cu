@@ -181,17 +181,23 @@ __device__ __forceinline__ int bucket_of_degree(int d, const Bounds& bd) {
     return k;
 }
 
-__global__ void k_bucket_classify(const int32_t* row_ptr, long long N, Bounds bd, uint8_t* bucket_of, PlanCounts* c) {
-    __shared__ int cnt[G3S_NUM_BUCKETS];
-    if (threadIdx.x < G3S_NUM_BUCKETS) cnt[threadIdx.x] = 0;
+// Also counts the rows with at most short_limit entries (the short-row packs'
+// candidates; short_limit 0: none counted).
+__global__ void k_bucket_classify(const int32_t* row_ptr, long long N, Bounds bd, int short_limit, uint8_t* bucket_of,
+                                  PlanCounts* c) {
+    __shared__ int cnt[G3S_NUM_BUCKETS + 1];
+    if (threadIdx.x <= G3S_NUM_BUCKETS) cnt[threadIdx.x] = 0;
     __syncthreads();
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += (long long)gridDim.x * blockDim.x) {
-        const int b = bucket_of_degree(row_ptr[i + 1] - row_ptr[i], bd);
+        const int d = row_ptr[i + 1] - row_ptr[i];
+        const int b = bucket_of_degree(d, bd);
         bucket_of[i] = (uint8_t)b;
         atomicAdd(&cnt[b], 1);
+        if (short_limit > 0 && d <= short_limit) atomicAdd(&cnt[G3S_NUM_BUCKETS], 1);
     }
     __syncthreads();
     if (threadIdx.x < G3S_NUM_BUCKETS && cnt[threadIdx.x]) atomicAdd(&c->bucket_count[threadIdx.x], cnt[threadIdx.x]);
+    if (threadIdx.x == G3S_NUM_BUCKETS && cnt[threadIdx.x]) atomicAdd(&c->n_short, cnt[threadIdx.x]);
 }
 
 __global__ void k_bucket_ptr(const PlanCounts* c, int32_t* bucket_ptr) {
@@ -608,7 +614,7 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
     Bounds bd;
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) bd.b[k] = s.bounds[k];
     if (s.N > 0) {
-        k_bucket_classify<<<grid_for(s.N, 256), 256, 0, st>>>(row_ptr, s.N, bd, a.bucket_of, c);
+        k_bucket_classify<<<grid_for(s.N, 256), 256, 0, st>>>(row_ptr, s.N, bd, s.pack_limit, a.bucket_of, c);
         G3S_TRY(cudaGetLastError());
     }
     k_bucket_ptr<<<1, 32, 0, st>>>(c, a.bucket_ptr);
