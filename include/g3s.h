@@ -203,9 +203,11 @@ g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int hea
  *   stream                all planner kernels run here; synchronised before return
  *   out                   receives the plan; free with g3s_plan_destroy
  * Besides its host struct, a plan with tile-path windows holds one CUDA
- * stream and two events: g3s_forward runs the tile kernel on that stream,
- * forked from and joined back into the caller's stream (so both kernels
- * overlap and the call stays capturable in a CUDA graph).
+ * stream (created at the device's highest stream priority) and two events:
+ * g3s_forward runs the CUDA-core kernel on that stream, forked from and
+ * joined back into the caller's stream, and the tile kernel on the caller's
+ * stream after it (so both kernels overlap, the few CUDA-core CTAs are
+ * placed first, and the call stays capturable in a CUDA graph).
  * Returns BAD_GRAPH when validation finds row_ptr[0] != 0, a decreasing
  * row_ptr, row_ptr[N] != E or a source outside [0, N).  With validation off
  * a malformed CSR is undefined behaviour.

@@ -162,12 +162,14 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->win_nnz = c.take<int32_t>(s.W);
         a->win_flags = c.take<uint8_t>(s.W);
         a->tile_windows = c.take<int32_t>(s.W);
+        a->core_windows = c.take<int32_t>(s.W);
         a->large_windows = c.take<int32_t>(s.W);
         a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
         a->tile_bits = c.take<uint32_t>(s.max_tiles * 4);
         a->bitmap_scratch = c.take<uint32_t>((long long)kLargeCtas * 3 * s.bitmap_words);
     } else {
         a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
+        a->core_windows = nullptr;
         a->win_flags = nullptr;
         a->tile_bits = a->bitmap_scratch = nullptr;
     }
@@ -303,7 +305,11 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
     p->edge_id = nullptr;
     p->edge_slots = num_edges;
     if (hc.n_tile_windows > 0) {
-        cudaError_t e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+        // the CUDA-core kernel runs here, at the highest priority, so its few
+        // CTAs are placed before the tile kernel's waves take every SM
+        int least = 0, greatest = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, greatest);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
         if (e != cudaSuccess) {
@@ -414,6 +420,10 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.part_acc = p->arr.part_acc;
     cp.part_ml = p->arr.part_ml;
     cp.win_flags = p->counts.n_tile_windows > 0 ? p->arr.win_flags : nullptr;
+    if (p->counts.n_tile_windows > 0) {
+        cp.core_windows = p->arr.core_windows;
+        cp.n_core_windows = s.W - p->counts.n_tile_windows;
+    }
     cp.work_counter = p->arr.work_counter;
     cp.N = s.N;
     cp.n_chunks = p->counts.n_chunks;
@@ -443,16 +453,19 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.tile_bits = p->arr.tile_bits;
         tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;
         tp.status = p->arr.fwd_status;
-        // the tile kernel on the side stream, the CUDA-core kernel on the caller's, overlapping
+        // the CUDA-core kernel first, on the plan's high-priority side stream,
+        // then the tile kernel on the caller's stream; the two overlap
         CUDA_OR_FAIL(cudaEventRecord(p->ev_fork, stream), "cudaEventRecord(fork)");
         CUDA_OR_FAIL(cudaStreamWaitEvent(p->side, p->ev_fork, 0), "cudaStreamWaitEvent(fork)");
-        CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, p->side), "tile kernel launch");
+        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, p->side),
+                     "fused kernel launch");
         CUDA_OR_FAIL(cudaEventRecord(p->ev_join, p->side), "cudaEventRecord(join)");
-    }
-    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, stream),
-                 "fused kernel launch");
-    if (p->counts.n_tile_windows > 0)
+        CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
         CUDA_OR_FAIL(cudaStreamWaitEvent(stream, p->ev_join, 0), "cudaStreamWaitEvent(join)");
+    } else {
+        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, stream),
+                     "fused kernel launch");
+    }
     if (p->counts.n_chunks > 0) {
         MergeParams mp{};
         mp.heavy_rows = p->arr.heavy_rows;

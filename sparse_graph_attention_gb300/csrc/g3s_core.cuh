@@ -598,21 +598,32 @@ __device__ __forceinline__ void process_pack(const CoreParams& p, const Lanes& L
 // bound by one row's latency chain, not by balance.
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : 1)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : (NV == 2 && MODE != kModeRtm ? 3 : 1))
     core_kernel(const CoreParams p) {
     static_assert(!PACK || (NV == 1 && MODE != kModeRtm), "packs: one vector per lane, no edge outputs");
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
     const int pack = PACK ? p.pack : 1;  // rows per item: 1, or G (the pack flavour; 16 % G == 0)
-    const unsigned long long total = n_chunks + (unsigned long long)((p.N + pack - 1) / pack);
+    // Row items: every row (pack) in id order, or with tile windows only the
+    // rows of the windows left to this kernel (16 rows = 16 / pack items each).
+    const int per_win = 16 / pack;
+    const unsigned long long total =
+        n_chunks + (p.core_windows != nullptr ? (unsigned long long)p.n_core_windows * per_win
+                                              : (unsigned long long)((p.N + pack - 1) / pack));
     auto run = [&](unsigned long long it) {
         if (it < n_chunks) {
             const int32_t* c = p.chunks + 3 * it;
             process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
             return;
         }
-        const int r0 = (int)(it - n_chunks) * pack;
-        if (p.win_flags != nullptr && (p.win_flags[r0 >> 4] & kFlagTile)) return;  // tile path (whole window)
+        int r0;
+        if (p.core_windows != nullptr) {
+            const long long q = (long long)(it - n_chunks);
+            r0 = p.core_windows[q / per_win] * 16 + (int)(q % per_win) * pack;
+            if (r0 >= p.N) return;  // past the last (partial) window
+        } else {
+            r0 = (int)(it - n_chunks) * pack;
+        }
         if constexpr (!PACK) {
             const int e0 = p.row_ptr[r0], e1 = p.row_ptr[r0 + 1];
             if (e1 - e0 > p.heavy_threshold) return;  // chunks + merge
@@ -717,7 +728,8 @@ cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
         p.pack = G;
         p.pack_max_deg = t;
     }
-    const long long items = p.n_chunks + (p.N + p.pack - 1) / p.pack;
+    const long long items = p.n_chunks + (p.core_windows != nullptr ? p.n_core_windows * (16 / p.pack)
+                                                                     : (p.N + p.pack - 1) / p.pack);
     if (items <= 0) return cudaSuccess;
     // one resident wave of CTAs (cached per instantiation and device)
     static int cached_dev = -1, cached_ctas = 0;

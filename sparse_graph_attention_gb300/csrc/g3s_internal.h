@@ -58,6 +58,7 @@ struct PlanArrays {
     int32_t* win_nnz;          // [W]
     uint8_t* win_flags;        // [W]
     int32_t* tile_windows;     // [W]
+    int32_t* core_windows;     // [W] the other windows, ascending (rows left to the CUDA-core kernel)
     int32_t* large_windows;    // [W]
     int32_t* tile_cols;        // [max_tiles][8]
     uint32_t* tile_bits;       // [max_tiles][4]
@@ -126,6 +127,10 @@ struct CoreParams {
     float* part_acc;
     float* part_ml;
     const uint8_t* win_flags;  // nullptr when no window takes the tile path
+    // With tile windows: the windows of 16 rows left to this kernel (ascending)
+    // and their count; its row items then run over these windows only.
+    const int32_t* core_windows;
+    long long n_core_windows;
     unsigned long long* work_counter;  // device scratch word, zeroed before every launch
     long long N;
     long long n_chunks;

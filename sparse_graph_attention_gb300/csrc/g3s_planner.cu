@@ -572,6 +572,10 @@ struct TileFlag {
     const uint8_t* win_flags;
     __device__ int operator()(long long w) const { return (win_flags[w] & kFlagTile) ? 1 : 0; }
 };
+struct CoreWindowFlag {
+    const uint8_t* win_flags;
+    __device__ int operator()(long long w) const { return (win_flags[w] & kFlagTile) ? 0 : 1; }
+};
 
 #define G3S_TRY(x)                          \
     do {                                    \
@@ -681,6 +685,7 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
         G3S_TRY(cudaGetLastError());
     }
     G3S_TRY(scan(TileFlag{a.win_flags}, ListOut{a.tile_windows}, W, a.scan_blocks, &c->n_tile_windows, st));
+    G3S_TRY(scan(CoreWindowFlag{a.win_flags}, ListOut{a.core_windows}, W, a.scan_blocks, nullptr, st));
     return cudaSuccess;
 }
 
