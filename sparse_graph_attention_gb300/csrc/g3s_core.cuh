@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "g3s_internal.h"
 
 namespace g3s {
@@ -597,19 +599,20 @@ __device__ __forceinline__ void process_pack(const CoreParams& p, const Lanes& L
 // exactly one item by its id (no counter, no memset launch): small graphs are
 // bound by one row's latency chain, not by balance.
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK>
+template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK, bool WINS>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm ? 3 : 4) : (NV == 2 && MODE != kModeRtm ? 3 : 1))
     core_kernel(const CoreParams p) {
     static_assert(!PACK || (NV == 1 && MODE != kModeRtm), "packs: one vector per lane, no edge outputs");
     const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
     const unsigned long long n_chunks = (unsigned long long)p.n_chunks;
     const int pack = PACK ? p.pack : 1;  // rows per item: 1, or G (the pack flavour; 16 % G == 0)
-    // Row items: every row (pack) in id order, or with tile windows only the
-    // rows of the windows left to this kernel (16 rows = 16 / pack items each).
-    const int per_win = 16 / pack;
+    // Row items: every row (pack) in id order; in the WINS flavour (plans with
+    // tile windows) only the rows of the windows left to this kernel, 16 / pack
+    // items a window.  (Kept apart: the extra mapping slows the plain flavour.)
+    const int pack_shift = __ffs(pack) - 1, win_shift = 4 - pack_shift;
     const unsigned long long total =
-        n_chunks + (p.core_windows != nullptr ? (unsigned long long)p.n_core_windows * per_win
-                                              : (unsigned long long)((p.N + pack - 1) / pack));
+        n_chunks + (WINS ? (unsigned long long)p.n_core_windows << win_shift
+                         : (unsigned long long)((p.N + pack - 1) / pack));
     auto run = [&](unsigned long long it) {
         if (it < n_chunks) {
             const int32_t* c = p.chunks + 3 * it;
@@ -617,12 +620,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
             return;
         }
         int r0;
-        if (p.core_windows != nullptr) {
-            const long long q = (long long)(it - n_chunks);
-            r0 = p.core_windows[q / per_win] * 16 + (int)(q % per_win) * pack;
+        if constexpr (WINS) {
+            const int q = (int)(it - n_chunks);  // row item (< N)
+            r0 = p.core_windows[q >> win_shift] * 16 + ((q & ((1 << win_shift) - 1)) << pack_shift);
             if (r0 >= p.N) return;  // past the last (partial) window
         } else {
             r0 = (int)(it - n_chunks) * pack;
+            if (p.win_flags != nullptr && (p.win_flags[r0 >> 4] & kFlagTile)) return;  // tile path (whole window)
         }
         if constexpr (!PACK) {
             const int e0 = p.row_ptr[r0], e1 = p.row_ptr[r0 + 1];
@@ -713,7 +717,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
-template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK>
+template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK, bool WINS = false>
 cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
     CoreParams p = p_in;
     // Short-row packs: one row per lane group, where a row is narrower than
@@ -728,8 +732,8 @@ cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
         p.pack = G;
         p.pack_max_deg = t;
     }
-    const long long items = p.n_chunks + (p.core_windows != nullptr ? p.n_core_windows * (16 / p.pack)
-                                                                     : (p.N + p.pack - 1) / p.pack);
+    if (WINS != (p.core_windows != nullptr)) return cudaErrorInvalidValue;
+    const long long items = p.n_chunks + (WINS ? p.n_core_windows * (16 / p.pack) : (p.N + p.pack - 1) / p.pack);
     if (items <= 0) return cudaSuccess;
     // one resident wave of CTAs (cached per instantiation and device)
     static int cached_dev = -1, cached_ctas = 0;
@@ -740,7 +744,7 @@ cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE, LPH, PACK>, kWarpsPerCta * 32,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, core_kernel<T, OutT, NV, MODE, LPH, PACK, WINS>, kWarpsPerCta * 32,
                                                           0);
         if (e != cudaSuccess) return e;
         cached_ctas = sms * (per_sm > 0 ? per_sm : 1);
@@ -752,19 +756,42 @@ cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
         CoreParams q = p;
         q.static_items = 1;
         const int ctas = (int)((items + kWarpsPerCta - 1) / kWarpsPerCta);
-        core_kernel<T, OutT, NV, MODE, LPH, PACK><<<ctas, kWarpsPerCta * 32, 0, st>>>(q);
+        core_kernel<T, OutT, NV, MODE, LPH, PACK, WINS><<<ctas, kWarpsPerCta * 32, 0, st>>>(q);
         return cudaGetLastError();
     }
     const long long need = (items + (long long)kWarpsPerCta * kItemsPerGrab - 1) / ((long long)kWarpsPerCta * kItemsPerGrab);
     const int ctas = (int)(need < cached_ctas ? need : cached_ctas);
     e = cudaMemsetAsync(p.work_counter, 0, sizeof(unsigned long long), st);
     if (e != cudaSuccess) return e;
-    core_kernel<T, OutT, NV, MODE, LPH, PACK><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
+    core_kernel<T, OutT, NV, MODE, LPH, PACK, WINS><<<ctas, kWarpsPerCta * 32, 0, st>>>(p);
     return cudaGetLastError();
+}
+
+// The WINS flavour: plans with tile windows, which exist for the standard
+// form with 16-bit inputs and head_dim 64 (8 vectors a head).
+template <typename T, typename OutT, bool PACK>
+cudaError_t launch_core_wins(const CoreParams& p, cudaStream_t st) {
+    if constexpr (std::is_same<T, float>::value) {
+        return cudaErrorInvalidValue;
+    } else {
+        if (p.lph != 8) return cudaErrorInvalidValue;
+        const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
+        if (PACK || nv == 1) return launch_core_nv<T, OutT, 1, kModeStd, 8, PACK, true>(p, st);
+        switch (nv) {
+            case 2: return launch_core_nv<T, OutT, 2, kModeStd, 0, false, true>(p, st);
+            case 4: return launch_core_nv<T, OutT, 4, kModeStd, 0, false, true>(p, st);
+            case 8: return launch_core_nv<T, OutT, 8, kModeStd, 0, false, true>(p, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
 }
 
 template <typename T, typename OutT, int MODE>
 cudaError_t launch_core(const CoreParams& p, cudaStream_t st) {
+    if (p.core_windows != nullptr) {
+        if constexpr (MODE == kModeStd) return launch_core_wins<T, OutT, false>(p, st);
+        return cudaErrorInvalidValue;
+    }
     const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
     if (nv == 1) {  // one vector per lane: the head-lane reduction is unrolled
         switch (p.lph) {
@@ -799,6 +826,10 @@ cudaError_t launch_core_mode(int mode, const CoreParams& p, cudaStream_t st) {
 template <typename T, typename OutT, int MODE>
 cudaError_t launch_core_packed(const CoreParams& p, cudaStream_t st) {
     if (p.row_vecs > 16) return cudaErrorInvalidValue;
+    if (p.core_windows != nullptr) {
+        if constexpr (MODE == kModeStd) return launch_core_wins<T, OutT, true>(p, st);
+        return cudaErrorInvalidValue;
+    }
     switch (p.lph) {
         case 2: return launch_core_nv<T, OutT, 1, MODE, 2, true>(p, st);
         case 4: return launch_core_nv<T, OutT, 1, MODE, 4, true>(p, st);
