@@ -549,19 +549,20 @@ __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L
 }
 
 // ---------------------------------------------------------------------------
-// A pack of G consecutive short rows, one per lane group (G = 32 / row_vecs
-// >= 2): every group walks its own row U edges per step, so a warp covers G
-// rows at once and no lane-group merge is needed.  Used when every row of the
-// pack has at most pack_max_deg <= 2 * group-size entries, held two per lane
-// of the group.  deg: this group's row length; maxdeg: the largest in the pack.
+// A pack of G consecutive rows, one per lane group (G = 32 / row_vecs >= 2):
+// every group walks its own short row U edges per step, so a warp covers G
+// rows at once and no lane-group merge is needed.  A short row has at most
+// pack_max_deg <= 2 * group-size entries, held two per lane of the group.
+// live: this group writes its row (a short row inside the graph; a long row
+// of the pack is left to the whole warp afterwards and passes deg 0 here);
+// deg: this group's row length; maxdeg: the largest among the pack's groups.
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT, int NV, int MODE, int LPH>
 __device__ __forceinline__ void process_pack(const CoreParams& p, const Lanes& L, const int row, const int e0,
-                                             const int deg, const int maxdeg) {
+                                             const int deg, const int maxdeg, const bool live) {
     constexpr int VP = Vec<T>::N / 2;
     constexpr int U = NV >= 4 ? 1 : 4 / NV;
     const int gs = L.gsize;
-    const bool live = row < p.N;
     ItemState<NV, VP> st;
     // the query of this group's row (row 0 stands in past the end) and an empty state
     init_item<T, NV, MODE, VP>(p, L, st, live ? row : 0, 0, 0);
@@ -633,24 +634,24 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
             if (e1 - e0 > p.heavy_threshold) return;  // chunks + merge
             process_item<T, OutT, NV, MODE, LPH>(p, L, r0, e0, e1, -1);
         } else {
-            // this group's row, then the pack's longest
+            // this group's row: the short ones are packed, one per group ...
             const int row = r0 + L.g;
             int e0 = 0, e1 = 0;
             if (row < p.N) {
                 e0 = p.row_ptr[row];
                 e1 = p.row_ptr[row + 1];
             }
-            const int maxdeg = __reduce_max_sync(kFull, e1 - e0);
-            if (maxdeg <= p.pack_max_deg) {
-                process_pack<T, OutT, NV, MODE, LPH>(p, L, row, e0, e1 - e0, maxdeg);
-                return;
-            }
-            // a long row in the pack: each row on the whole warp, in order
-            const int n_sub = pack < p.N - r0 ? pack : (int)(p.N - r0);
-            for (int j = 0; j < n_sub; ++j) {
-                const int a = __shfl_sync(kFull, e0, j * L.gsize), b = __shfl_sync(kFull, e1, j * L.gsize);
-                if (b - a > p.heavy_threshold) continue;  // chunks + merge
-                process_item<T, OutT, NV, MODE, LPH>(p, L, r0 + j, a, b, -1);
+            const bool is_short = e1 - e0 <= p.pack_max_deg;
+            const int sdeg = is_short ? e1 - e0 : 0;
+            process_pack<T, OutT, NV, MODE, LPH>(p, L, row, e0, sdeg, __reduce_max_sync(kFull, sdeg),
+                                                 is_short && row < p.N);
+            // ... then each longer one on the whole warp (heavy rows: chunks + merge)
+            unsigned longs = __ballot_sync(kFull, !is_short && e1 - e0 <= p.heavy_threshold);
+            while (longs) {
+                const int lane0 = __ffs(longs) - 1;  // first lane of the row's group
+                longs &= ~(((1u << (L.gsize - 1)) << 1) - 1u) << lane0;  // the whole group
+                const int a = __shfl_sync(kFull, e0, lane0), b = __shfl_sync(kFull, e1, lane0);
+                process_item<T, OutT, NV, MODE, LPH>(p, L, r0 + lane0 / L.gsize, a, b, -1);
             }
         }
     };
@@ -775,13 +776,16 @@ cudaError_t launch_core_wins(const CoreParams& p, cudaStream_t st) {
         return cudaErrorInvalidValue;
     } else {
         if (p.lph != 8) return cudaErrorInvalidValue;
-        const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
-        if (PACK || nv == 1) return launch_core_nv<T, OutT, 1, kModeStd, 8, PACK, true>(p, st);
-        switch (nv) {
-            case 2: return launch_core_nv<T, OutT, 2, kModeStd, 0, false, true>(p, st);
-            case 4: return launch_core_nv<T, OutT, 4, kModeStd, 0, false, true>(p, st);
-            case 8: return launch_core_nv<T, OutT, 8, kModeStd, 0, false, true>(p, st);
-            default: return cudaErrorInvalidValue;
+        if constexpr (PACK) {
+            return launch_core_nv<T, OutT, 1, kModeStd, 8, true, true>(p, st);
+        } else {
+            switch (p.row_vecs <= 32 ? 1 : p.row_vecs / 32) {
+                case 1: return launch_core_nv<T, OutT, 1, kModeStd, 8, false, true>(p, st);
+                case 2: return launch_core_nv<T, OutT, 2, kModeStd, 0, false, true>(p, st);
+                case 4: return launch_core_nv<T, OutT, 4, kModeStd, 0, false, true>(p, st);
+                case 8: return launch_core_nv<T, OutT, 8, kModeStd, 0, false, true>(p, st);
+                default: return cudaErrorInvalidValue;
+            }
         }
     }
 }
