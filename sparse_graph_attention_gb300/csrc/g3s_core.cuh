@@ -182,7 +182,8 @@ struct MixedDot<__half> {
 
 __device__ __forceinline__ float clamp5(float x) { return fminf(fmaxf(x, -5.0f), 5.0f); }
 
-// Store VE fp32 values as OutT at element offset `elem` (16-byte aligned).
+// Store VE fp32 values as OutT at element offset `elem` (16-byte aligned),
+// with the streaming hint (written once, never read back by this kernel).
 template <typename OutT, int VE>
 struct Store;
 template <int VE>
@@ -190,19 +191,19 @@ struct Store<float, VE> {
     __device__ static void run(void* base, long long elem, const float (&f)[VE]) {
         float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + elem);
 #pragma unroll
-        for (int k = 0; k < VE / 4; ++k) d[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+        for (int k = 0; k < VE / 4; ++k) __stcs(d + k, make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]));
     }
 };
 template <>
 struct Store<__nv_bfloat16, 8> {
     __device__ static void run(void* base, long long elem, const float (&f)[8]) {
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem) = Vec<__nv_bfloat16>::from_float(f);
+        __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem), Vec<__nv_bfloat16>::from_float(f));
     }
 };
 template <>
 struct Store<__half, 8> {
     __device__ static void run(void* base, long long elem, const float (&f)[8]) {
-        *reinterpret_cast<uint4*>(static_cast<__half*>(base) + elem) = Vec<__half>::from_float(f);
+        __stcs(reinterpret_cast<uint4*>(static_cast<__half*>(base) + elem), Vec<__half>::from_float(f));
     }
 };
 
