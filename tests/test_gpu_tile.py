@@ -149,3 +149,21 @@ def test_tile_rows_with_no_edges():
     plan, O, _ = _run(g, 1, "bf16", dict(tile_path=1, tile_density_milli=0))
     assert plan.stats()["tile_windows"] == 4
     assert torch.count_nonzero(O[[3, 17, 18, 40]]).item() == 0
+
+
+@pytest.mark.parametrize("H", [1, 8])
+def test_tile_mixed_full_size_persistent_core_rows(H):
+    """Full-size batched graphs with p = 0.5: about 60% of the windows on
+    tiles and the rest left to the CUDA-core kernel's window list, with more
+    of those rows than resident warps (its persistent loop).  H = 1 also
+    takes the short-row pack flavour beside the tile windows.  Sampled rows
+    and both ends are checked."""
+    g = graphgen.batched_dense(num_graphs=1024, p=0.5, seed=1003)
+    vals = graphgen.make_values(g.num_nodes, g.num_edges, H, 64, False, seed=2003)
+    rows = np.unique(np.concatenate([np.random.default_rng(17).choice(g.num_nodes, 4000, replace=False),
+                                     np.arange(16), g.num_nodes - 1 - np.arange(16)]))
+    plan, _, _ = run_case(g, vals, H, 64, "bf16", "standard", rows=rows, plan_kw=dict(pack_rows=1 if H == 1 else -1))
+    plan.check()
+    st = plan.stats()
+    core_rows = 16 * (st["windows"] - st["tile_windows"])
+    assert 0 < st["tile_windows"] < st["windows"] and core_rows > 152 * 8 * 3
