@@ -64,14 +64,39 @@ def measured_bf16_peak(sustained: bool):
         return (1700.0 if sustained else 1900.0), "fallback"
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank runs (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_sources_hash() -> str:
+    """Hash of the CUDA sources' code (comments and blank lines left out, so a
+    comment edit does not void a DRAM-traffic record of the same kernels)."""
     csrc = os.path.join(ROOT, "sparse_graph_attention_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(f.encode())
-                h.update(fh.read())
+                h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -13,6 +13,8 @@
 // applied after the reduction).  Every group keeps its own online-softmax state (running
 // max m, denominator l, fp32 accumulator) in registers; the groups are merged
 // with a fixed butterfly at the end, so the result does not depend on timing.
+// In the pack flavour a work item is instead G consecutive short rows, one
+// per lane group, each walked by its group alone (no merge).
 //
 // This is the per-node gather of the Triton article (stondelli.it/articles/
 // gattn-triton, "Using the CSC index for fast edge lookup" and "Fusing the
@@ -589,7 +591,12 @@ __device__ __forceinline__ void process_pack(const CoreParams& p, const Lanes& L
 
 // ---------------------------------------------------------------------------
 // The fused kernel.  T: input element type; OutT: type of O and Eout (fp32
-// or T); NV: 16-byte vectors per lane per edge; RTM: edge-modulated variant.
+// or T); NV: 16-byte vectors per lane per edge; MODE: standard, RTMScore or
+// weighted aggregation; LPH: lanes per head when known at compile time (0:
+// from the parameters); PACK: the short-row pack flavour (items are packs of
+// G rows); WINS: the window-list flavour (plans with tile windows: row items
+// only over the windows the tile kernel leaves).  The flavours are separate
+// instantiations because their extra code costs the plain one registers.
 //
 // Persistent: the grid fills the GPU once and every warp takes work items
 // (heavy-row chunks first, then rows in ascending id) kItemsPerGrab at a
