@@ -251,6 +251,9 @@ def parse_args():
     ap.add_argument("--layer", type=int, default=0, metavar="KIN",
                     help="also time one attention layer on 16-bit workloads: Q|K|V = X Wqkv^T for X of KIN "
                          "features (the tcgen05 projection), then the forward; adds a 'layer' object")
+    ap.add_argument("--aggregate", action="store_true",
+                    help="also time g3s_aggregate (normalised weighted aggregation) on the workload's graph; "
+                         "adds an 'aggregate' object")
     ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
                     help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
     ap.add_argument("--pack-rows", type=int, default=None, choices=[0, 1],
@@ -291,6 +294,54 @@ def run_reference(args, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def aggregate_bytes(g, w, out_dtype):
+    """Algorithmic bytes of one g3s_aggregate: CSR + per edge its weights (H)
+    and its source row of X (H*d) + O written once; the compulsory count
+    reads X once instead of once per edge."""
+    e, eo = ELT[w.dtype], ELT[out_dtype]
+    N, E, H, HD = g.num_nodes, g.num_edges, w.heads, w.heads * w.head_dim
+    csr = 4 * (N + 1) + 4 * E
+    gathered = csr + E * H * e + E * HD * e + N * HD * eo
+    compulsory = csr + E * H * e + N * HD * e + N * HD * eo
+    return gathered, compulsory
+
+
+def time_aggregate(args, g, w, plan, O, stream, dev):
+    """g3s_aggregate (normalised weighted aggregation) over the workload's
+    graph, X = the workload's V, seeded positive weights per edge and head."""
+    import torch
+    import sparse_graph_attention_gb300 as g3s
+    tdt = g3s.torch_dtype(w.dtype)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4000 + w.number)
+    X = torch.randn(g.num_nodes, w.heads, w.head_dim, device=dev, generator=gen).to(tdt)
+    Wt = (torch.rand(g.num_edges, w.heads, device=dev, generator=gen) + 0.05).to(tdt)
+
+    def step():
+        plan.aggregate(Wt, X, O=O, normalize=True, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 100))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / n
+    gathered, compulsory = aggregate_bytes(g, w, plan.out_dtype)
+    hbm, hbm_src = measured_hbm_peak()
+    sec = ms / 1e3
+    return {"ms": ms, "edges_per_s": g.num_edges / sec, "normalize": True,
+            "roofline": {"bound": "hbm", "achieved": gathered / sec / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": gathered / sec / 1e9 / hbm, "peak_source": hbm_src,
+                         "compulsory_gbs": compulsory / sec / 1e9, "compulsory_frac": compulsory / sec / 1e9 / hbm,
+                         "bytes_model": "gathered: CSR + W per edge + X row per edge + O; compulsory: X once"},
+            "data": "seeded synthetic X and positive weights (torch generator)"}
 
 
 def time_layer(args, g, w, plan, O, Eout, stream, dev):
@@ -483,6 +534,9 @@ def main():
     layer = None
     if args.layer:
         layer = time_layer(args, g, w, plan, O, Eout, stream, dev)
+    aggregate = None
+    if args.aggregate:
+        aggregate = time_aggregate(args, g, w, plan, O, stream, dev)
 
     # ---- end to end through the C ABI on host buffers --------------------
     # Every step uploads its Q, K, V (and E) from pinned host memory and
@@ -563,6 +617,7 @@ def main():
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
+            "aggregate": aggregate,
             "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
                      "pack_rows": plan.options.pack_rows,
                      "tile_windows": st["tile_windows"],

@@ -51,3 +51,33 @@ def test_byte_model():
     hd = w.heads * w.head_dim
     assert gathered == 4 * (g.num_nodes + 1) + 4 * g.num_edges + 2 * g.num_nodes * hd * 4 + 2 * g.num_edges * hd * 4
     assert compulsory == 4 * (g.num_nodes + 1) + 4 * g.num_edges + 4 * g.num_nodes * hd * 4
+
+
+def test_aggregate_byte_model():
+    import graphgen
+
+    g = graphgen.tiny_poisson()
+    w = graphgen.WORKLOADS["tiny_poisson"]
+    gathered, compulsory = bench.aggregate_bytes(g, w, "f32")
+    n, e, h, hd = g.num_nodes, g.num_edges, w.heads, w.heads * w.head_dim
+    csr = 4 * (n + 1) + 4 * e
+    # per edge: its H weights and its source's H*d features; O once
+    assert gathered == csr + e * h * 4 + e * hd * 4 + n * hd * 4
+    assert compulsory == csr + e * h * 4 + n * hd * 4 + n * hd * 4
+
+
+def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
+    """The DRAM-traffic record stays valid across comment edits of the CUDA
+    sources and is voided by any code edit."""
+    csrc = tmp_path / "sparse_graph_attention_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    f = csrc / "k.cu"
+    f.write_text('__global__ void k(int* p) { p[0] = 1; }  // one\n/* block */\nconst char* s = "a//b";\n')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_sources_hash()
+    f.write_text('// header\n__global__ void k(int* p) { p[0] = 1; }  // two\n\nconst char* s = "a//b";\n')
+    assert bench.kernel_sources_hash() == h0
+    f.write_text('__global__ void k(int* p) { p[0] = 2; }\nconst char* s = "a//b";\n')
+    assert bench.kernel_sources_hash() != h0
+    f.write_text('__global__ void k(int* p) { p[0] = 1; }\nconst char* s = "a//c";\n')
+    assert bench.kernel_sources_hash() != h0
