@@ -192,9 +192,10 @@ struct g3s_plan {
     size_t ws_used;
     const int32_t* edge_id;  // optional CSR position -> physical edge slot
     long long edge_slots;    // rows of E / Eout / W (E without edge ids)
-    // With tile windows, the tile kernel runs on this side stream beside the
-    // CUDA-core kernel (forked from and joined back into the caller's stream
-    // with the two events); created with the plan, destroyed with it.
+    // With tile windows, the CUDA-core kernel runs on this high-priority side
+    // stream (forked from and joined back into the caller's stream with the
+    // two events) while the tile kernel runs on the caller's; created with
+    // the plan, destroyed with it.
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
