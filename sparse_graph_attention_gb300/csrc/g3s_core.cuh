@@ -386,15 +386,37 @@ __device__ __forceinline__ void fetch_math(const CoreParams& p, const Lanes& L, 
     edge_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, kr, vr, er, wg, ok, eid);
 }
 
+// Edges a lane group takes per step (U): four 16-byte K and V vectors in
+// flight per lane; the aggregation gathers no K, so it takes twice as many.
+template <int NV, int MODE>
+struct StepEdges {
+    static constexpr int value = (NV >= 4 ? 1 : 4 / NV) * (MODE == kModeAgg ? 2 : 1);
+};
+
 // One step of S = G * U edges starting at CSR position `base`.  TAIL: the
 // step runs past the row's end; slots beyond it re-read the row's last edge
 // (a valid, cached address) and get weight 0, so no load is branched.
 template <bool TAIL, typename T, typename OutT, int NV, int MODE, int VP, int LPH>
 __device__ __forceinline__ void edge_step(const CoreParams& p, const Lanes& L, ItemState<NV, VP>& st, const int base,
                                           const int e1) {
-    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    constexpr int U = StepEdges<NV, MODE>::value;
     const int g = L.g;
     const int S = L.G * U;
+    if constexpr (U > 4) {  // aggregation: a step can span more than the 64-index window
+        if (S > 64) {       // (16 lane groups): each slot loads its index itself
+            int src[U], epos[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int pos = base + g * U + u;
+                ok[u] = !TAIL || pos < e1;
+                epos[u] = ok[u] ? pos : e1 - 1;
+                src[u] = __ldg(p.col_idx + epos[u]);
+            }
+            fetch_math<U, T, OutT, NV, MODE, VP, LPH>(p, L, st, src, ok, epos);
+            return;
+        }
+    }
     if (base - st.cbase >= 64) {  // warp-uniform: the next 64 indices
         st.cbase += 64;
         st.idx_lo = (st.cbase + L.lane < e1) ? __ldg(p.col_idx + st.cbase + L.lane) : 0;
@@ -540,7 +562,7 @@ template <typename T, typename OutT, int NV, int MODE, int LPH>
 __device__ __forceinline__ void process_item(const CoreParams& p, const Lanes& L, const int row, const int e0,
                                              const int e1, const long long chunk) {
     constexpr int VP = Vec<T>::N / 2;
-    constexpr int U = NV >= 4 ? 1 : 4 / NV;
+    constexpr int U = StepEdges<NV, MODE>::value;
     const int S = L.G * U;
     ItemState<NV, VP> st;
     init_item<T, NV, MODE, VP>(p, L, st, row, e0, e1);
