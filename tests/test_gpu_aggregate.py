@@ -86,3 +86,27 @@ def test_aggregate_argument_errors():
     assert lib.g3s_aggregate(plan.handle, None, x.data_ptr(), x.data_ptr(), 0, 1e-6, s) == 1
     assert lib.g3s_aggregate(plan.handle, w.data_ptr(), x[1:].data_ptr(), x.data_ptr(), 0, 1e-6, s) == 1
     assert lib.g3s_aggregate(plan.handle, w.data_ptr(), x.data_ptr(), x.data_ptr(), 1, -1.0, s) == 1
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("pack", [0, 1])
+def test_aggregate_32_byte_rows(dtype, pack):
+    """Rows of 32 bytes (one head of 16 16-bit values): 16 lane groups of
+    eight edges make a step of 128 slots, wider than the 64-entry index
+    window, so each slot loads its own index; short rows, long rows, heavy
+    rows (chunks) and empty rows, with and without short-row packs."""
+    rng = np.random.default_rng(21)
+    n = 1500
+    deg = rng.integers(0, 6, n)
+    deg[rng.random(n) < 0.1] = rng.integers(60, 400, 1)[0]
+    deg[::97] = 0
+    deg[5] = 1200  # a heavy row
+    rows = [np.sort(rng.choice(n, int(k), replace=False)) for k in deg]
+    rp = np.zeros(n + 1, np.int64)
+    rp[1:] = np.cumsum(deg)
+    g = graphgen.Graph(rp.astype(np.int32), np.concatenate(rows).astype(np.int32))
+    plan = _case(g, 1, 16, dtype, True, positive=True, seed=22, plan_kw=dict(pack_rows=pack, heavy_threshold=500,
+                                                                              chunk_edges=130))
+    st = plan.stats()
+    assert st["chunks"] > 0 and st["pack_rows"] == pack
+    _case(g, 1, 16, dtype, False, positive=False, seed=23, plan_kw=dict(pack_rows=pack))
