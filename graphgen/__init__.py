@@ -329,7 +329,7 @@ WORKLOADS: Dict[str, Workload] = {
                  "N=2M, log-normal(3.6,0.8) in-degree (~100M edges), 60% sources within +-4096, 4x32 bf16"),
         # not one of the five benchmark configurations: the dense end of the
         # batched family, where the row windows are full and the tensor-core
-        # tile path is the faster one (it is chosen by default above density 0.5)
+        # tile path is the faster one (taken by default from window density 0.4)
         Workload(6, "batched_complete", batched_dense, dict(num_graphs=1024, p=1.0), dict(num_graphs=24, p=1.0),
                  8, 64, "bf16", "standard",
                  "1024 complete graphs of U[20,60] nodes (with self loops), 8x64 bf16"),

@@ -767,7 +767,7 @@ cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
     const long long items = p.n_chunks + (WINS ? p.n_core_windows * (16 / p.pack) : (p.N + p.pack - 1) / p.pack);
     if (items <= 0) return cudaSuccess;
     // one resident wave of CTAs (cached per instantiation and device)
-    static int cached_dev = -1, cached_ctas = 0;
+    thread_local int cached_dev = -1, cached_ctas = 0;  // per host thread: no shared mutable state
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -177,7 +177,7 @@ cudaError_t launch_core_tma_lph(const CoreParams& p, const CUtensorMap& tk, cons
     if (items <= 0) return cudaSuccess;
     auto kern = core_tma_kernel<T, OutT, RV, LPH, D>;
     const int smem = kWarpsPerCta * D * kTmaStageBytes + 1024;
-    static int cached_dev = -1, cached_ctas = 0;
+    thread_local int cached_dev = -1, cached_ctas = 0;  // per host thread: no shared mutable state
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -301,7 +301,7 @@ cudaError_t launch_lin(const LinearParams& p, cudaStream_t st) {
         mp.esz = esz;
     }
     const int smem = (int)sizeof(LinSmem<BN>) + 1024;
-    static int cached_dev = -1, sms = 0;
+    thread_local int cached_dev = -1, sms = 0;  // per host thread: no shared mutable state
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
