@@ -149,7 +149,8 @@ typedef struct g3s_plan_stats {
     int32_t has_bsb, tile_path;
     int64_t windows, tiles, tile_windows, dup_windows, large_windows;
     int64_t tile_window_nnz; /* CSR entries handled by the tile path */
-    int32_t pack_rows;       /* 1 when forwards use short-row packs */
+    int32_t pack_rows;       /* 1 when standard-form forwards and aggregations use short-row
+                                packs (an RTMScore forward never does) */
     int32_t pack_limit;      /* most entries of a packed row (0: this row width does not pack) */
     int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
