@@ -619,7 +619,7 @@ def main():
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
             "aggregate": aggregate,
             "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
-                     "pack_rows": plan.options.pack_rows,
+                     "heavy_threshold": st["heavy_threshold"], "pack_rows": st["pack_rows"],
                      "tile_windows": st["tile_windows"],
                      "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},
         }

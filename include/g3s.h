@@ -78,8 +78,11 @@ typedef enum g3s_variant {
  *  bucket_bounds   inclusive upper degree bounds of buckets 1..3 (bucket 0 is
  *                  degree 0, bucket 4 is above bucket_bounds[2]); default 32, 256, 2048
  *  heavy_threshold rows with more in-edges are cut into chunks processed by
- *                  several warps and merged (default 512)
- *  chunk_edges     CSR positions per chunk of a heavy row (default 256)
+ *                  several warps and merged; chunks are taken before the rows,
+ *                  so long rows do not finish last.  0 (default): ten times
+ *                  the mean degree E/N, clamped to [64, 512] (stats.heavy_threshold
+ *                  reports the value used)
+ *  chunk_edges     CSR positions per chunk of a heavy row (default 512)
  *  bsb             build the 16x8 BSB tiles: 1 on, 0 off, -1 when the tile path
  *                  is eligible (default -1)
  *  tile_path       route dense row windows to the tensor-core kernel: 1 on,
@@ -152,6 +155,8 @@ typedef struct g3s_plan_stats {
     int32_t pack_rows;       /* 1 when standard-form forwards and aggregations use short-row
                                 packs (an RTMScore forward never does) */
     int32_t pack_limit;      /* most entries of a packed row (0: this row width does not pack) */
+    int32_t heavy_threshold; /* the heavy-row threshold in use (option 0 resolved) */
+    int32_t chunk_edges;     /* CSR positions per heavy-row chunk */
     int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
 } g3s_plan_stats;
@@ -377,7 +382,8 @@ void g3s_plan_destroy(g3s_plan *plan);
  * G3S_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading this library
  * holds until the process exits.  A graph whose plan needs more -- the size
  * g3s_plan_workspace_size reports with bsb = 0, about 9 bytes per node plus
- * 6*(H*d + 2*H + 3) bytes per 256 edges -- is rejected with
+ * 4*(H*d + 2*H + 3) bytes per possible chunk, E/512 + E/(T+1) of them for
+ * the automatic heavy-row threshold T -- is rejected with
  * G3S_ERR_WORKSPACE before any device work.
  *
  * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call

@@ -59,6 +59,16 @@ def degree_buckets(row_ptr: np.ndarray, bounds) -> dict:
                 bucket_rows=order.astype(np.int32))
 
 
+def auto_heavy_threshold(num_nodes: int, num_edges: int) -> int:
+    """The planner's default heavy-row threshold (a scheduling choice of this
+    library, not of the pages): ten times the mean degree, rounded to the
+    nearest integer, clamped to [64, 512]; 512 for an empty graph."""
+    if num_nodes <= 0:
+        return 512
+    t = (10 * int(num_edges) + int(num_nodes) // 2) // int(num_nodes)
+    return int(min(max(t, 64), 512))
+
+
 def heavy_chunks(row_ptr: np.ndarray, heavy_threshold: int, chunk_edges: int) -> dict:
     deg = degrees(row_ptr)
     heavy = np.flatnonzero(deg > heavy_threshold)

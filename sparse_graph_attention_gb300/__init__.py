@@ -79,7 +79,8 @@ class PlanStats(ctypes.Structure):
         ("windows", ctypes.c_int64), ("tiles", ctypes.c_int64), ("tile_windows", ctypes.c_int64),
         ("dup_windows", ctypes.c_int64), ("large_windows", ctypes.c_int64),
         ("tile_window_nnz", ctypes.c_int64),
-        ("pack_rows", ctypes.c_int32), ("pack_limit", ctypes.c_int32), ("short_rows", ctypes.c_int64),
+        ("pack_rows", ctypes.c_int32), ("pack_limit", ctypes.c_int32),
+        ("heavy_threshold", ctypes.c_int32), ("chunk_edges", ctypes.c_int32), ("short_rows", ctypes.c_int64),
         ("workspace_used", ctypes.c_size_t),
     ]
 

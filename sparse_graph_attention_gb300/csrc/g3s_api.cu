@@ -60,8 +60,8 @@ void default_options(g3s_plan_options* o) {
     o->bucket_bounds[0] = 32;
     o->bucket_bounds[1] = 256;
     o->bucket_bounds[2] = 2048;
-    o->heavy_threshold = 512;
-    o->chunk_edges = 256;
+    o->heavy_threshold = 0;  // automatic: 10 x mean degree in [64, 512]
+    o->chunk_edges = 512;
     o->bsb = -1;
     o->tile_path = -1;
     o->tile_density_milli = 400;
@@ -95,7 +95,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
         if (o.bucket_bounds[k] < 1 || (k > 0 && o.bucket_bounds[k] <= o.bucket_bounds[k - 1]))
             return fail(G3S_ERR_INVALID_ARG, "bucket_bounds must be positive and increasing");
     }
-    if (o.heavy_threshold < 1) return fail(G3S_ERR_INVALID_ARG, "heavy_threshold must be >= 1");
+    if (o.heavy_threshold < 0) return fail(G3S_ERR_INVALID_ARG, "heavy_threshold must be >= 0 (0: automatic)");
     if (o.chunk_edges < 1) return fail(G3S_ERR_INVALID_ARG, "chunk_edges must be >= 1");
     if (o.bsb < -1 || o.bsb > 1 || o.tile_path < -1 || o.tile_path > 1)
         return fail(G3S_ERR_INVALID_ARG, "bsb and tile_path take -1, 0 or 1");
@@ -116,8 +116,16 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->E = E;
     s->H = heads;
     s->D = head_dim;
-    s->heavy_threshold = o.heavy_threshold;
-    s->pack_limit = pack_limit_for((int)row_vecs, o.heavy_threshold);
+    // Heavy rows go to the front of the work queue as chunks.  Automatic
+    // threshold: rows over ten times the mean degree (a long row taken late
+    // in id order would otherwise finish last), between 64 and 512.
+    if (o.heavy_threshold > 0) {
+        s->heavy_threshold = o.heavy_threshold;
+    } else {
+        const long long t = N > 0 ? (10 * E + N / 2) / N : 512;
+        s->heavy_threshold = (int)(t < 64 ? 64 : (t > 512 ? 512 : t));
+    }
+    s->pack_limit = pack_limit_for((int)row_vecs, s->heavy_threshold);
     s->chunk_edges = o.chunk_edges;
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
@@ -130,7 +138,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->build_bsb = o.bsb == 1 || (o.bsb == -1 && s->tile_enabled);
     if (s->tile_enabled && !s->build_bsb)
         return fail(G3S_ERR_INVALID_ARG, "the tile path needs the BSB tiles (bsb = 0 with tile_path on)");
-    const long long T = o.heavy_threshold;
+    const long long T = s->heavy_threshold;
     s->max_heavy = N < E / (T + 1) ? N : E / (T + 1);
     s->max_chunks = E / o.chunk_edges + s->max_heavy;
     s->W = (N + kWinRows - 1) / kWinRows;
@@ -349,6 +357,8 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->tile_window_nnz = p->counts.tile_window_nnz;
     st->pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
     st->pack_limit = p->shape.pack_limit;
+    st->heavy_threshold = p->shape.heavy_threshold;
+    st->chunk_edges = p->shape.chunk_edges;
     st->short_rows = p->counts.n_short;
     st->workspace_used = p->ws_used;
     return G3S_OK;

@@ -211,6 +211,28 @@ def test_planner_bit_exact(name, g, kw):
         assert st["large_windows"] > 0
 
 
+def test_planner_default_heavy_threshold():
+    """Default options: the heavy-row threshold is ten times the mean degree
+    in [64, 512], chunks of 512, and the heavy rows and chunks equal the
+    reference planner's for that threshold."""
+    ensure_built()
+    graphs = [graphgen.powerlaw(num_nodes=20_000, seed=41),                      # mean 14: 143
+              graphgen.lognormal_local(num_nodes=20_000, radius=512, seed=42),    # mean 50: ~504
+              graphgen.tiny_poisson(seed=43),                                     # no heavy row
+              graphgen.random_csr(300, 3, seed=44, zero_frac=0.5)]                # mean < 6.4: 64
+    for g in graphs:
+        rp, ci = upload_graph(g)
+        plan = g3s.Plan(rp, ci, g.num_nodes, 1, 64, "f16")
+        st = plan.stats()
+        t = ref_planner.auto_heavy_threshold(g.num_nodes, g.num_edges)
+        assert st["heavy_threshold"] == t and st["chunk_edges"] == 512
+        ref = ref_planner.heavy_chunks(g.row_ptr, t, 512)
+        for name_ in ("heavy_rows", "heavy_chunk_ptr", "chunks"):
+            got = plan.export(name_)
+            assert np.array_equal(got, ref[name_].astype(got.dtype)), name_
+    assert ref_planner.auto_heavy_threshold(20_000, 285_200) == 143
+
+
 # ---------------------------------------------------------------------------
 # errors
 # ---------------------------------------------------------------------------
