@@ -677,9 +677,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
                                                  is_short && row < p.N);
             // ... then each longer one on the whole warp (heavy rows: chunks + merge)
             unsigned longs = __ballot_sync(kFull, !is_short && e1 - e0 <= p.heavy_threshold);
+            const unsigned group_bits = (1u << L.gsize) - 1u;  // gsize <= 16 in a pack
             while (longs) {
                 const int lane0 = __ffs(longs) - 1;  // first lane of the row's group
-                longs &= ~(((1u << (L.gsize - 1)) << 1) - 1u) << lane0;  // the whole group
+                longs &= ~(group_bits << lane0);      // the whole group
                 const int a = __shfl_sync(kFull, e0, lane0), b = __shfl_sync(kFull, e1, lane0);
                 process_item<T, OutT, NV, MODE, LPH>(p, L, r0 + lane0 / L.gsize, a, b, -1);
             }
