@@ -134,3 +134,18 @@ def test_noalloc_rejects_graphs_beyond_its_scratch(lib):
     assert st == 4
     assert b"static scratch" in lib.g3s_last_error()
     assert g3s.workspace_size(200_000, 2_850_000, 1, 64, "f16", bsb=0) <= g3s.NOALLOC_SCRATCH_BYTES
+
+
+@pytest.mark.parametrize("n,e", [(320, 4480), (200_000, 2_851_788), (2_000_000, 100_717_572), (1000, 10),
+                                 (10, 100_000), (0, 0)])
+def test_automatic_heavy_threshold_sizes_like_its_value(lib, n, e):
+    """heavy_threshold = 0 resolves to ten times the mean degree in [64, 512]
+    (512 for an empty graph): the workspace bound equals the one for that
+    value given explicitly."""
+    from oracle import planner
+
+    t = planner.auto_heavy_threshold(n, e)
+    assert 64 <= t <= 512
+    assert g3s.workspace_size(n, e, 4, 32, "bf16") == g3s.workspace_size(n, e, 4, 32, "bf16", heavy_threshold=t)
+    if 0 < n and 64 < 10 * e / n < 512:
+        assert g3s.workspace_size(n, e, 4, 32, "bf16") != g3s.workspace_size(n, e, 4, 32, "bf16", heavy_threshold=t + 7)
