@@ -93,8 +93,8 @@ typedef enum g3s_variant {
  *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 400:
  *                  the tile kernel's time follows its tiles, the CUDA-core
  *                  kernel's its edges; measured on batched 20-60-node graphs
- *                  they cross near a window density of 0.4-0.5, and on
- *                  complete graphs the tile path is about twice as fast)
+ *                  they cross near edge probability 0.55, and on complete
+ *                  graphs the tile path is about 1.6 times as fast)
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 32)
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
