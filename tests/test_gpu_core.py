@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import graphgen
+import oracle
 from oracle import planner as ref_planner
 import sparse_graph_attention_gb300 as g3s
 
@@ -282,3 +283,27 @@ def test_argument_errors():
     ws = torch.empty(1024, dtype=torch.uint8, device=dev)
     assert lib.g3s_plan_create(rp.data_ptr(), ci.data_ptr(), g.num_nodes, g.num_edges, 8, 32, 2, 0, ctypes.byref(o),
                                ws.data_ptr(), 1024, s, ctypes.byref(out)) == 4
+
+
+@pytest.mark.parametrize("tma", [0, 1])
+def test_repeated_persistent_launches(tma):
+    """Forwards and aggregations on one plan, back to back in the persistent
+    launch form (the work queue reused): every repeat gives the first one's
+    bits, with the plain or the TMA-fed forward."""
+    ensure_built()
+    g = graphgen.lognormal_local(num_nodes=120_000, radius=1024, seed=61)
+    vals = graphgen.make_values(g.num_nodes, g.num_edges, 4, 32, False, seed=62)
+    t = {k: v.to(device()) for k, v in cast_values(vals, "bf16").items()}
+    rp, ci = upload_graph(g)
+    plan = g3s.Plan(rp, ci, g.num_nodes, 4, 32, "bf16", tma_gather=tma)
+    W = torch.ones(g.num_edges, 4, dtype=torch.bfloat16, device=device())
+    first = plan.forward(t["Q"], t["K"], t["V"]).clone()
+    agg0 = plan.aggregate(W, t["V"], normalize=True).clone()
+    for _ in range(3):
+        assert torch.equal(plan.forward(t["Q"], t["K"], t["V"]), first)
+        assert torch.equal(plan.aggregate(W, t["V"], normalize=True), agg0)
+    plan.check()
+    rows = np.random.default_rng(63).choice(g.num_nodes, 2000, replace=False)
+    want = oracle.forward(g.row_ptr, g.col_idx, g.num_nodes, 4, 32, "bf16", "standard",
+                          *(cast_values(vals, "bf16")[k] for k in "QKV"), rows=rows)
+    assert_close(first[torch.from_numpy(rows).to(device())], want, "bf16", "O")
