@@ -173,7 +173,9 @@ typedef enum g3s_plan_array {
     G3S_ARR_TILE_BITS = 7,       /* uint32 [tiles][4], bit r*8+c of a 128-bit word */
     G3S_ARR_WIN_NNZ = 8,         /* [W] CSR entries per window */
     G3S_ARR_WIN_FLAGS = 9,       /* uint8 [W]: bit0 repeated edge, bit1 tile path */
-    G3S_ARR_TILE_WINDOWS = 10    /* [tile_windows] ascending */
+    G3S_ARR_TILE_WINDOWS = 10,   /* [tile_windows] ascending */
+    G3S_ARR_CORE_WINDOWS = 11    /* [windows - tile_windows] ascending: the windows whose rows the
+                                    CUDA-core kernel takes (every window without bit 1) */
 } g3s_plan_array;
 
 typedef struct g3s_plan g3s_plan; /* opaque */
@@ -389,6 +391,9 @@ void g3s_plan_destroy(g3s_plan *plan);
  * Calls no cudaMalloc, cudaFree or other allocating routine.  The first call
  * on a device looks up the scratch's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.
+ * The address is kept for the life of the process: after cudaDeviceReset on
+ * a device (which ends its context and the library's device memory with
+ * it) do not call this entry point on that device again.
  * Every call on a device shares the one scratch array and leaves its
  * contents behind (the counters it needs are cleared at the start of each
  * call), so calls that overlap on the GPU, from any stream or thread, race:

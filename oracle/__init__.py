@@ -61,6 +61,8 @@ def _bind(path):
     lib.g3s_oracle_decode.argtypes = [ctypes.c_int, P, ctypes.c_int64, P]
     lib.g3s_oracle_decode.restype = ctypes.c_int
     lib.g3s_oracle_threads.restype = ctypes.c_int
+    lib.g3s_oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.g3s_oracle_set_threads.restype = None
     lib.g3s_oracle_aggregate.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
                                          ctypes.c_int64, P, ctypes.c_int, ctypes.c_double]
     lib.g3s_oracle_aggregate.restype = ctypes.c_int
@@ -82,6 +84,11 @@ def load_library(path: str):
 
 def threads() -> int:
     return int(_load().g3s_oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads the oracle's later calls use (results do not depend on it)."""
+    _load().g3s_oracle_set_threads(int(n))
 
 
 def _raw(x, dtype: str) -> np.ndarray:

@@ -111,6 +111,17 @@ int g3s_oracle_threads(void)
 #endif
 }
 
+/* Thread count of later calls (n >= 1); for timing the oracle on one core
+ * and on all of them.  Results do not depend on it (fixed per-row order). */
+void g3s_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /*
  * Standard or RTMScore attention for the rows listed in rows[0..n_rows).
  *   O_out   : (n_rows, H, d) doubles, row k holds destination rows[k]

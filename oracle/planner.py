@@ -30,7 +30,8 @@ Three outputs, all integer, all unique under the canonical orderings below.
    tile path.  A window takes the tile path when the tile path is enabled and
    it has no repeated pair, 1 <= T_w <= max_tiles, no heavy row, and
    1000 * nnz >= density_milli * 128 * T_w.  ``tile_windows`` lists them in
-   ascending order.
+   ascending order, ``core_windows`` the other windows (whose rows the
+   CUDA-core kernel takes), also ascending.
 """
 from __future__ import annotations
 
@@ -154,7 +155,8 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
             & (1000 * nnz >= int(density_milli) * 128 * nt)
         flags = flags | np.where(ok, FLAG_TILE, 0).astype(np.uint8)
     tile_windows = np.flatnonzero(flags & FLAG_TILE).astype(np.int32)
-    return dict(win_flags=flags, tile_windows=tile_windows)
+    core_windows = np.flatnonzero((flags & FLAG_TILE) == 0).astype(np.int32)
+    return dict(win_flags=flags, tile_windows=tile_windows, core_windows=core_windows)
 
 
 def full_plan(row_ptr, col_idx, num_nodes, bounds=(32, 256, 2048), heavy_threshold=512,

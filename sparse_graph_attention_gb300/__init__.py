@@ -39,6 +39,7 @@ ARRAYS = {  # name -> (enum, numpy dtype, trailing shape)
     "win_nnz": (8, np.int32, ()),
     "win_flags": (9, np.uint8, ()),
     "tile_windows": (10, np.int32, ()),
+    "core_windows": (11, np.int32, ()),
 }
 
 

@@ -384,6 +384,7 @@ g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_d
         case G3S_ARR_WIN_NNZ: src = p->arr.win_nnz; n = 4 * (size_t)s.W; break;
         case G3S_ARR_WIN_FLAGS: src = p->arr.win_flags; n = (size_t)s.W; break;
         case G3S_ARR_TILE_WINDOWS: src = p->arr.tile_windows; n = 4 * (size_t)c.n_tile_windows; break;
+        case G3S_ARR_CORE_WINDOWS: src = p->arr.core_windows; n = 4 * (size_t)(s.W - c.n_tile_windows); break;
         default: return fail(G3S_ERR_INVALID_ARG, "unknown plan array %d", (int)which);
     }
     if (bytes_needed) *bytes_needed = n;

@@ -38,15 +38,12 @@ def test_full_workload_all_rows(name):
     run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant)
 
 
-def test_full_lognormal_sampled_rows():
-    """The large HBM-bound workload at full size (~100M edges), checked on
-    sampled rows: random ones, the heaviest ones (split into chunks), both ends."""
+def test_full_lognormal_all_rows():
+    """The large HBM-bound workload at full size (2M rows, ~100M edges), in
+    the launch configuration the benchmark times, checked on every row
+    against the oracle (heavy rows split into chunks included)."""
     g, vals, w = graphgen.make_workload("lognormal_local", "full")
-    deg = g.degrees()
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([rng.choice(g.num_nodes, 3000, replace=False), np.argsort(deg)[-40:],
-                                     np.flatnonzero((deg > 500) & (deg < 530))[:20], [0, g.num_nodes - 1]]))
-    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, rows=rows)
+    plan, _, errs = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant)
     assert plan.stats()["chunks"] > 0
 
 

@@ -167,3 +167,58 @@ def test_tile_mixed_full_size_persistent_core_rows(H):
     st = plan.stats()
     core_rows = 16 * (st["windows"] - st["tile_windows"])
     assert 0 < st["tile_windows"] < st["windows"] and core_rows > 152 * 8 * 3
+
+
+# ---------------------------------------------------------------------------
+# the device planner's tile-path selection, bit-exact with the tile path on
+# ---------------------------------------------------------------------------
+def _mixed_graph():
+    a = graphgen.batched_dense(num_graphs=30, seed=11)
+    b = graphgen.powerlaw(num_nodes=2003, max_degree=1500, seed=12)
+    rp = np.concatenate([a.row_ptr, a.row_ptr[-1] + b.row_ptr[1:]]).astype(np.int32)
+    col = np.concatenate([a.col_idx, b.col_idx + a.num_nodes]).astype(np.int32)
+    return graphgen.Graph(rp, col)
+
+
+def _selection_cases():
+    dense_full = lambda: graphgen.make_workload("batched_dense", "full")[0]  # noqa: E731
+    complete_small = lambda: graphgen.make_workload("batched_complete", "small")[0]  # noqa: E731
+    yield "batched_dense_full_default", dense_full, 8, {}
+    yield "batched_dense_full_150", dense_full, 8, dict(tile_density_milli=150)
+    yield "batched_dense_full_150_global_bitmap", dense_full, 8, dict(tile_density_milli=150, bsb_smem_edges=64)
+    yield "batched_complete_small", complete_small, 8, {}
+    yield "batched_complete_small_global_bitmap", complete_small, 8, dict(bsb_smem_edges=100)
+    yield "mixed_heavy", _mixed_graph, 2, dict(tile_density_milli=150, heavy_threshold=60, chunk_edges=25)
+    yield "mixed_heavy_global_bitmap", _mixed_graph, 2, dict(tile_density_milli=150, heavy_threshold=60,
+                                                              chunk_edges=25, bsb_smem_edges=48)
+    yield "mixed_max_tiles", _mixed_graph, 2, dict(tile_density_milli=0, tile_max_tiles=5)
+
+
+@pytest.mark.parametrize("name,make,H,kw", list(_selection_cases()), ids=[c[0] for c in _selection_cases()])
+def test_tile_selection_bit_exact(name, make, H, kw):
+    """With the tile path on, the device planner's BSB arrays, window flags
+    (bit 1 = tile path), the tile-path window list and the list of windows
+    left to the CUDA-core kernel equal the reference planner's, through both
+    window-compaction kernels (shared-memory sort and global bitmap)."""
+    from oracle import planner as ref_planner
+    g = make()
+    rp, ci = upload_graph(g)
+    plan = g3s.Plan(rp, ci, g.num_nodes, H, 64, "bf16", tile_path=1, **kw)
+    st = plan.stats()
+    opts = g3s.make_options(tile_path=1, **kw)
+    b = ref_planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    sel = ref_planner.tile_selection(g.row_ptr, b, True, heavy_threshold=st["heavy_threshold"],
+                                     max_tiles=opts.tile_max_tiles, density_milli=opts.tile_density_milli)
+    ref = dict(b, **sel)
+    for arr in ("win_tile_ptr", "tile_cols", "tile_bits", "win_nnz", "win_flags", "tile_windows", "core_windows"):
+        got = plan.export(arr)
+        want = ref[arr]
+        assert got.shape == want.shape and np.array_equal(got, want.astype(got.dtype)), arr
+    assert st["tile_windows"] == sel["tile_windows"].size
+    assert st["tile_window_nnz"] == int(b["win_nnz"][sel["tile_windows"]].sum())
+    if "bsb_smem_edges" in kw:
+        assert st["large_windows"] > 0
+    if name != "batched_dense_full_default":
+        assert st["tile_windows"] > 0
+    if name.startswith("mixed"):
+        assert 0 < st["tile_windows"] < st["windows"]

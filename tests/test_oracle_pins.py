@@ -105,3 +105,19 @@ def test_round_to_ties_and_ranges():
     assert oracle.round_to(np.array([one + 2.0 ** -11]), "f16")[0] == 1.0          # tie -> even
     assert oracle.round_to(np.array([one + 3 * 2.0 ** -12]), "f16")[0] == one + 2.0 ** -10
     assert oracle.round_to(np.array([-2.5]), "bf16")[0] == -2.5
+
+
+def test_thread_count_does_not_change_results():
+    """Each row is summed in a fixed order by one thread, so one thread and
+    every thread give identical bits (the benchmark times both)."""
+    g = graphgen.powerlaw(num_nodes=3000, max_degree=1500, seed=91)
+    vals = graphgen.make_values(g.num_nodes, g.num_edges, 2, 32, True, seed=92)
+    t = {k: graphgen.to_dtype(v, "bf16") for k, v in vals.items()}
+    n_all = oracle.threads()
+    outs = []
+    for n in (1, n_all):
+        oracle.set_threads(n)
+        outs.append(oracle.forward(g.row_ptr, g.col_idx, g.num_nodes, 2, 32, "bf16", "rtmscore", t["Q"], t["K"],
+                                   t["V"], t["E"], want_eout=True))
+    oracle.set_threads(n_all)
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1], equal_nan=True)

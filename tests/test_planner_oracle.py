@@ -135,3 +135,7 @@ def test_tile_selection_brute_force():
         ok = (not b["win_dup"][w]) and 1 <= nt <= 6 and md <= 40 and b["win_nnz"][w] / (128.0 * nt) >= 0.2
         assert bool(sel["win_flags"][w] & planner.FLAG_TILE) == ok
     assert np.array_equal(sel["tile_windows"], np.flatnonzero(sel["win_flags"] & planner.FLAG_TILE))
+    # every window is on exactly one of the two lists, each ascending
+    tile, core = list(sel["tile_windows"]), list(sel["core_windows"])
+    assert sorted(tile + core) == list(range(W)) and tile == sorted(tile) and core == sorted(core)
+    assert 0 < len(tile) < W
