@@ -100,24 +100,36 @@ def kernel_sources_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per forward from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def recorded_profile(workload: str):
+    """ncu record of one forward on ``workload`` from profiles/traffic_<workload>.txt
+    (DRAM bytes per forward, the dominant kernel and its share of device
+    time), if it was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % workload)
     if not os.path.exists(path):
         return None
     kv = {}
     with open(path) as f:
         for line in f:
-            if ":" in line:
+            if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
     if kv.get("kernel_sources_sha256") != kernel_sources_hash():
         return None
     try:
-        return int(kv["dram_bytes_per_forward"])
+        rec = {"dram_bytes_per_forward": int(kv["dram_bytes_per_forward"])}
     except (KeyError, ValueError):
         return None
+    if "dominant_kernel" in kv:
+        rec["dominant_kernel"] = kv["dominant_kernel"]
+    if "dominant_share" in kv:
+        rec["dominant_share"] = float(kv["dominant_share"])
+    return rec
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per forward from the committed ncu record, if current (else None)."""
+    rec = recorded_profile(workload)
+    return None if rec is None else rec["dram_bytes_per_forward"]
 
 
 def byte_counts(g, w, out_dtype):
@@ -230,6 +242,148 @@ def oracle_rate(g, w, t, target_s: float, rows_start: int = 0):
     return edges / dt, dt, n_rows, edges, oracle.threads()
 
 
+def oracle_timings(g, w, t, seconds_each: float):
+    """The fp64 oracle as it stands, timed on one thread and on every core
+    of this host, each on a contiguous block of rows worth ~seconds_each
+    (the whole graph when it is faster)."""
+    import oracle
+
+    n_all = oracle.threads()
+    out = {}
+    for label, n in (("one_thread", 1), ("all_cores", n_all)):
+        oracle.set_threads(n)
+        rate, dt, rows, edges, _ = oracle_rate(g, w, t, seconds_each)
+        out[label] = {"edges_per_s": rate, "threads": n, "seconds": dt, "rows": rows, "edges": edges}
+    oracle.set_threads(n_all)
+    return out
+
+
+L2_FLUSH_BYTES = 256 << 20  # twice the L2 (126 MB): written between cold runs
+
+
+def median_ms(step, runs: int, stream, flush=None):
+    """Median over ``runs`` of one call's CUDA-event time on ``stream``; with
+    ``flush`` (a device buffer larger than L2) it is overwritten before each
+    run, outside the timed events, so every run starts with a cold L2."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    for a, b in ev:
+        if flush is not None:
+            flush.add_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def tile_mma_flops(plan, heads: int, head_dim: int) -> int:
+    """FLOPs the tile kernel issues on the tensor cores for one forward.  Per
+    tile-path window and head: S^T = K_cols Q_w^T as one 128 x 16 x head_dim
+    product, and O^T = V_cols^T P^T as a 128 x 16 product (the 64 feature
+    rows issued twice) over the window's columns rounded up to 16."""
+    tw = plan.export("tile_windows")
+    if tw.size == 0:
+        return 0
+    ptr = plan.export("win_tile_ptr").astype(np.int64)
+    cols = 8 * (ptr[tw + 1] - ptr[tw])
+    ksteps = (cols + 15) // 16
+    per_window = 2 * 128 * 16 * head_dim + 2 * 128 * 16 * 16 * ksteps
+    return int(per_window.sum() * heads)
+
+
+def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_paths: bool):
+    """One workload at full size through the default plan: warm and
+    cold-L2 medians, rates, byte and FLOP fractions, the ncu record when it
+    matches the sources, the oracle on one thread and on all cores; for
+    the batched family also the CUDA-core-only and tile-only plans."""
+    import torch
+
+    import sparse_graph_attention_gb300 as g3s
+    g, vals, w = graphgen.make_workload(name, "full")
+    t = {k: graphgen.to_dtype(v, w.dtype) for k, v in vals.items()}
+    rp = torch.from_numpy(g.row_ptr).to(dev)
+    ci = torch.from_numpy(g.col_idx).to(dev)
+    dQ, dK, dV = (t[k].to(dev) for k in "QKV")
+    dE = t["E"].to(dev) if w.variant == "rtmscore" else None
+    stream = torch.cuda.current_stream(dev)
+    hbm, hbm_src = measured_hbm_peak()
+    tf, tf_src = measured_bf16_peak(sustained=False)
+    flops = 4.0 * w.heads * w.head_dim * g.num_edges
+
+    def measure(plan):
+        odt = g3s.torch_dtype(plan.out_dtype)
+        O = torch.empty(dQ.shape, dtype=odt, device=dev)
+        Eout = torch.empty(dE.shape, dtype=odt, device=dev) if dE is not None else None
+
+        def step():
+            if dE is not None:
+                plan.forward(dQ, dK, dV, dE, O, Eout)
+            else:
+                plan.forward(dQ, dK, dV, None, O)
+
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize(dev)
+        warm = median_ms(step, runs, stream)
+        cold = median_ms(step, runs, stream, flush)
+        plan.check()
+        return warm, cold
+
+    plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant)
+    st = plan.stats()
+    warm, cold = measure(plan)
+    gathered, compulsory = byte_counts(g, w, plan.out_dtype)
+    sec = cold / 1e3
+    rec = {"num_nodes": g.num_nodes, "num_edges": g.num_edges, "heads": w.heads, "head_dim": w.head_dim,
+           "dtype": w.dtype, "variant": w.variant, "out_dtype": plan.out_dtype,
+           "ms_warm": warm, "ms_cold": cold,
+           "edges_per_s": g.num_edges / sec, "gflops": flops / sec / 1e9,
+           "compulsory_frac": compulsory / sec / 1e9 / hbm, "gathered_frac": gathered / sec / 1e9 / hbm,
+           "peak_gbs": hbm, "peak_source": hbm_src,
+           "timing": "median of %d single-forward CUDA-event times; cold: %d MB written between runs "
+                     "(outside the events) to evict L2; warm: back-to-back" % (runs, L2_FLUSH_BYTES >> 20),
+           "plan": {"tile_windows": st["tile_windows"], "windows": st["windows"], "chunks": st["chunks"],
+                    "pack_rows": st["pack_rows"], "heavy_threshold": st["heavy_threshold"]}}
+    prof = recorded_profile(name)
+    if prof is not None:
+        rec["dram_bytes"] = prof["dram_bytes_per_forward"]
+        rec["dram_frac_cold"] = prof["dram_bytes_per_forward"] / sec / 1e9 / hbm
+        if "dominant_kernel" in prof:
+            rec["dominant_kernel"] = prof["dominant_kernel"]
+            rec["dominant_share"] = prof.get("dominant_share")
+    if st["tile_windows"] > 0:
+        issued = tile_mma_flops(plan, w.heads, w.head_dim)
+        useful = 4.0 * w.heads * w.head_dim * st["tile_window_nnz"]
+        rec["tile"] = {"useful_flops": useful, "issued_flops": issued,
+                       "useful_frac_of_forward": useful / sec / 1e12 / tf,
+                       "peak_tflops": tf, "peak_source": tf_src + " (fp16 dense rate equals bf16's)"}
+    if with_paths:
+        paths = {}
+        for label, kw in (("core_only", dict(tile_path=0)), ("tile_only", dict(tile_path=1, tile_density_milli=0))):
+            p2 = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **kw)
+            s2 = p2.stats()
+            w2, c2 = measure(p2)
+            entry = {"ms_warm": w2, "ms_cold": c2, "tile_windows": s2["tile_windows"], "windows": s2["windows"]}
+            if s2["tile_windows"] > 0:
+                useful = 4.0 * w.heads * w.head_dim * s2["tile_window_nnz"]
+                issued = tile_mma_flops(p2, w.heads, w.head_dim)
+                entry["tile_useful_tflops"] = useful / (c2 / 1e3) / 1e12
+                entry["tile_useful_frac"] = entry["tile_useful_tflops"] / tf
+                entry["tile_issued_frac"] = issued / (c2 / 1e3) / 1e12 / tf
+                entry["tile_window_nnz"] = s2["tile_window_nnz"]
+            paths[label] = entry
+            p2.close()
+        rec["paths"] = paths
+    if oracle_seconds > 0:
+        rec["oracle"] = oracle_timings(g, w, t, oracle_seconds)
+    plan.close()
+    del dQ, dK, dV, dE, rp, ci
+    torch.cuda.empty_cache()
+    return rec
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -262,6 +416,11 @@ def parse_args():
     ap.add_argument("--e2e-streams", type=int, default=3,
                     help="plans (each with its own staging) taking e2e steps in turn, one stream each")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the 'workloads' record (the other benchmark graphs, timed warm and cold)")
+    ap.add_argument("--workload-runs", type=int, default=20, help="timed runs per workload (median)")
+    ap.add_argument("--workload-oracle-seconds", type=float, default=1.5,
+                    help="oracle work per workload and thread count")
     return ap.parse_args()
 
 
@@ -508,27 +667,33 @@ def main():
     value = whole_job_rate(g.num_edges, args.steps, world, total_ms)
 
     # ---- roofline of the forward (fused kernel + heavy-row merge) --------
+    # frac: DRAM bytes one forward moves (ncu, recorded on these kernel
+    # sources) / the live mean launch time / the measured copy peak.  The
+    # gathered-bytes model (every K, V row read once per edge) exceeds the
+    # DRAM bytes where sources repeat in L2, so its fraction is kept beside
+    # it as gathered_frac, with the compulsory lower bound (every array once).
     gathered, compulsory = byte_counts(g, w, plan.out_dtype)
     fwd_s = statistics.mean(per_launch_ms) / 1000.0
     peak, peak_src = measured_hbm_peak()
-    achieved = gathered / fwd_s / 1e9
-    traffic = recorded_traffic(w.name)
+    prof = recorded_profile(w.name)
+    traffic = None if prof is None else prof["dram_bytes_per_forward"]
+    basis = traffic if traffic is not None else compulsory
+    achieved = basis / fwd_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "peak_source": peak_src,
+                "basis": ("ncu DRAM bytes per forward (dram__bytes_read.sum + dram__bytes_write.sum, "
+                          "profiles/traffic_%s.txt, same kernel sources) / live mean forward time" % w.name)
+                if traffic is not None else
+                "compulsory bytes (no ncu DRAM record for the current kernel sources): a lower bound",
                 "kernel": "g3s_forward (fused CUDA-core kernel + heavy-row merge)",
-                "bytes_model": "gathered: CSR + Q + K,V per edge (+E, Eout) + O; L2 reuse of local sources lets "
-                               "frac exceed 1",
+                "gathered_gbs": gathered / fwd_s / 1e9, "gathered_frac": gathered / fwd_s / 1e9 / peak,
+                "bytes_model": "gathered: CSR + Q + K,V per edge (+E, Eout) + O (L2 hits of local sources let "
+                               "it exceed 1); compulsory: every array once",
                 "compulsory_gbs": compulsory / fwd_s / 1e9,
                 "compulsory_frac": compulsory / fwd_s / 1e9 / peak}
-    if traffic is not None:
-        roofline["dram_gbs"] = traffic / fwd_s / 1e9
-        roofline["dram_frac"] = traffic / fwd_s / 1e9 / peak
-    if st["tile_windows"] > 0:
-        # tile path: useful tile FLOPs (4 * 128 entries per 16x8 tile * d, per head) and the
-        # MMA FLOPs the kernel issues (two 128x64x64 products per 64-column chunk and head)
-        tiles = st["tiles_on_tile_path"] if "tiles_on_tile_path" in st else None
-        roofline["tile_windows"] = st["tile_windows"]
-        roofline["tile_window_nnz"] = st["tile_window_nnz"]
+    if prof is not None and "dominant_kernel" in prof:
+        roofline["dominant_kernel"] = prof["dominant_kernel"]
+        roofline["dominant_share"] = prof.get("dominant_share")
 
     # ---- optional: a whole layer (projection on the tensor cores + forward) ----
     layer = None
@@ -602,6 +767,23 @@ def main():
         rate, dt, n_rows, edges, threads = oracle_rate(g, w, t, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "rows 0..%d (%d edges, %.1f s) of the same workload, fp64 oracle" % (n_rows - 1, edges, dt)}
+        import oracle
+        oracle.set_threads(1)
+        r1, dt1, n1, e1, _ = oracle_rate(g, w, t, args.cpu_seconds / 4)
+        oracle.set_threads(threads)
+        cpu["one_thread"] = {"value": r1, "cores": 1,
+                             "sample": "rows 0..%d (%d edges, %.1f s)" % (n1 - 1, e1, dt1)}
+
+    # ---- the other workloads (rank 0): each at full size, warm and cold L2 ----
+    workloads = None
+    if rank == 0 and not args.no_workloads:
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        workloads = {}
+        for name in ("tiny_poisson", "rtmscore_batch64", "batched_dense", "powerlaw", "batched_complete"):
+            workloads[name] = time_workload(name, dev, args.workload_runs,
+                                            0.0 if args.no_cpu_baseline else args.workload_oracle_seconds, flush,
+                                            with_paths=name.startswith("batched"))
+        del flush
 
     if rank == 0:
         line = {
@@ -617,7 +799,7 @@ def main():
             "gflops": 4.0 * w.heads * w.head_dim * g.num_edges / (ms_per_step / 1000.0) / 1e9,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
-            "aggregate": aggregate,
+            "aggregate": aggregate, "workloads": workloads,
             "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
                      "heavy_threshold": st["heavy_threshold"], "pack_rows": st["pack_rows"],
                      "tile_windows": st["tile_windows"],

@@ -96,7 +96,8 @@ typedef enum g3s_variant {
  *                  they cross near edge probability 0.55, and on complete
  *                  graphs the tile path is about 1.6 times as fast)
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
- *                  maximum with the tile path on: 32)
+ *                  maximum with the tile path on: 16, i.e. 128 source columns,
+ *                  the M side of the kernel's tcgen05 product)
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
  *                  the global-bitmap planner kernel instead of the shared-
  *                  memory sort (default 2048; a testing knob)
@@ -159,6 +160,7 @@ typedef struct g3s_plan_stats {
     int32_t chunk_edges;     /* CSR positions per heavy-row chunk */
     int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
+    int64_t tile_items;      /* work items of the tile kernel: one or two tile-path windows each */
 } g3s_plan_stats;
 
 /* Planner arrays readable with g3s_plan_export (all int32 unless noted). */
@@ -174,8 +176,14 @@ typedef enum g3s_plan_array {
     G3S_ARR_WIN_NNZ = 8,         /* [W] CSR entries per window */
     G3S_ARR_WIN_FLAGS = 9,       /* uint8 [W]: bit0 repeated edge, bit1 tile path */
     G3S_ARR_TILE_WINDOWS = 10,   /* [tile_windows] ascending */
-    G3S_ARR_CORE_WINDOWS = 11    /* [windows - tile_windows] ascending: the windows whose rows the
+    G3S_ARR_CORE_WINDOWS = 11,   /* [windows - tile_windows] ascending: the windows whose rows the
                                     CUDA-core kernel takes (every window without bit 1) */
+    G3S_ARR_TILE_ITEMS = 12      /* [tile_items][8]: the tile kernel's items.  Tile-path list
+                                    entries 2k and 2k+1 share an item when ceil(T/2) of both
+                                    (16-column units of T tiles) sum to <= 8.  Per item
+                                    (w0, first tile of w0, T0, nwin | units0 << 8,
+                                     w1, first tile of w1, T1, 0), the second window zero
+                                    when nwin = 1 */
 } g3s_plan_array;
 
 typedef struct g3s_plan g3s_plan; /* opaque */

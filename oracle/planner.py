@@ -159,8 +159,38 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
     return dict(win_flags=flags, tile_windows=tile_windows, core_windows=core_windows)
 
 
+def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray) -> np.ndarray:
+    """Work items of the tile kernel, (n_items, 8) int32.  Entries 2k and
+    2k+1 of the tile-path list share an item when ceil(T/2) of each (T = the
+    window's tile count, so 16-column units) sum to at most 8; otherwise each
+    is an item of its own, as is a last unpaired entry.  Per item:
+    (w0, first tile of w0, T0, nwin | units0 << 8, w1, first tile of w1, T1, 0),
+    the second half zero when nwin = 1."""
+    ptr = b["win_tile_ptr"].astype(np.int64)
+    out = []
+
+    def entry(i):
+        w = int(tile_windows[i])
+        return w, int(ptr[w]), int(ptr[w + 1] - ptr[w])
+
+    n = len(tile_windows)
+    for i0 in range(0, n, 2):
+        w0, f0, t0 = entry(i0)
+        u0 = (t0 + 1) // 2
+        if i0 + 1 < n:
+            w1, f1, t1 = entry(i0 + 1)
+            if u0 + (t1 + 1) // 2 <= 8:
+                out.append([w0, f0, t0, 2 | (u0 << 8), w1, f1, t1, 0])
+            else:
+                out.append([w0, f0, t0, 1 | (u0 << 8), 0, 0, 0, 0])
+                out.append([w1, f1, t1, 1 | (((t1 + 1) // 2) << 8), 0, 0, 0, 0])
+        else:
+            out.append([w0, f0, t0, 1 | (u0 << 8), 0, 0, 0, 0])
+    return np.asarray(out, np.int32).reshape(-1, 8)
+
+
 def full_plan(row_ptr, col_idx, num_nodes, bounds=(32, 256, 2048), heavy_threshold=512,
-              chunk_edges=256, with_bsb=True, tile_enabled=False, max_tiles=32,
+              chunk_edges=256, with_bsb=True, tile_enabled=False, max_tiles=16,
               density_milli=150) -> dict:
     out = {}
     out.update(degree_buckets(row_ptr, bounds))

@@ -40,6 +40,7 @@ ARRAYS = {  # name -> (enum, numpy dtype, trailing shape)
     "win_flags": (9, np.uint8, ()),
     "tile_windows": (10, np.int32, ()),
     "core_windows": (11, np.int32, ()),
+    "tile_items": (12, np.int32, (8,)),
 }
 
 
@@ -83,6 +84,7 @@ class PlanStats(ctypes.Structure):
         ("pack_rows", ctypes.c_int32), ("pack_limit", ctypes.c_int32),
         ("heavy_threshold", ctypes.c_int32), ("chunk_edges", ctypes.c_int32), ("short_rows", ctypes.c_int64),
         ("workspace_used", ctypes.c_size_t),
+        ("tile_items", ctypes.c_int64),
     ]
 
 

@@ -65,7 +65,7 @@ void default_options(g3s_plan_options* o) {
     o->bsb = -1;
     o->tile_path = -1;
     o->tile_density_milli = 400;
-    o->tile_max_tiles = 32;
+    o->tile_max_tiles = 16;
     o->bsb_smem_edges = 2048;
     o->rtm_elementwise_clamp = 1;
     o->rtm_epsilon = 1e-6f;
@@ -170,6 +170,7 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->win_nnz = c.take<int32_t>(s.W);
         a->win_flags = c.take<uint8_t>(s.W);
         a->tile_windows = c.take<int32_t>(s.W);
+        a->tile_items = c.take<int4>(2 * s.W);
         a->core_windows = c.take<int32_t>(s.W);
         a->large_windows = c.take<int32_t>(s.W);
         a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
@@ -178,6 +179,7 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     } else {
         a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
         a->core_windows = nullptr;
+        a->tile_items = nullptr;
         a->win_flags = nullptr;
         a->tile_bits = a->bitmap_scratch = nullptr;
     }
@@ -361,6 +363,7 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->chunk_edges = p->shape.chunk_edges;
     st->short_rows = p->counts.n_short;
     st->workspace_used = p->ws_used;
+    st->tile_items = p->counts.n_tile_items;
     return G3S_OK;
 }
 
@@ -385,6 +388,11 @@ g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_d
         case G3S_ARR_WIN_FLAGS: src = p->arr.win_flags; n = (size_t)s.W; break;
         case G3S_ARR_TILE_WINDOWS: src = p->arr.tile_windows; n = 4 * (size_t)c.n_tile_windows; break;
         case G3S_ARR_CORE_WINDOWS: src = p->arr.core_windows; n = 4 * (size_t)(s.W - c.n_tile_windows); break;
+        case G3S_ARR_TILE_ITEMS:
+            if (!s.tile_enabled) return fail(G3S_ERR_UNSUPPORTED, "plan was built without the tile path");
+            src = p->arr.tile_items;
+            n = 32 * (size_t)c.n_tile_items;
+            break;
         default: return fail(G3S_ERR_INVALID_ARG, "unknown plan array %d", (int)which);
     }
     if (bytes_needed) *bytes_needed = n;
@@ -458,9 +466,8 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.O = O;
         tp.N = s.N;
         tp.H = s.H;
-        tp.tile_windows = p->arr.tile_windows;
-        tp.n_tile_windows = p->counts.n_tile_windows;
-        tp.win_tile_ptr = p->arr.win_tile_ptr;
+        tp.tile_items = p->arr.tile_items;
+        tp.n_tile_items = p->counts.n_tile_items;
         tp.tile_cols = p->arr.tile_cols;
         tp.tile_bits = p->arr.tile_bits;
         tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;

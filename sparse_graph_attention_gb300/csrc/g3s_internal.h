@@ -25,7 +25,14 @@ enum : int32_t {
     kErrEdgeId = 32,      // an edge id outside [0, edge slots)
 };
 
-constexpr int kTileMaxTilesPerWindow = 32;  // tile-path windows have at most this many 16x8 tiles
+constexpr int kTileMaxTilesPerWindow = 16;  // tile-path windows have at most this many 16x8 tiles (128 columns)
+// A tile-kernel item holds one or two consecutive tile-path windows (in list
+// order), each starting at a 16-column boundary of the item, together at most
+// 128 columns: a window of T tiles takes ceil(T/2) units of 16 columns, and a
+// pair is formed from list entries (2k, 2k+1) when their units sum to <= 8.
+// Stored as two int4: (w0, first tile of w0, T0, nwin | units0 << 8) and
+// (w1, first tile of w1, T1, 0).
+constexpr int kTileItemUnits = 8;
 
 // Small device-resident counters filled by the planner and read back once.
 struct PlanCounts {
@@ -39,6 +46,7 @@ struct PlanCounts {
     int32_t n_large_windows;
     int32_t n_short;  // rows with at most PlanShape::pack_limit entries
     long long tile_window_nnz;
+    int32_t n_tile_items;  // work items of the tile kernel (one or two tile-path windows each)
 };
 
 // Device views the planner writes into (all inside the caller's workspace).
@@ -58,6 +66,7 @@ struct PlanArrays {
     int32_t* win_nnz;          // [W]
     uint8_t* win_flags;        // [W]
     int32_t* tile_windows;     // [W]
+    int4* tile_items;          // [2W] tile kernel items: two int4 per item (see kTileItem* below)
     int32_t* core_windows;     // [W] the other windows, ascending (rows left to the CUDA-core kernel)
     int32_t* large_windows;    // [W]
     int32_t* tile_cols;        // [max_tiles][8]
@@ -207,9 +216,8 @@ struct TileParams {
     void* O;
     long long N;
     int H;
-    const int32_t* tile_windows;
-    long long n_tile_windows;
-    const int32_t* win_tile_ptr;
+    const int4* tile_items;  // two int4 per item (kTileItemUnits above)
+    long long n_tile_items;
     const int32_t* tile_cols;
     const uint32_t* tile_bits;
     float scale_log2;  // log2(e)/sqrt(d)

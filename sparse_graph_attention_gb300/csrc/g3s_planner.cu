@@ -568,6 +568,49 @@ __global__ void k_tile_select(const int32_t* row_ptr, long long N, long long W, 
     if (ndup) atomicAdd(&c->n_dup_windows, ndup);
 }
 
+// Tile-kernel items: list entries (2k, 2k+1) share an item when their
+// 16-column units (ceil(T/2) each) sum to at most kTileItemUnits.
+struct TilePair {
+    const int32_t* tile_windows;
+    const int32_t* win_tile_ptr;
+    const PlanCounts* c;
+    __device__ int ntiles(long long i) const {
+        const int w = tile_windows[i];
+        return win_tile_ptr[w + 1] - win_tile_ptr[w];
+    }
+    __device__ int operator()(long long pair) const {
+        const long long n = c->n_tile_windows, i0 = 2 * pair;
+        if (i0 >= n) return 0;
+        if (i0 + 1 >= n) return 1;
+        return (ntiles(i0) + 1) / 2 + (ntiles(i0 + 1) + 1) / 2 <= kTileItemUnits ? 1 : 2;
+    }
+};
+struct TilePairOut {
+    TilePair pr;
+    int4* items;
+    __device__ int4 single(long long i, int nwin, int units0) const {
+        const int w = pr.tile_windows[i];
+        const int t0 = pr.win_tile_ptr[w];
+        return make_int4(w, t0, pr.win_tile_ptr[w + 1] - t0, nwin | (units0 << 8));
+    }
+    __device__ void operator()(long long pair, int p, int v) const {
+        const long long i0 = 2 * pair;
+        if (v == 1) {
+            const bool two = i0 + 1 < pr.c->n_tile_windows;
+            const int units0 = (pr.ntiles(i0) + 1) / 2;
+            items[2 * p] = single(i0, two ? 2 : 1, units0);
+            int4 b = two ? single(i0 + 1, 0, 0) : make_int4(0, 0, 0, 0);
+            b.w = 0;
+            items[2 * p + 1] = b;
+        } else if (v == 2) {
+            items[2 * p] = single(i0, 1, (pr.ntiles(i0) + 1) / 2);
+            items[2 * p + 1] = make_int4(0, 0, 0, 0);
+            items[2 * p + 2] = single(i0 + 1, 1, (pr.ntiles(i0 + 1) + 1) / 2);
+            items[2 * p + 3] = make_int4(0, 0, 0, 0);
+        }
+    }
+};
+
 struct TileFlag {
     const uint8_t* win_flags;
     __device__ int operator()(long long w) const { return (win_flags[w] & kFlagTile) ? 1 : 0; }
@@ -685,6 +728,10 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
         G3S_TRY(cudaGetLastError());
     }
     G3S_TRY(scan(TileFlag{a.win_flags}, ListOut{a.tile_windows}, W, a.scan_blocks, &c->n_tile_windows, st));
+    if (s.tile_enabled) {
+        const TilePair pr{a.tile_windows, a.win_tile_ptr, c};
+        G3S_TRY(scan(pr, TilePairOut{pr, a.tile_items}, (W + 1) / 2, a.scan_blocks, &c->n_tile_items, st));
+    }
     G3S_TRY(scan(CoreWindowFlag{a.win_flags}, ListOut{a.core_windows}, W, a.scan_blocks, nullptr, st));
     return cudaSuccess;
 }

@@ -42,6 +42,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about hint_ns nanoseconds pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_wait_bounded, sleeping in the hardware between checks (about 20 us
+// at most per check), so a waiting warp issues almost nothing.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u))
+        if (globaltimer() - t0 > limit_ns) return false;
+    return true;
+}
+
 // Wait for the phase with the given parity to complete, giving up after
 // limit_ns nanoseconds of the global timer (returns false then).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -77,6 +99,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// this thread's cp.async groups except the newest N have completed
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ---- TMA tiles and bulk groups -------------------------------------------------
 // 2-D tile load of the box at element coordinates (x, y) into dst, counted on bar.
@@ -182,12 +209,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor with the 32-byte swizzle (mode 6 in bits
+// 61-63): for an MN-major operand of 16 elements (32 bytes) along MN, 8 K rows
+// per 256-byte atom (the 16-byte half of a row at address bit 4 is XOR-ed with
+// address bit 7); stride byte offset = the distance between 8-row K groups.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
-// B fp16 (0) or bf16 (1) in bits 7-9 and 10-12, A K-major (bit 15 = 0), B
-// K-major (bit 16 = 0) or MN-major (1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// B fp16 (0) or bf16 (1) in bits 7-9 and 10-12, A K-major (bit 15 = 0) or
+// MN-major (1), B K-major (bit 16 = 0) or MN-major (1), N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N, bool a_mn_major = false) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace ptx

@@ -4,35 +4,52 @@
 // Source: the Fused3S design (sciencestack.ai/paper/2505.08098): a 16-row
 // window is compacted to its unique source columns and tiled into 16x8 tiles
 // with bitmaps (Figure 1); one thread block owns a window's Q and O rows
-// (node-parallel, Figure 2); SDDMM, softmax and SpMM stay on chip with an
-// online softmax (TL;DR).  Its warp-level MMA layout is not reused: on sm_103a
-// one thread issues tcgen05.mma for the whole CTA and the accumulators live
-// in tensor memory.
+// (node-parallel, Figure 2); SDDMM, softmax and SpMM stay on chip (TL;DR).
+// Its warp-level MMA layout is not reused: on sm_103a one thread issues
+// tcgen05.mma for the whole CTA, an MMA has 64 or 128 rows (M), and the
+// accumulators live in tensor memory.
 //
-// Mapping.  A CTA (4 warps, 128 threads) takes one group of up to 8 tile
-// windows and one head.  The 8 x 16 window rows stack into the 128 rows of
-// the MMA; the group's tiles are concatenated (window by window) and walked
-// 64 columns (8 tiles) at a time:
-//   1. cp.async gathers the K and V rows of the 64 columns (head h, d = 64)
-//      into 128-byte-swizzled shared memory (Q rows once per CTA); the
-//      gathers of the next chunk (two buffers) and the column ids and bitmaps
-//      of the chunk after it (three buffers) are in flight while this chunk
-//      is computed;
-//   2. S = Q K^T (M=128, N=64, K=64) into TMEM columns [0, 64);
-//   3. thread i reads row i of S, masks entries outside its own window's
-//      tiles or absent from the bitmap, updates its running max / sum and
-//      writes P = 2^(s - m) in the input type to shared memory;
-//   4. O += P V (M=128, N=64, K=64; V read as an MN-major operand) accumulates
-//      in TMEM columns [64, 128); it is issued together with the next chunk's
-//      S = Q K^T under one commit, so each chunk costs one MMA round trip.
-//      When a row's reference max moves (rarely: only by more than 2^8), the
-//      thread rescales its row of O in TMEM before the next accumulation.
-// Rows are read back from TMEM, normalised and stored at the end.  Every wait on an mbarrier is
-// bounded (about one second of %globaltimer); on expiry the CTA sets the
-// plan's status word, frees its TMEM and returns.
+// Mapping (the transposed products).  A window has 16 rows but up to 128
+// source columns, so the columns go on the MMA's M side and the rows on N.
+// A work item is one head of one or two consecutive tile-path windows whose
+// columns, each window starting at a 16-column boundary, fill at most the
+// 128 rows of M (the planner's items):
+//   S^T = K_cols Q_w^T   M = 128 item columns, N = 16 rows per window, K = d
+//   O^T = V_cols^T P^T   per window: M = d (64, issued as 128: see below),
+//                        N = its 16 rows, K = its columns, 16 at a time
+// so every column of the item serves its own window's rows in one MMA round
+// trip, and the second product runs only over each window's own columns.
+//
+// Per item: cp.async gathers the head's 128-byte K and V rows of the item's
+// columns and its windows' Q rows into 128-byte-swizzled shared memory; one
+// thread issues S^T into TMEM; each thread reads its column of S^T (the 16
+// logits of its window's rows) and masks it by the tile bitmap.  The row
+// maxima need all of a window's columns: the scaled logits go through a
+// transposed buffer where eight threads per row take the max and the row
+// sum of P = 2^(s - m) rounded to the input type.  A window has at most 128
+// columns, so the max is final before any P is formed and the softmax needs
+// no online rescale.  Each column's thread then forms its own 16 values of P
+// (the same rounded values the row sums were taken over) and writes them as
+// one 32-byte row of P^T, the MN-major B operand of the second product.  O^T
+// uses the V rows as its MN-major A operand; its 64 feature rows are issued
+// as M = 128 with the second half reading the same rows again (atom stride
+// 0), so TMEM lanes 64-127 repeat lanes 0-63 and all four warps store rows.
+//
+// Pipeline (persistent CTAs, three per SM, static item order): K, Q and the
+// bitmaps are double-buffered and V single-buffered; S^T is double-buffered
+// in TMEM.  Item i+1's S^T is issued as soon as item i's logits are out of
+// TMEM, and item i+2's K, Q and bitmaps are requested once item i's row maxima
+// are done (the transposed logits live in item i's K buffer), so both have a
+// whole item's time to complete; item i's V rows are requested once O^T of
+// item i-1 is done, and arrive while item i-1's rows are stored and item i
+// goes through its softmax.  Item descriptors and column ids are loaded three
+// and two items ahead.  Every mbarrier wait is bounded (about one second of
+// %globaltimer); on expiry the CTA sets the plan's status word, frees its TMEM
+// and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstddef>
 #include <type_traits>
 
 #include "g3s_internal.h"
@@ -42,30 +59,31 @@ namespace g3s {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kD = 64;               // head_dim of this kernel
-constexpr int kNC = 64;              // columns per chunk (8 tiles)
-constexpr int kGroupWindows = 8;     // windows per CTA: 8 x 16 rows = 128 MMA rows
-constexpr int kMaxGroupTiles = kGroupWindows * kTileMaxTilesPerWindow;
-constexpr uint32_t kTmemCols = 128;  // S chunk [0, 64) + O chunk [64, 128)
-constexpr float kNegBig = -1e30f;
-constexpr float kRescaleSlack = 8.0f;
+constexpr int kD = 64;                         // head_dim of this kernel
+constexpr int kRows = kWinRows;                // 16 rows per window: the N of a window
+constexpr int kCols = kTileItemUnits * 16;     // 128 item columns: the MMA's M
+constexpr int kTiles = kCols / kTileCols;      // 16 tile slots per item
+constexpr int kMaxWin = 2;                     // windows per item
+constexpr int kItemRows = kMaxWin * kRows;     // 32
+constexpr int kXtPitch = 20;                   // words per column of the transposed logits (16 used)
+constexpr uint32_t kTmemCols = 128;            // S^T by item parity [0, 32) and [32, 64), O^T [64, 96)
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 struct TileSmem {
-    uint8_t q[128 * 128];     // Q rows, 128B-swizzled, K-major A operand
-    uint8_t k[2][kNC * 128];  // K rows of a chunk (K-major B operand of S), two stages
-    uint8_t v[2][kNC * 128];  // V rows of a chunk (MN-major B operand of O), two stages
-    uint8_t p[128 * 128];     // P rows (K-major A operand of O)
-    int cols[3][kNC];         // column ids of a chunk, three stages
-    uint32_t bits[3][8][4];   // bitmaps of a chunk's 8 tiles, three stages
-    int tile_g[kMaxGroupTiles];     // global tile index of each group tile
-    int8_t tile_j[kMaxGroupTiles];  // window slot of each group tile
-    int win[kGroupWindows];
-    int win_t0[kGroupWindows], win_t1[kGroupWindows];  // group-tile range of each window
-    unsigned long long mbar;
+    uint8_t k[2][kCols * 128];         // K rows by stage: K-major A operand of S^T; then the transposed logits
+    uint8_t v[kCols * 128];            // V rows: MN-major A operand of O^T (M rows 0-63)
+    uint8_t q[2][kItemRows * 128];     // Q rows by stage (row 16 j + r of window j): K-major B operand of S^T
+    uint8_t pt[kCols * 32];            // P^T: [column][16 rows of its window], MN-major B operand, 32-byte swizzle
+    float rowmax[kItemRows];           // row maxima of the item's windows (row 16 j + r)
+    float inv_l[kItemRows];            // 1 / row sum of P (0 for a row without entries)
+    uint32_t bits[2][kTiles][4];       // tile bitmaps by stage and item tile slot
+    int cols[3][kCols];                // source ids of the item columns, item i in slot i % 3 (-1: none)
+    unsigned long long bar_s, bar_o;
     uint32_t tmem_base;
-    int nw, tt;
 };
+static_assert(sizeof(TileSmem) + 1024 <= 75 * 1024, "three CTAs per SM");
+static_assert(kCols * kXtPitch * 4 <= kCols * 128, "transposed logits fit a K stage");
+static_assert(offsetof(TileSmem, pt) % 1024 == 0, "operand alignment");
 
 using namespace ptx;
 
@@ -75,66 +93,50 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// two floats rounded to the input type, packed (first in the low half); and
+// one float rounded to it, back as a float
 template <typename T>
-struct Pack2;
+struct Half2;
 template <>
-struct Pack2<__nv_bfloat16> {
-    // round two floats to bf16, return the packed pair and the rounded values
-    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        float2 f = __bfloat1622float2(h);
-        ra = f.x;
-        rb = f.y;
+struct Half2<__nv_bfloat16> {
+    __device__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&h);
     }
+    __device__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 };
 template <>
-struct Pack2<__half> {
-    __device__ static uint32_t pack(float a, float b, float& ra, float& rb) {
-        __half2 h = __floats2half2_rn(a, b);
-        float2 f = __half22float2(h);
-        ra = f.x;
-        rb = f.y;
+struct Half2<__half> {
+    __device__ static uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&h);
     }
+    __device__ static float round(float x) { return __half2float(__float2half_rn(x)); }
 };
 
 template <typename OutT>
-__device__ __forceinline__ void store_row(void* O, long long off, const float (&o)[kD], float inv);
+__device__ __forceinline__ void store_out(void* O, long long idx, float v);
 template <>
-__device__ __forceinline__ void store_row<float>(void* O, long long off, const float (&o)[kD], float inv) {
-    float4* d = reinterpret_cast<float4*>(static_cast<float*>(O) + off);
-#pragma unroll
-    for (int i = 0; i < kD / 4; ++i) d[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+__device__ __forceinline__ void store_out<float>(void* O, long long idx, float v) {
+    __stcs(static_cast<float*>(O) + idx, v);
 }
 template <>
-__device__ __forceinline__ void store_row<__nv_bfloat16>(void* O, long long off, const float (&o)[kD], float inv) {
-    uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(O) + off);
-#pragma unroll
-    for (int i = 0; i < kD / 8; ++i) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(o[8 * i + 2 * k] * inv, o[8 * i + 2 * k + 1] * inv);
-            w[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        d[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+__device__ __forceinline__ void store_out<__nv_bfloat16>(void* O, long long idx, float v) {
+    static_cast<__nv_bfloat16*>(O)[idx] = __float2bfloat16_rn(v);
 }
 template <>
-__device__ __forceinline__ void store_row<__half>(void* O, long long off, const float (&o)[kD], float inv) {
-    uint4* d = reinterpret_cast<uint4*>(static_cast<__half*>(O) + off);
-#pragma unroll
-    for (int i = 0; i < kD / 8; ++i) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            __half2 h = __floats2half2_rn(o[8 * i + 2 * k] * inv, o[8 * i + 2 * k + 1] * inv);
-            w[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        d[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+__device__ __forceinline__ void store_out<__half>(void* O, long long idx, float v) {
+    static_cast<__half*>(O)[idx] = __float2half_rn(v);
 }
+
+// An item: its windows (w, first tile, tiles), the 16-column units of window
+// 0 (window 1 starts there) and the head.
+struct Item {
+    int4 a, b;  // (w0, t0, T0, nwin | units0 << 8), (w1, t1, T1, 0)
+    int h;
+    __device__ int nwin() const { return a.w & 0xff; }
+    __device__ int units0() const { return a.w >> 8; }
+};
 
 // ---------------------------------------------------------------------------
 template <typename T, typename OutT>
@@ -142,269 +144,341 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int group = blockIdx.x, h = blockIdx.y;
     const T* Q = static_cast<const T*>(p.Q);
     const T* K = static_cast<const T*>(p.K);
     const T* V = static_cast<const T*>(p.V);
-    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
-    constexpr uint32_t kIdescS = idesc_f16(kBf16, false, 128, kNC);
-    constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kD);
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kRows, true);  // A and B MN-major
+    const long long n_work = p.n_tile_items * p.H;
+    const long long G = gridDim.x;
+    const long long first = blockIdx.x;
+    const int n_my = first < n_work ? (int)((n_work - 1 - first) / G + 1) : 0;
 
-    // ---- set-up: TMEM, mbarrier, the group's windows and tiles ---------------
     if (warp == 0) tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     if (tid == 0) {
-        mbar_init(smem_u32(&sm.mbar), 1);
+        mbar_init(smem_u32(&sm.bar_s), 1);
+        mbar_init(smem_u32(&sm.bar_o), 1);
         fence_mbar_init();
-    }
-    // windows of the group and their tile ranges, read in parallel by the first warp
-    if (warp == 0) {
-        const int lane = tid;
-        int w = -1, t0 = 0, cnt = 0;
-        if (lane < kGroupWindows) {
-            const long long idx = (long long)group * kGroupWindows + lane;
-            if (idx < p.n_tile_windows) {
-                w = p.tile_windows[idx];
-                t0 = p.win_tile_ptr[w];
-                cnt = min(p.win_tile_ptr[w + 1] - t0, kTileMaxTilesPerWindow);
-            }
-            sm.win[lane] = w;
-        }
-        int start = cnt;  // exclusive prefix of the tile counts over the 8 windows
-#pragma unroll
-        for (int o = 1; o < kGroupWindows; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, start, o);
-            if (lane >= o) start += y;
-        }
-        start -= cnt;
-        if (lane < kGroupWindows) {
-            for (int k = 0; k < cnt; ++k) {
-                sm.tile_g[start + k] = t0 + k;
-                sm.tile_j[start + k] = (int8_t)lane;
-            }
-            sm.win_t0[lane] = start;
-            sm.win_t1[lane] = start + cnt;
-        }
-        const int nw = __popc(__ballot_sync(0xffffffffu, w >= 0));
-        const int tt = __shfl_sync(0xffffffffu, start + cnt, kGroupWindows - 1);
-        if (lane == 0) {
-            sm.nw = nw;
-            sm.tt = tt;
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t tmem_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
-    const int tt = sm.tt;
-    const int nchunks = (tt + 7) / 8;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
 
-    // chunk `ch`'s column ids and bitmaps into meta stage `ms` (24 copies of 16 B)
-    auto issue_meta = [&](int ch, int ms) {
-        if (tid < 24) {
-            const int slot = tid / 3, part = tid - 3 * slot;
-            const int t = ch * 8 + slot;
-            const bool valid = t < tt;
-            const long long g = valid ? sm.tile_g[t] : 0;
-            if (part < 2)
-                cp_async16(smem_u32(&sm.cols[ms][slot * 8 + part * 4]), p.tile_cols + g * kTileCols + part * 4,
-                           valid ? 16u : 0u);
-            else
-                cp_async16(smem_u32(&sm.bits[ms][slot][0]), p.tile_bits + g * 4, valid ? 16u : 0u);
+    // Wait for an MMA commit: thread 0 polls the mbarrier (bounded), the
+    // other threads block in the CTA barrier, which issues nothing, instead of
+    // spinning beside the other CTAs of the SM.  False when the wait gave up.
+    auto cta_wait = [&](uint32_t bar, uint32_t parity) {
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait_bounded_sleep(bar, parity, kWaitLimitNs);
+        return __syncthreads_or(!ok) == 0;
+    };
+    // item j of this CTA (a zero item past the end)
+    // (work index first + j G = k H + h: k and h advanced by G per item, no division)
+    const int gk = (int)(G / p.H), gh = (int)(G - (long long)gk * p.H);
+    int next_k = (int)(first / p.H), next_h = (int)(first - (long long)next_k * p.H);
+    auto fetch_item = [&](int j) {  // called with j = 0, 1, 2, ... in order
+        Item it;
+        it.a = it.b = make_int4(0, 0, 0, 0);
+        it.h = 0;
+        if (j < n_my) {
+            it.h = next_h;
+            it.a = p.tile_items[2 * next_k];
+            it.b = p.tile_items[2 * next_k + 1];
+        }
+        next_k += gk;
+        next_h += gh;
+        if (next_h >= p.H) {
+            next_h -= p.H;
+            ++next_k;
+        }
+        return it;
+    };
+    // source id of item column c (-1: padding or no column)
+    auto column_of = [&](const Item& it, int c) {
+        const int nw = it.nwin();
+        if (nw == 0) return -1;
+        const int split = 16 * it.units0();
+        const bool second = nw == 2 && c >= split;
+        const int local = second ? c - split : c;
+        const int wt = second ? it.b.z : it.a.z, wy = second ? it.b.y : it.a.y;
+        if (local >= kTileCols * min(wt, kTiles)) return -1;
+        return p.tile_cols[(long long)wy * kTileCols + local];
+    };
+    // K rows of the item, its Q rows and its tile bitmaps into stage s.  Eight
+    // threads share a row (one 16-byte piece each), so a warp's copy covers
+    // four whole 128-byte rows; the column ids come from slot cs.
+    auto load_kq = [&](const Item& it, int cs, int s) {
+        const int nw = it.nwin();
+        if (nw == 0) return;
+        const int x = tid & 7;
+        const T* kh = K + (long long)it.h * kD + x * 8;  // this thread's piece of head h of node 0
+        const long long node_stride = (long long)p.H * kD;
+        const uint32_t kdst = smem_u32(sm.k[s]) + (tid >> 3) * 128 + ((x ^ ((tid >> 3) & 7)) << 4);
+#pragma unroll
+        for (int rep = 0; rep < kCols / 16; ++rep) {
+            const int col = sm.cols[cs][(tid >> 3) + 16 * rep];
+            if (col >= 0) cp_async16(kdst + rep * 16 * 128, kh + col * node_stride);
+        }
+#pragma unroll
+        for (int half = 0; half < kMaxWin; ++half) {
+            const int R = (tid >> 3) + kRows * half;
+            const long long node = (long long)(half ? it.b.x : it.a.x) * kRows + (R & 15);
+            const bool ok = half < nw && node < p.N;
+            const T* qsrc = ok ? Q + (node * p.H + it.h) * kD + x * 8 : Q;
+            cp_async16(smem_u32(sm.q[s]) + R * 128 + ((x ^ (R & 7)) << 4), qsrc, ok ? 16u : 0u);
+        }
+        if (tid < kTiles) {
+            const int split = 2 * it.units0();
+            const bool second = nw == 2 && tid >= split;
+            const int t = second ? tid - split : tid;
+            const int wt = second ? it.b.z : it.a.z, wy = second ? it.b.y : it.a.y;
+            if (t < min(wt, kTiles)) cp_async16(smem_u32(&sm.bits[s][tid][0]), p.tile_bits + ((long long)wy + t) * 4);
         }
     };
-    // chunk `ch`'s K or V rows (64 rows x 8 pieces of 16 B) into stage `st`
-    auto issue_gather = [&](const T* src, uint8_t* dst_base, int ch, int ms) {
+    // V rows of the item: every column of each window's 16-column MMA steps,
+    // padding ones zero-filled (their P is 0, and 0 * stale data could be NaN)
+    auto load_v = [&](const Item& it, int cs) {
+        const int nw = it.nwin();
+        if (nw == 0) return;
+        const int x = tid & 7;
+        const int used = 16 * (it.units0() + (nw == 2 ? (min(it.b.z, kTiles) + 1) / 2 : 0));
+        const T* vh = V + (long long)it.h * kD + x * 8;
+        const long long node_stride = (long long)p.H * kD;
+        const uint32_t vdst = smem_u32(sm.v) + (tid >> 3) * 128 + ((x ^ ((tid >> 3) & 7)) << 4);
 #pragma unroll
-        for (int it = 0; it < (kNC * 8) / kThreads; ++it) {
-            const int piece = tid + kThreads * it;
-            const int c = piece >> 3, x = piece & 7;
-            const int col = (ch * 8 + (c >> 3)) < tt ? sm.cols[ms][c] : -1;
-            const long long off = col >= 0 ? ((long long)col * p.H + h) * kD + x * 8 : 0;
-            const uint32_t d = (uint32_t)(c * 128 + ((x ^ (c & 7)) << 4));
-            cp_async16(smem_u32(dst_base) + d, src + off, col >= 0 ? 16u : 0u);
+        for (int rep = 0; rep < kCols / 16; ++rep) {
+            const int c = (tid >> 3) + 16 * rep;
+            if (c < used) {
+                const int col = sm.cols[cs][c];
+                cp_async16(vdst + rep * 16 * 128, col >= 0 ? vh + col * node_stride : V, col >= 0 ? 16u : 0u);
+            }
+        }
+    };
+    // read back O^T of an item, normalise and store its windows' rows: TMEM
+    // lanes 0-63 and again 64-127 hold the 64 features; warps 0 and 1 take
+    // rows 0-7 of each window, warps 2 and 3 rows 8-15, 32 features per warp.
+    auto epilogue = [&](const Item& it) {
+        const int nw = it.nwin();
+        const int f = (warp & 1) * 32 + (tid & 31);
+        const int r0 = (warp >> 1) * 8;
+        const long long stride = (long long)p.H * kD;
+        for (int j = 0; j < nw; ++j) {
+            float o[kRows];
+            tmem_ld16(tmem + 64 + 16 * j + lane_base, o);
+            const long long node0 = (long long)(j ? it.b.x : it.a.x) * kRows + r0;
+            const long long rows_left = p.N - node0;
+            OutT* dst = static_cast<OutT*>(p.O) + (node0 * p.H + it.h) * kD + f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float v = r0 == 0 ? o[r] : o[8 + r];  // static register indices
+                if (r < rows_left) store_out<OutT>(dst, r * stride, v * sm.inv_l[kRows * j + r0 + r]);
+            }
         }
     };
 
-    // ---- this thread's row ------------------------------------------------------
-    const int j = tid >> 4, r = tid & 15;
-    long long node = -1;
-    if (j < sm.nw) {
-        const long long n = (long long)sm.win[j] * kWinRows + r;
-        if (n < p.N) node = n;
-    }
-    const int my_t0 = j < sm.nw ? sm.win_t0[j] : 0;  // this row's window: group tiles [my_t0, my_t1)
-    const int my_t1 = j < sm.nw ? sm.win_t1[j] : 0;
-    const uint32_t tmem_S = tmem;             // S chunk, columns [0, 64)
-    const uint32_t tmem_O = tmem + kNC;       // O accumulator, columns [64, 128)
-    const uint32_t row_S = tmem_row;          // this warp's lanes of S
-    const uint32_t row_O = tmem_row + kNC;    // and of O
-
-    // ---- prologue: Q, chunk 0's metadata, then chunk 0's rows + chunk 1's metadata
-    {
-        const T* qrow = node >= 0 ? Q + (node * p.H + h) * kD : Q;
-        const uint32_t qdst = smem_u32(sm.q) + tid * 128;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) cp_async16(qdst + ((x ^ (tid & 7)) << 4), qrow + x * 8, node >= 0 ? 16u : 0u);
-    }
-    issue_meta(0, 0);
-    cp_async_commit();
-    cp_async_wait_all();
+    // descriptors of items i .. i+3 and this thread's column ids of items i .. i+2
+    Item it0 = fetch_item(0), it1 = fetch_item(1), it2 = fetch_item(2), it3 = fetch_item(3);
+    int col0 = column_of(it0, tid), col1 = column_of(it1, tid), col2 = column_of(it2, tid);
+    Item itp = it0;  // the previous item (for its epilogue)
+    sm.cols[0][tid] = col0;
+    sm.cols[1][tid] = col1;
     __syncthreads();
-    if (nchunks > 0) {
-        issue_gather(K, sm.k[0], 0, 0);
-        issue_gather(V, sm.v[0], 0, 0);
-    }
-    if (nchunks > 1) issue_meta(1, 1);
+    // cp.async groups, oldest first: KQ(0), KQ(1), then per item i: V(i), KQ(i+2).
+    load_kq(it0, 0, 0);
     cp_async_commit();
-
-    float m = kNegBig, l = 0.f;
-    uint32_t phase = 0;
-    bool failed = false;
+    load_kq(it1, 1, 1);
+    cp_async_commit();
     const float scale = p.scale_log2;
-
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const int ks = ch & 1, ms = ch % 3;
-        cp_async_wait_all();  // this chunk's K and V rows, the next chunk's metadata
-        fence_proxy_async_smem();   // ... and the previous chunk's P: visible to the tensor core
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // O += P_{ch-1} V_{ch-1} (accumulated in TMEM), then S = Q K_ch^T; one commit covers both
-        if (tid == 0) {
-            if (ch > 0) {
+    const uint32_t vbase = smem_u32(sm.v), ptbase = smem_u32(sm.pt);
+    // S^T = K Q^T of an item from K/Q stage ks into TMEM S buffer ks (columns [32 ks, 32 ks + 16 nw))
+    auto issue_s = [&](const Item& it, int ks) {
+        const uint32_t idesc = idesc_f16(kBf16, false, 128, kRows * it.nwin());
 #pragma unroll
-                for (int kk = 0; kk < kNC / 16; ++kk)
-                    mma_f16(tmem_O, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
-                            sdesc_sw128(smem_u32(sm.v[ks ^ 1]) + kk * 16 * 128, kNC * 128, 1024), kIdescO,
-                            (ch > 1 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16(tmem + 32 * ks, sdesc_sw128(smem_u32(sm.k[ks]) + kk * 32, 16, 1024),
+                    sdesc_sw128(smem_u32(sm.q[ks]) + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&sm.bar_s));
+    };
+    cp_async_wait_group<1>();  // item 0's K, Q and bitmaps
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && n_my > 0) issue_s(it0, 0);
+    bool failed = false;
+
+    for (int i = 0; i < n_my; ++i) {
+        const int s = i & 1;
+        const int cs = i % 3;
+        sm.cols[(i + 2) % 3][tid] = col2;  // slot last read by item i-1's V copies, before the next barrier
+        const int nw = it0.nwin();
+        const int split = 16 * it0.units0();  // first column of window 1
+        // (c) O^T of item i-1 complete: V and P^T are free.  Item i's V rows are
+        // requested and item i-1's rows stored.
+        {
+            // thread 0 also takes item i's S^T (issued during item i-1, normally done by
+            // now), so one barrier serves both waits
+            bool ok = true;
+            if (tid == 0) {
+                if (i > 0) ok = mbar_wait_bounded_sleep(smem_u32(&sm.bar_o), (uint32_t)((i - 1) & 1), kWaitLimitNs);
+                if (ok) ok = mbar_wait_bounded_sleep(smem_u32(&sm.bar_s), (uint32_t)(i & 1), kWaitLimitNs);
             }
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-                mma_f16(tmem_S, sdesc_sw128(smem_u32(sm.q) + kk * 32, 16, 1024),
-                        sdesc_sw128(smem_u32(sm.k[ks]) + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&sm.mbar));
+            if (__syncthreads_or(!ok)) {
+                failed = true;
+                break;
+            }
+            tc_fence_after();
         }
-        // the next chunk's K rows (that stage was last read by S_{ch-1}, complete) and
-        // the metadata two chunks ahead
-        if (ch + 1 < nchunks) issue_gather(K, sm.k[ks ^ 1], ch + 1, (ch + 1) % 3);
-        if (ch + 2 < nchunks) issue_meta(ch + 2, (ch + 2) % 3);
-
-        const bool ok = mbar_wait_bounded(smem_u32(&sm.mbar), phase, kWaitLimitNs);
-        phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        tc_fence_after();
-        // the next chunk's V rows (that stage was last read by P_{ch-1} V_{ch-1}, now complete)
-        if (ch + 1 < nchunks) issue_gather(V, sm.v[ks ^ 1], ch + 1, (ch + 1) % 3);
+        load_v(it0, cs);
         cp_async_commit();
+        if (i > 0) epilogue(itp);
+        // column ids of item i+3 and the descriptor of item i+4, for the next iterations
+        const int col3 = column_of(it3, tid);
+        const Item it4 = fetch_item(i + 4);
 
-        // masked online softmax of this row of S_ch
-        float s[kNC];
+        // (d) this thread's column of item i's logits, masked and scaled
+        const int c = tid;
+        const bool second = nw == 2 && c >= split;
+        float x[kRows];
+        {
+            float t16[kRows];
+            tmem_ld16(tmem + 32 * s + lane_base, t16);  // warp-collective: window 0's rows, every column
 #pragma unroll
-        for (int q4 = 0; q4 < kNC / 16; ++q4) {
-            float v16[16];
-            tmem_ld16(row_S + q4 * 16, v16);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s[q4 * 16 + i] = v16[i];
+            for (int r = 0; r < kRows; ++r) x[r] = t16[r];
         }
-        float cmax = -INFINITY;
+        if (nw == 2) {
+            float t16[kRows];
+            tmem_ld16(tmem + 32 * s + 16 + lane_base, t16);  // window 1's rows
+            if (second) {
 #pragma unroll
-        for (int slot = 0; slot < 8; ++slot) {
-            const int t = ch * 8 + slot;
-            uint32_t mask8 = 0;
-            if (node >= 0 && t >= my_t0 && t < my_t1) mask8 = (sm.bits[ms][slot][r >> 2] >> ((r & 3) * 8)) & 0xffu;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float x = ((mask8 >> c) & 1u) ? s[slot * 8 + c] * scale : -INFINITY;
-                s[slot * 8 + c] = x;
-                cmax = fmaxf(cmax, x);
-            }
-        }
-        // Move the reference max when a logit exceeds it by more than the slack.
-        // The row of O in TMEM then needs the same factor -- unless nothing has
-        // been accumulated for this row yet (l == 0: its O row is still zero).
-        float corr = 1.f;
-        bool rescale = false;
-        if (cmax > m + kRescaleSlack) {
-            corr = ex2(m - cmax);
-            rescale = l > 0.f;
-            l *= corr;
-            m = cmax;
-        }
-        // tcgen05.ld / st are warp-collective: every thread takes part, the
-        // ones that need no rescale multiply by 1.
-        if (__syncthreads_or(rescale)) {  // rare; O_{ch-1} is complete, nothing is in flight on O
-            const float f = rescale ? corr : 1.f;
-#pragma unroll
-            for (int q4 = 0; q4 < kD / 16; ++q4) {
-                float v16[16];
-                tmem_ld16(row_O + q4 * 16, v16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v16[i] *= f;
-                tmem_st16(row_O + q4 * 16, v16);
+                for (int r = 0; r < kRows; ++r) x[r] = t16[r];
             }
         }
         {
-            const uint32_t pdst = smem_u32(sm.p) + tid * 128;
+            uint4 b = make_uint4(0u, 0u, 0u, 0u);
+            if (col0 >= 0) b = *reinterpret_cast<const uint4*>(&sm.bits[s][c >> 3][0]);
+            const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
+            float* xt = reinterpret_cast<float*>(sm.k[s]);  // [column][kXtPitch]
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                uint32_t w[4];
+            for (int r = 0; r < kRows; ++r) {
+                const bool on = (w4[r >> 2] >> ((r & 3) * 8 + (c & 7))) & 1u;
+                x[r] = on ? x[r] * scale : -INFINITY;
+            }
+            float4* dst = reinterpret_cast<float4*>(xt + c * kXtPitch);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float ra, rb;
-                    w[k] = Pack2<T>::pack(ex2(s[x * 8 + 2 * k] - m), ex2(s[x * 8 + 2 * k + 1] - m), ra, rb);
-                    l += ra + rb;
-                }
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pdst + ((x ^ (tid & 7)) << 4)), "r"(w[0]),
-                             "r"(w[1]), "r"(w[2]), "r"(w[3])
-                             : "memory");
+            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+        }
+        cp_async_wait_group<1>();  // item i+1's K, Q and bitmaps (only item i's V may still be in flight)
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();  // transposed logits complete; S^T, item i's Q and bitmaps are no longer read
+        tc_fence_after();
+        if (tid == 0 && i + 1 < n_my) issue_s(it1, s ^ 1);  // runs while item i goes through its softmax
+        // (d2) row maxima and row sums of the rounded P: eight threads per row over
+        // the item's columns 8 at a time (column 8 k + part)
+        {
+            const int r = tid >> 3, part = tid & 7;
+            const int ksplit = split >> 3;
+            const int nsteps = ksplit + (nw == 2 ? 2 * ((min(it0.b.z, kTiles) + 1) / 2) : 0);
+            const float* xt = reinterpret_cast<const float*>(sm.k[s]);
+            float xs[2 * kTileItemUnits];
+            float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 2 * kTileItemUnits; ++k) {
+                xs[k] = k < nsteps ? xt[(8 * k + part) * kXtPitch + r] : -INFINITY;
+                if (k < ksplit)
+                    m0 = fmaxf(m0, xs[k]);
+                else
+                    m1 = fmaxf(m1, xs[k]);
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (m0 == -INFINITY) m0 = 0.f;  // a row without entries: every P is 0
+            if (m1 == -INFINITY) m1 = 0.f;
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 2 * kTileItemUnits; ++k) {
+                if (k < ksplit)
+                    l0 += Half2<T>::round(ex2(xs[k] - m0));
+                else
+                    l1 += Half2<T>::round(ex2(xs[k] - m1));
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            if (part == 0) {
+                sm.rowmax[r] = m0;
+                sm.rowmax[kRows + r] = m1;
+                sm.inv_l[r] = l0 > 0.f ? 1.0f / l0 : 0.f;
+                sm.inv_l[kRows + r] = l1 > 0.f ? 1.0f / l1 : 0.f;
             }
         }
-    }
-
-    // the last chunk's P V
-    if (!failed && nchunks > 0) {
-        cp_async_wait_all();
+        __syncthreads();  // row maxima published; item i's K stage is free
+        // (e) item i+2's K, Q and bitmaps into stage s
+        load_kq(it2, (i + 2) % 3, s);
+        cp_async_commit();
+        // (f) this column's 16 values of P, one 32-byte row of P^T (rows 0-7 and 8-15 in
+        // the two 16-byte halves, swapped on every other group of four columns)
+        {
+            const float4* mr = reinterpret_cast<const float4*>(&sm.rowmax[second ? kRows : 0]);
+            uint32_t w[8];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 m = mr[q4];
+                w[2 * q4] = Half2<T>::pack(ex2(x[4 * q4] - m.x), ex2(x[4 * q4 + 1] - m.y));
+                w[2 * q4 + 1] = Half2<T>::pack(ex2(x[4 * q4 + 2] - m.z), ex2(x[4 * q4 + 3] - m.w));
+            }
+            const uint32_t row = ptbase + c * 32, sw = (uint32_t)((c >> 2) & 1) << 4;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + sw), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (sw ^ 16u)), "r"(w[4]), "r"(w[5]),
+                         "r"(w[6]), "r"(w[7])
+                         : "memory");
+        }
+        // (g) item i's V rows; O^T = V^T P^T per window, over its columns 16 at a time
+        cp_async_wait_group<1>();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < kNC / 16; ++kk)
-                mma_f16(tmem_O, sdesc_sw128(smem_u32(sm.p) + kk * 32, 16, 1024),
-                        sdesc_sw128(smem_u32(sm.v[(nchunks - 1) & 1]) + kk * 16 * 128, kNC * 128, 1024), kIdescO,
-                        (nchunks > 1 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&sm.mbar));
+            for (int j = 0; j < nw; ++j) {
+                const int c0 = j ? split : 0;
+                const int ksteps = j ? (min(it0.b.z, kTiles) + 1) / 2 : it0.units0();
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    const uint32_t va = vbase + (uint32_t)(c0 + 16 * kk) * 128;
+                    mma_f16(tmem + 64 + 16 * j, sdesc_sw128(va, 0, 1024),
+                            sdesc_sw32(ptbase + (uint32_t)(c0 + 16 * kk) * 32, 0, 256), kIdescO, kk > 0 ? 1u : 0u);
+                }
+            }
+            mma_commit(smem_u32(&sm.bar_o));
         }
-        const bool ok = mbar_wait_bounded(smem_u32(&sm.mbar), phase, kWaitLimitNs);
-        phase ^= 1u;
-        if (__syncthreads_or(!ok)) failed = true;
-        tc_fence_after();
+        itp = it0;
+        it0 = it1;
+        it1 = it2;
+        it2 = it3;
+        it3 = it4;
+        col0 = col1;
+        col1 = col2;
+        col2 = col3;
+    }
+    if (!failed && n_my > 0) {
+        if (!cta_wait(smem_u32(&sm.bar_o), (uint32_t)((n_my - 1) & 1))) {
+            failed = true;
+        } else {
+            tc_fence_after();
+            epilogue(itp);
+        }
     }
     cp_async_wait_all();
-
-    if (!failed) {  // uniform over the CTA
-        float o[kD];
-        if (nchunks > 0) {
-            // warp-collective read of every row, padding rows included
-#pragma unroll
-            for (int q4 = 0; q4 < kD / 16; ++q4) {
-                float v16[16];
-                tmem_ld16(row_O + q4 * 16, v16);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[q4 * 16 + i] = v16[i];
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kD; ++i) o[i] = 0.f;
-        }
-        if (node >= 0) store_row<OutT>(p.O, (node * p.H + h) * kD, o, l > 0.f ? 1.0f / l : 0.f);
-    }
     if (failed && tid == 0) atomicOr(p.status, kErrTimeout);
     tc_fence_before();
     __syncthreads();
@@ -427,13 +501,32 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int32_t* statu
 
 template <typename T, typename OutT>
 cudaError_t launch(const TileParams& p, cudaStream_t st) {
-    if (p.n_tile_windows <= 0) return cudaSuccess;
+    if (p.n_tile_items <= 0) return cudaSuccess;
     const size_t smem = sizeof(TileSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const long long groups = (p.n_tile_windows + kGroupWindows - 1) / kGroupWindows;
-    dim3 grid((unsigned)groups, (unsigned)p.H);
-    tile_kernel<T, OutT><<<grid, kThreads, smem, st>>>(p);
+    // all of the SM's unified L1/shared storage as shared memory, so three CTAs fit
+    e = cudaFuncSetAttribute(tile_kernel<T, OutT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    // resident CTAs per SM from shared memory, registers and TMEM (the
+    // occupancy query does not see the carveout set above)
+    int dev = 0, sms = 0, smem_sm = 0, reserved = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, tile_kernel<T, OutT>)) != cudaSuccess) return e;
+    int per_sm = smem_sm / (int)(smem + reserved);
+    const int regs = (fa.numRegs + 7) / 8 * 8 * kThreads;
+    if (regs > 0 && 65536 / regs < per_sm) per_sm = 65536 / regs;
+    if ((int)(512 / kTmemCols) < per_sm) per_sm = (int)(512 / kTmemCols);
+    if (per_sm < 1) per_sm = 1;
+    const long long work = p.n_tile_items * p.H;
+    long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    if (grid > work) grid = work;
+    tile_kernel<T, OutT><<<(unsigned)grid, kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -139,3 +139,36 @@ def test_tile_selection_brute_force():
     tile, core = list(sel["tile_windows"]), list(sel["core_windows"])
     assert sorted(tile + core) == list(range(W)) and tile == sorted(tile) and core == sorted(core)
     assert 0 < len(tile) < W
+
+
+def test_tile_items_pairing():
+    """Every tile-path window sits in exactly one item, in list order; two
+    share an item only as list entries 2k and 2k+1 and only when their
+    16-column units (ceil(T/2)) fit the 8 units of an item; an item of two
+    starts its second window at 16 * units0 columns."""
+    g = graphgen.batched_dense(num_graphs=60, seed=12)
+    b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=100, max_tiles=16, density_milli=0)
+    tw = sel["tile_windows"]
+    items = planner.tile_items(g.row_ptr, b, tw)
+    ptr = b["win_tile_ptr"]
+    seen = []
+    for it in items:
+        nwin, u0 = it[3] & 0xFF, it[3] >> 8
+        assert nwin in (1, 2)
+        wins = [it[0]] + ([it[4]] if nwin == 2 else [])
+        for w, first, t in zip(wins, (it[1], it[5]), (it[2], it[6])):
+            assert first == ptr[w] and t == ptr[w + 1] - ptr[w]
+        assert u0 == (it[2] + 1) // 2
+        if nwin == 2:
+            assert u0 + (it[6] + 1) // 2 <= 8
+            assert len(seen) % 2 == 0  # a pair starts at an even list position
+        else:
+            assert not np.any(it[4:])
+        seen += wins
+    assert seen == list(tw)
+    # an unpaired even entry: its partner did not fit
+    units = [(ptr[w + 1] - ptr[w] + 1) // 2 for w in tw]
+    pairs = sum(1 for it in items if (it[3] & 0xFF) == 2)
+    want_pairs = sum(1 for k in range(0, len(tw) - 1, 2) if units[k] + units[k + 1] <= 8)
+    assert pairs == want_pairs and 0 < pairs < len(tw) // 2 + 1
