@@ -361,7 +361,8 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
                        "peak_tflops": tf, "peak_source": tf_src + " (fp16 dense rate equals bf16's)"}
     if with_paths:
         paths = {}
-        for label, kw in (("core_only", dict(tile_path=0)), ("tile_only", dict(tile_path=1, tile_density_milli=0))):
+        for label, kw in (("core_only", dict(tile_path=0)),
+                          ("tile_only", dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))):
             p2 = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **kw)
             s2 = p2.stats()
             w2, c2 = measure(p2)
@@ -398,6 +399,8 @@ def parse_args():
                     help="tensor-core tile path: -1 automatic (default), 0 off, 1 on")
     ap.add_argument("--tile-density-milli", type=int, default=None,
                     help="density cutoff of the tile path in 1/1000 (default: the library's)")
+    ap.add_argument("--tile-pool-density-milli", type=int, default=None,
+                    help="pooled density the tile-eligible windows need to take the tile path (default: the library's)")
     ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
                     help="element type of O (default fp32)")
     ap.add_argument("--graph", action="store_true",
@@ -604,6 +607,8 @@ def main():
         plan_kw["out_dtype"] = args.out_dtype
     if args.tile_density_milli is not None:
         plan_kw["tile_density_milli"] = args.tile_density_milli
+    if args.tile_pool_density_milli is not None:
+        plan_kw["tile_pool_density_milli"] = args.tile_pool_density_milli
     if args.tma_gather is not None:
         plan_kw["tma_gather"] = args.tma_gather
     if args.pack_rows is not None:

@@ -89,12 +89,20 @@ typedef enum g3s_variant {
  *                  0 off, -1 automatic (default -1: on where compiled, which
  *                  is the standard form with fp16/bf16 inputs and d = 64,
  *                  unless bsb = 0)
- *  tile_density_milli  a window takes the tile path when
- *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 400:
- *                  the tile kernel's time follows its tiles, the CUDA-core
- *                  kernel's its edges; measured on batched 20-60-node graphs
- *                  they cross near edge probability 0.55, and on complete
- *                  graphs the tile path is about 1.6 times as fast)
+ *  tile_density_milli  a window is eligible for the tile path when
+ *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 150)
+ *                  and it has no repeated (row, source) pair, at most
+ *                  tile_max_tiles tiles and no heavy row
+ *  tile_pool_density_milli  the eligible windows take the tile path together
+ *                  when 1000 * (their CSR entries) >= tile_pool_density_milli *
+ *                  128 * (their tiles), and none does otherwise (default 300).
+ *                  Measured on one GB300 with batched 20-60-node graphs (8 x 64
+ *                  bf16): the tensor-core kernel wins from a pooled density of
+ *                  about 0.3 (edge probability 0.4: 0.127 ms against 0.139 ms;
+ *                  complete graphs 0.139 against 0.302), loses slightly below it
+ *                  (p = 0.3, pooled 0.24: 0.133 against 0.119); a plan that
+ *                  splits a batch between the two kernels pays the slower
+ *                  one's tail, so the choice is made for the batch
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 16, i.e. 128 source columns,
  *                  the M side of the kernel's tcgen05 product)
@@ -142,6 +150,7 @@ typedef struct g3s_plan_options {
     int32_t out_dtype;
     int32_t tma_gather;
     int32_t pack_rows;
+    int32_t tile_pool_density_milli;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {

@@ -27,9 +27,11 @@ Three outputs, all integer, all unique under the canonical orderings below.
    (r*8+c)//32) is set iff the CSR holds an edge (16w + r <- tile_cols[8t+c]).
    ``win_nnz`` counts CSR entries per window; ``win_flags`` bit 0 marks a
    window with a repeated (row, source) pair, bit 1 a window that takes the
-   tile path.  A window takes the tile path when the tile path is enabled and
-   it has no repeated pair, 1 <= T_w <= max_tiles, no heavy row, and
-   1000 * nnz >= density_milli * 128 * T_w.  ``tile_windows`` lists them in
+   tile path.  With the tile path enabled, a window is eligible when it has
+   no repeated pair, 1 <= T_w <= max_tiles, no heavy row, and
+   1000 * nnz >= density_milli * 128 * T_w; the eligible windows take the tile
+   path together when 1000 * (sum of their nnz) >= pool_milli * 128 * (sum of
+   their T_w), and none does otherwise.  ``tile_windows`` lists them in
    ascending order, ``core_windows`` the other windows (whose rows the
    CUDA-core kernel takes), also ascending.
 """
@@ -140,7 +142,7 @@ def bsb(row_ptr: np.ndarray, col_idx: np.ndarray, num_nodes: int) -> dict:
 
 
 def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold: int,
-                   max_tiles: int, density_milli: int) -> dict:
+                   max_tiles: int, density_milli: int, pool_milli: int = 0) -> dict:
     W = b["win_nnz"].shape[0]
     flags = np.where(b["win_dup"], FLAG_DUP, 0).astype(np.uint8)
     if enabled:
@@ -151,9 +153,12 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
         maxdeg = pad.reshape(W, WIN_ROWS).max(axis=1)
         nt = np.diff(b["win_tile_ptr"].astype(np.int64))
         nnz = b["win_nnz"].astype(np.int64)
-        ok = (~b["win_dup"]) & (nt >= 1) & (nt <= max_tiles) & (maxdeg <= heavy_threshold) \
+        elig = (~b["win_dup"]) & (nt >= 1) & (nt <= max_tiles) & (maxdeg <= heavy_threshold) \
             & (1000 * nnz >= int(density_milli) * 128 * nt)
-        flags = flags | np.where(ok, FLAG_TILE, 0).astype(np.uint8)
+        pool_nnz, pool_tiles = int(nnz[elig].sum()), int(nt[elig].sum())
+        take = pool_tiles > 0 and 1000 * pool_nnz >= int(pool_milli) * 128 * pool_tiles
+        if take:
+            flags = flags | np.where(elig, FLAG_TILE, 0).astype(np.uint8)
     tile_windows = np.flatnonzero(flags & FLAG_TILE).astype(np.int32)
     core_windows = np.flatnonzero((flags & FLAG_TILE) == 0).astype(np.int32)
     return dict(win_flags=flags, tile_windows=tile_windows, core_windows=core_windows)

@@ -66,6 +66,7 @@ class PlanOptions(ctypes.Structure):
         ("out_dtype", ctypes.c_int32),
         ("tma_gather", ctypes.c_int32),
         ("pack_rows", ctypes.c_int32),
+        ("tile_pool_density_milli", ctypes.c_int32),
     ]
 
 

@@ -64,7 +64,8 @@ void default_options(g3s_plan_options* o) {
     o->chunk_edges = 512;
     o->bsb = -1;
     o->tile_path = -1;
-    o->tile_density_milli = 400;
+    o->tile_density_milli = 150;
+    o->tile_pool_density_milli = 300;
     o->tile_max_tiles = 16;
     o->bsb_smem_edges = 2048;
     o->rtm_elementwise_clamp = 1;
@@ -99,8 +100,9 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (o.chunk_edges < 1) return fail(G3S_ERR_INVALID_ARG, "chunk_edges must be >= 1");
     if (o.bsb < -1 || o.bsb > 1 || o.tile_path < -1 || o.tile_path > 1)
         return fail(G3S_ERR_INVALID_ARG, "bsb and tile_path take -1, 0 or 1");
-    if (o.tile_density_milli < 0 || o.tile_max_tiles < 1)
-        return fail(G3S_ERR_INVALID_ARG, "tile_density_milli >= 0 and tile_max_tiles >= 1 required");
+    if (o.tile_density_milli < 0 || o.tile_max_tiles < 1 || o.tile_pool_density_milli < 0)
+        return fail(G3S_ERR_INVALID_ARG,
+                    "tile_density_milli >= 0, tile_pool_density_milli >= 0 and tile_max_tiles >= 1 required");
     if (o.bsb_smem_edges < 1 || o.bsb_smem_edges > 16384)
         return fail(G3S_ERR_INVALID_ARG, "bsb_smem_edges must be in [1, 16384]");
     if (!(o.rtm_epsilon >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "rtm_epsilon must be >= 0");
@@ -130,6 +132,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
     s->tile_density_milli = o.tile_density_milli;
+    s->tile_pool_milli = o.tile_pool_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
     // automatic: on where compiled, unless the caller turned the BSB tiles off
     s->tile_enabled = tile_ok && (o.tile_path == 1 || (o.tile_path == -1 && o.bsb != 0));
@@ -153,6 +156,7 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     Carver c{static_cast<char*>(base)};
     a->counts = c.take<PlanCounts>(1);
     a->work_counter = c.take<unsigned long long>(1);
+    a->tile_counter = c.take<unsigned int>(1);
     a->fwd_status = c.take<int32_t>(1);
     a->bucket_of = c.take<uint8_t>(s.N);
     a->bucket_ptr = c.take<int32_t>(G3S_NUM_BUCKETS + 1);
@@ -472,6 +476,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.tile_bits = p->arr.tile_bits;
         tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;
         tp.status = p->arr.fwd_status;
+        tp.work_counter = p->arr.tile_counter;
         // the CUDA-core kernel first, on the plan's high-priority side stream,
         // then the tile kernel on the caller's stream; the two overlap
         CUDA_OR_FAIL(cudaEventRecord(p->ev_fork, stream), "cudaEventRecord(fork)");
@@ -479,6 +484,7 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, p->side),
                      "fused kernel launch");
         CUDA_OR_FAIL(cudaEventRecord(p->ev_join, p->side), "cudaEventRecord(join)");
+        CUDA_OR_FAIL(cudaMemsetAsync(p->arr.tile_counter, 0, sizeof(unsigned int), stream), "cudaMemsetAsync(tile queue)");
         CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
         CUDA_OR_FAIL(cudaStreamWaitEvent(stream, p->ev_join, 0), "cudaStreamWaitEvent(join)");
     } else {

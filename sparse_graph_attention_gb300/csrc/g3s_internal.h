@@ -13,6 +13,7 @@ constexpr int kWinRows = 16;   // rows per BSB row window
 constexpr int kTileCols = 8;   // columns per BSB tile (16x8 tiles)
 constexpr int kFlagDup = 1;    // window holds a repeated (row, source) pair
 constexpr int kFlagTile = 2;   // window takes the tensor-core tile path
+constexpr int kFlagElig = 4;   // planner scratch: window eligible for the tile path (cleared before the plan is done)
 constexpr int kWarpsPerCta = 8;
 
 // Error bits written by the CSR validation kernel.
@@ -46,6 +47,7 @@ struct PlanCounts {
     int32_t n_large_windows;
     int32_t n_short;  // rows with at most PlanShape::pack_limit entries
     long long tile_window_nnz;
+    long long elig_nnz, elig_tiles;  // CSR entries and tiles of the tile-eligible windows
     int32_t n_tile_items;  // work items of the tile kernel (one or two tile-path windows each)
 };
 
@@ -76,6 +78,7 @@ struct PlanArrays {
     int32_t* scan_blocks;      // [scan_block_capacity]
     PlanCounts* counts;
     unsigned long long* work_counter;  // the fused kernel's work queue head
+    unsigned int* tile_counter;        // the tile kernel's work queue head
     int32_t* fwd_status;               // error bits set by forward kernels (kErrTimeout)
 };
 
@@ -87,7 +90,7 @@ struct PlanShape {
     int heavy_threshold, chunk_edges;
     int bounds[G3S_NUM_BUCKETS - 2];
     int bsb_smem_edges;
-    int tile_density_milli, tile_max_tiles;
+    int tile_density_milli, tile_max_tiles, tile_pool_milli;
     bool build_bsb, tile_enabled;
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
     int64_t scan_blocks;
@@ -222,6 +225,7 @@ struct TileParams {
     const uint32_t* tile_bits;
     float scale_log2;  // log2(e)/sqrt(d)
     int32_t* status;   // kErrTimeout is OR-ed in when a wait gives up
+    unsigned int* work_counter;  // zeroed before the launch; CTAs take work indices from it
 };
 bool tile_supported(int dtype, int variant, int head_dim);
 cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st);

@@ -544,10 +544,19 @@ __global__ void k_tile_ptr_tail(const PlanCounts* c, int32_t* win_tile_ptr, long
     if (threadIdx.x == 0 && blockIdx.x == 0) win_tile_ptr[W] = c->n_tiles;
 }
 
-__global__ void k_tile_select(const int32_t* row_ptr, long long N, long long W, const int32_t* win_tile_ptr,
-                              const int32_t* win_nnz, uint8_t* win_flags, bool enabled, int heavy_threshold,
-                              int max_tiles, int density_milli, PlanCounts* c) {
+// Tile-path selection, two passes.  A window is eligible when it has no
+// repeated (row, source) pair, 1..max_tiles tiles, no heavy row and a density
+// (CSR entries / (128 tiles)) of at least density_milli / 1000.  The eligible
+// windows then take the tile path together when their pooled density
+// (their entries / (128 x their tiles)) reaches pool_milli / 1000, and none does
+// otherwise: the two kernels run concurrently but a plan that splits a batch of
+// similar windows between them pays the slower kernel's tail, so the choice is
+// made for the batch.
+__global__ void k_tile_eligible(const int32_t* row_ptr, long long N, long long W, const int32_t* win_tile_ptr,
+                                const int32_t* win_nnz, uint8_t* win_flags, bool enabled, int heavy_threshold,
+                                int max_tiles, int density_milli, PlanCounts* c) {
     int ndup = 0;
+    unsigned long long nnz_sum = 0, tile_sum = 0;
     for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < W; w += (long long)gridDim.x * blockDim.x) {
         uint8_t f = win_flags[w];
         if (f & kFlagDup) ++ndup;
@@ -559,13 +568,26 @@ __global__ void k_tile_select(const int32_t* row_ptr, long long N, long long W, 
             const long long nnz = win_nnz[w];
             if (nt >= 1 && nt <= max_tiles && md <= heavy_threshold &&
                 1000LL * nnz >= (long long)density_milli * 128LL * nt) {
-                f |= kFlagTile;
-                atomicAdd(reinterpret_cast<unsigned long long*>(&c->tile_window_nnz), (unsigned long long)nnz);
+                f |= kFlagElig;
+                nnz_sum += (unsigned long long)nnz;
+                tile_sum += (unsigned long long)nt;
             }
         }
         win_flags[w] = f;
     }
     if (ndup) atomicAdd(&c->n_dup_windows, ndup);
+    if (nnz_sum) atomicAdd(reinterpret_cast<unsigned long long*>(&c->elig_nnz), nnz_sum);
+    if (tile_sum) atomicAdd(reinterpret_cast<unsigned long long*>(&c->elig_tiles), tile_sum);
+}
+
+__global__ void k_tile_pool(long long W, uint8_t* win_flags, int pool_milli, PlanCounts* c) {
+    const unsigned long long nnz = (unsigned long long)c->elig_nnz, tiles = (unsigned long long)c->elig_tiles;
+    const bool take = tiles > 0 && 1000ull * nnz >= (unsigned long long)pool_milli * 128ull * tiles;
+    for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < W; w += (long long)gridDim.x * blockDim.x) {
+        const uint8_t f = win_flags[w];
+        win_flags[w] = (uint8_t)((f & ~kFlagElig) | ((take && (f & kFlagElig)) ? kFlagTile : 0));
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) c->tile_window_nnz = take ? (long long)nnz : 0;
 }
 
 // Tile-kernel items: list entries (2k, 2k+1) share an item when their
@@ -722,9 +744,11 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
 
     // 4. tile-path selection
     if (W > 0) {
-        k_tile_select<<<grid_for(W, 256), 256, 0, st>>>(row_ptr, s.N, W, a.win_tile_ptr, a.win_nnz, a.win_flags,
-                                                        s.tile_enabled, s.heavy_threshold, s.tile_max_tiles,
-                                                        s.tile_density_milli, c);
+        k_tile_eligible<<<grid_for(W, 256), 256, 0, st>>>(row_ptr, s.N, W, a.win_tile_ptr, a.win_nnz, a.win_flags,
+                                                          s.tile_enabled, s.heavy_threshold, s.tile_max_tiles,
+                                                          s.tile_density_milli, c);
+        G3S_TRY(cudaGetLastError());
+        k_tile_pool<<<grid_for(W, 256), 256, 0, st>>>(W, a.win_flags, s.tile_pool_milli, c);
         G3S_TRY(cudaGetLastError());
     }
     G3S_TRY(scan(TileFlag{a.win_flags}, ListOut{a.tile_windows}, W, a.scan_blocks, &c->n_tile_windows, st));

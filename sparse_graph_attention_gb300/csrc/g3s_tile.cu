@@ -78,6 +78,7 @@ struct TileSmem {
     float inv_l[kItemRows];            // 1 / row sum of P (0 for a row without entries)
     uint32_t bits[2][kTiles][4];       // tile bitmaps by stage and item tile slot
     int cols[3][kCols];                // source ids of the item columns, item i in slot i % 3 (-1: none)
+    int ring[8];                       // work indices of this CTA's items, item j in slot j % 8
     unsigned long long bar_s, bar_o;
     uint32_t tmem_base;
 };
@@ -149,16 +150,16 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     const T* V = static_cast<const T*>(p.V);
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kRows, true);  // A and B MN-major
-    const long long n_work = p.n_tile_items * p.H;
-    const long long G = gridDim.x;
-    const long long first = blockIdx.x;
-    const int n_my = first < n_work ? (int)((n_work - 1 - first) / G + 1) : 0;
+    const int n_work = (int)(p.n_tile_items * p.H);  // work index k H + h: item k, head h
 
     if (warp == 0) tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     if (tid == 0) {
         mbar_init(smem_u32(&sm.bar_s), 1);
         mbar_init(smem_u32(&sm.bar_o), 1);
         fence_mbar_init();
+        // the first five work indices of this CTA (a CTA that starts late takes fewer)
+#pragma unroll
+        for (int j = 0; j < 5; ++j) sm.ring[j] = (int)atomicAdd(p.work_counter, 1u);
     }
     tc_fence_before();
     __syncthreads();
@@ -174,24 +175,17 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         if (tid == 0) ok = mbar_wait_bounded_sleep(bar, parity, kWaitLimitNs);
         return __syncthreads_or(!ok) == 0;
     };
-    // item j of this CTA (a zero item past the end)
-    // (work index first + j G = k H + h: k and h advanced by G per item, no division)
-    const int gk = (int)(G / p.H), gh = (int)(G - (long long)gk * p.H);
-    int next_k = (int)(first / p.H), next_h = (int)(first - (long long)next_k * p.H);
-    auto fetch_item = [&](int j) {  // called with j = 0, 1, 2, ... in order
+    // item j of this CTA from its work index in the ring (a zero item past the end)
+    auto fetch_item = [&](int j) {
         Item it;
         it.a = it.b = make_int4(0, 0, 0, 0);
         it.h = 0;
-        if (j < n_my) {
-            it.h = next_h;
-            it.a = p.tile_items[2 * next_k];
-            it.b = p.tile_items[2 * next_k + 1];
-        }
-        next_k += gk;
-        next_h += gh;
-        if (next_h >= p.H) {
-            next_h -= p.H;
-            ++next_k;
+        const int wk = sm.ring[j & 7];
+        if (wk < n_work) {
+            const int k = wk / p.H;
+            it.h = wk - k * p.H;
+            it.a = p.tile_items[2 * k];
+            it.b = p.tile_items[2 * k + 1];
         }
         return it;
     };
@@ -306,10 +300,16 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && n_my > 0) issue_s(it0, 0);
+    if (tid == 0 && it0.nwin() > 0) issue_s(it0, 0);
     bool failed = false;
+    int done = 0;  // items this CTA has finished
 
-    for (int i = 0; i < n_my; ++i) {
+    // Work indices are taken from one counter in increasing order, so the first
+    // empty item ends the CTA's sequence.
+    for (int i = 0; it0.nwin() > 0; ++i) {
+        // the work index of item i+5, stored at the end of this iteration
+        int grab = 0;
+        if (tid == 96) grab = (int)atomicAdd(p.work_counter, 1u);
         const int s = i & 1;
         const int cs = i % 3;
         sm.cols[(i + 2) % 3][tid] = col2;  // slot last read by item i-1's V copies, before the next barrier
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         tc_fence_before();
         __syncthreads();  // transposed logits complete; S^T, item i's Q and bitmaps are no longer read
         tc_fence_after();
-        if (tid == 0 && i + 1 < n_my) issue_s(it1, s ^ 1);  // runs while item i goes through its softmax
+        if (tid == 0 && it1.nwin() > 0) issue_s(it1, s ^ 1);  // runs while item i goes through its softmax
         // (d2) row maxima and row sums of the rounded P: eight threads per row over
         // the item's columns 8 at a time (column 8 k + part)
         {
@@ -461,6 +461,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
             }
             mma_commit(smem_u32(&sm.bar_o));
         }
+        if (tid == 96) sm.ring[(i + 5) & 7] = grab;  // read by fetch_item(i + 5) after the next barriers
+        ++done;
         itp = it0;
         it0 = it1;
         it1 = it2;
@@ -470,8 +472,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const TileParams p) {
         col1 = col2;
         col2 = col3;
     }
-    if (!failed && n_my > 0) {
-        if (!cta_wait(smem_u32(&sm.bar_o), (uint32_t)((n_my - 1) & 1))) {
+    if (!failed && done > 0) {
+        if (!cta_wait(smem_u32(&sm.bar_o), (uint32_t)((done - 1) & 1))) {
             failed = true;
         } else {
             tc_fence_after();

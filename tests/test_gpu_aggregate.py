@@ -65,7 +65,7 @@ def test_aggregate_full_powerlaw():
 def test_aggregate_on_tile_plan_covers_tile_windows():
     """Rows in tile-path windows are aggregated too (the tile kernel is attention-only)."""
     g = graphgen.batched_dense(num_graphs=20, seed=12)
-    plan = _case(g, 2, 64, "bf16", True, positive=True, seed=13, plan_kw=dict(tile_path=1, tile_density_milli=0))
+    plan = _case(g, 2, 64, "bf16", True, positive=True, seed=13, plan_kw=dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))
     assert plan.stats()["tile_windows"] > 0
 
 

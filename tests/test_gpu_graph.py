@@ -24,7 +24,7 @@ def _build():
 
 
 @pytest.mark.parametrize("name,kw", [("tiny_poisson", {}), ("rtmscore_batch64", {}),
-                                     ("batched_dense", {"tile_path": 1, "tile_density_milli": 200}),
+                                     ("batched_dense", {"tile_path": 1, "tile_density_milli": 200, "tile_pool_density_milli": 0}),
                                      ("powerlaw", {"heavy_threshold": 64, "chunk_edges": 40})])
 def test_forward_replays_in_a_cuda_graph(name, kw):
     dev = device()

@@ -111,7 +111,7 @@ def test_pack_beside_tile_windows():
     g = graphgen.batched_dense(num_graphs=40, seed=10)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 1, 64, False, seed=11)
     plan, _, _ = run_case(g, vals, 1, 64, "bf16", "standard",
-                          plan_kw=dict(tile_path=1, tile_density_milli=300, pack_rows=1))
+                          plan_kw=dict(tile_path=1, tile_density_milli=300, tile_pool_density_milli=0, pack_rows=1))
     st = plan.stats()
     assert 0 < st["tile_windows"] < st["windows"] and st["pack_rows"] == 1
 

@@ -28,7 +28,7 @@ def _run(g, H, dtype, plan_kw, seed=7):
 
 def test_tile_small_batched_dense():
     g = graphgen.batched_dense(num_graphs=24, seed=3)
-    plan, _, _ = _run(g, 8, "bf16", dict(tile_path=1, tile_density_milli=150))
+    plan, _, _ = _run(g, 8, "bf16", dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0))
     st = plan.stats()
     assert st["tile_path"] == 1 and st["tile_windows"] > 0
 
@@ -37,7 +37,7 @@ def test_full_batched_dense_on_tile_path():
     """The batched dense-ish workload at full size with its windows on the tile path."""
     g, vals, w = graphgen.make_workload("batched_dense", "full")
     plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant,
-                          plan_kw=dict(tile_path=1, tile_density_milli=150))
+                          plan_kw=dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0))
     plan.check()
     assert plan.stats()["tile_windows"] > 0.8 * plan.stats()["windows"]
 
@@ -49,7 +49,7 @@ def test_tile_matches_core_path(dtype):
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 4, 64, False, seed=9)
     t = {k: v.to(device()) for k, v in cast_values(vals, dtype).items()}
     rp, ci = upload_graph(g)
-    tile = g3s.Plan(rp, ci, g.num_nodes, 4, 64, dtype, tile_path=1, tile_density_milli=0)
+    tile = g3s.Plan(rp, ci, g.num_nodes, 4, 64, dtype, tile_path=1, tile_density_milli=0, tile_pool_density_milli=0)
     core = g3s.Plan(rp, ci, g.num_nodes, 4, 64, dtype, tile_path=0)
     assert tile.stats()["tile_windows"] == (g.num_nodes + 15) // 16  # every window dense enough
     assert core.stats()["tile_windows"] == 0
@@ -70,7 +70,7 @@ def test_tile_mixed_with_core_rows():
     rp = np.concatenate([a.row_ptr, a.row_ptr[-1] + b.row_ptr[1:]]).astype(np.int32)
     col = np.concatenate([a.col_idx, b.col_idx + off]).astype(np.int32)
     g = graphgen.Graph(rp, col)
-    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=150, heavy_threshold=60, chunk_edges=25))
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0, heavy_threshold=60, chunk_edges=25))
     st = plan.stats()
     assert 0 < st["tile_windows"] < st["windows"] and st["chunks"] > 0
 
@@ -92,7 +92,7 @@ def test_tile_full_windows():
     rp = np.zeros(n + 1, np.int32)
     rp[1:] = np.cumsum(deg)
     g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
-    plan, _, _ = _run(g, 2, "f16", dict(tile_path=1, tile_density_milli=0, heavy_threshold=512))
+    plan, _, _ = _run(g, 2, "f16", dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0, heavy_threshold=512))
     st = plan.stats()
     assert st["tile_windows"] == (n + 15) // 16
     assert st["tiles"] >= 15 * st["tile_windows"]
@@ -115,7 +115,7 @@ def test_tile_windows_over_the_limit_stay_on_core():
     rp = np.concatenate([rp, np.full(nn - n, rp[-1], np.int32)])
     g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
     vals = graphgen.make_values(nn, g.num_edges, 2, 64, False, seed=15)
-    plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard", plan_kw=dict(tile_path=1, tile_density_milli=0))
+    plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard", plan_kw=dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))
     plan.check()
     flags = plan.export("win_flags")
     assert not (flags[0] & 2) and all(flags[1:6] & 2)
@@ -143,14 +143,14 @@ def test_tile_wide_logit_range():
     vals["K"] = np.abs(vals["K"] * ramp)
     vals["Q"] = np.abs(vals["Q"]) * 2.0
     plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard",
-                          plan_kw=dict(tile_path=1, tile_density_milli=0, heavy_threshold=512))
+                          plan_kw=dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0, heavy_threshold=512))
     plan.check()
     assert plan.stats()["tile_windows"] == 8
 
 
 def test_tile_multigraph_windows_stay_on_core():
     g = graphgen.random_csr(200, 30, seed=17, multigraph=True)
-    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=0))
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))
     flags = plan.export("win_flags")
     assert np.any(flags & 1)  # the multigraph has windows with repeated edges
     assert not np.any(((flags & 1) != 0) & ((flags & 2) != 0))  # none of them takes the tile path
@@ -158,7 +158,7 @@ def test_tile_multigraph_windows_stay_on_core():
 
 def test_tile_sixteen_bit_output():
     g = graphgen.batched_dense(num_graphs=16, seed=19)
-    plan, O, _ = _run(g, 8, "bf16", dict(tile_path=1, out_dtype="bf16", tile_density_milli=150))
+    plan, O, _ = _run(g, 8, "bf16", dict(tile_path=1, out_dtype="bf16", tile_density_milli=150, tile_pool_density_milli=0))
     assert O.dtype == torch.bfloat16 and plan.stats()["tile_windows"] > 0
 
 
@@ -171,15 +171,16 @@ def test_tile_rows_with_no_edges():
     rp = np.zeros(n + 1, np.int32)
     rp[1:] = np.cumsum(deg)
     g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
-    plan, O, _ = _run(g, 1, "bf16", dict(tile_path=1, tile_density_milli=0))
+    plan, O, _ = _run(g, 1, "bf16", dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))
     assert plan.stats()["tile_windows"] == 4
     assert torch.count_nonzero(O[[3, 17, 18, 40]]).item() == 0
 
 
 @pytest.mark.parametrize("H", [1, 8])
 def test_tile_mixed_full_size_persistent_core_rows(H):
-    """Full-size batched graphs with p = 0.5: about 60% of the windows on
-    tiles and the rest left to the CUDA-core kernel's window list, with more
+    """Full-size batched graphs with p = 0.5 and a per-window density cutoff
+    of 0.4: about 60% of the windows on tiles and the rest left to the
+    CUDA-core kernel's window list (both kernels in one forward), with more
     of those rows than resident warps (its persistent loop).  H = 1 also
     takes the short-row pack flavour beside the tile windows.  Sampled rows
     and both ends are checked."""
@@ -187,7 +188,9 @@ def test_tile_mixed_full_size_persistent_core_rows(H):
     vals = graphgen.make_values(g.num_nodes, g.num_edges, H, 64, False, seed=2003)
     rows = np.unique(np.concatenate([np.random.default_rng(17).choice(g.num_nodes, 4000, replace=False),
                                      np.arange(16), g.num_nodes - 1 - np.arange(16)]))
-    plan, _, _ = run_case(g, vals, H, 64, "bf16", "standard", rows=rows, plan_kw=dict(pack_rows=1 if H == 1 else -1))
+    plan, _, _ = run_case(g, vals, H, 64, "bf16", "standard", rows=rows,
+                          plan_kw=dict(pack_rows=1 if H == 1 else -1, tile_density_milli=400,
+                                       tile_pool_density_milli=0))
     plan.check()
     st = plan.stats()
     core_rows = 16 * (st["windows"] - st["tile_windows"])
@@ -206,21 +209,27 @@ def _mixed_graph():
 
 
 def _selection_cases():
+    """(name, graph, heads, plan options, whether windows take the tile path)"""
     dense_full = lambda: graphgen.make_workload("batched_dense", "full")[0]  # noqa: E731
     complete_small = lambda: graphgen.make_workload("batched_complete", "small")[0]  # noqa: E731
-    yield "batched_dense_full_default", dense_full, 8, {}
-    yield "batched_dense_full_150", dense_full, 8, dict(tile_density_milli=150)
-    yield "batched_dense_full_150_global_bitmap", dense_full, 8, dict(tile_density_milli=150, bsb_smem_edges=64)
-    yield "batched_complete_small", complete_small, 8, {}
-    yield "batched_complete_small_global_bitmap", complete_small, 8, dict(bsb_smem_edges=100)
-    yield "mixed_heavy", _mixed_graph, 2, dict(tile_density_milli=150, heavy_threshold=60, chunk_edges=25)
-    yield "mixed_heavy_global_bitmap", _mixed_graph, 2, dict(tile_density_milli=150, heavy_threshold=60,
-                                                              chunk_edges=25, bsb_smem_edges=48)
-    yield "mixed_max_tiles", _mixed_graph, 2, dict(tile_density_milli=0, tile_max_tiles=5)
+    per_window = dict(tile_density_milli=150, tile_pool_density_milli=0)
+    yield "batched_dense_full_default", dense_full, 8, {}, False  # pooled density 0.24 < 0.3
+    yield "batched_dense_full_pool_200", dense_full, 8, dict(tile_pool_density_milli=200), True
+    yield "batched_dense_full_per_window", dense_full, 8, per_window, True
+    yield "batched_dense_full_per_window_global_bitmap", dense_full, 8, dict(per_window, bsb_smem_edges=64), True
+    yield "batched_complete_small", complete_small, 8, {}, True
+    yield "batched_complete_small_global_bitmap", complete_small, 8, dict(bsb_smem_edges=100), True
+    yield "mixed_heavy", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25), True
+    yield "mixed_heavy_pooled_out", _mixed_graph, 2, dict(tile_pool_density_milli=500, heavy_threshold=60,
+                                                         chunk_edges=25), False
+    yield "mixed_heavy_global_bitmap", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25,
+                                                            bsb_smem_edges=48), True
+    yield "mixed_max_tiles", _mixed_graph, 2, dict(tile_density_milli=0, tile_pool_density_milli=0,
+                                                   tile_max_tiles=5), True
 
 
-@pytest.mark.parametrize("name,make,H,kw", list(_selection_cases()), ids=[c[0] for c in _selection_cases()])
-def test_tile_selection_bit_exact(name, make, H, kw):
+@pytest.mark.parametrize("name,make,H,kw,tiled", list(_selection_cases()), ids=[c[0] for c in _selection_cases()])
+def test_tile_selection_bit_exact(name, make, H, kw, tiled):
     """With the tile path on, the device planner's BSB arrays, window flags
     (bit 1 = tile path), the tile-path window list and the list of windows
     left to the CUDA-core kernel equal the reference planner's, through both
@@ -233,7 +242,8 @@ def test_tile_selection_bit_exact(name, make, H, kw):
     opts = g3s.make_options(tile_path=1, **kw)
     b = ref_planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
     sel = ref_planner.tile_selection(g.row_ptr, b, True, heavy_threshold=st["heavy_threshold"],
-                                     max_tiles=opts.tile_max_tiles, density_milli=opts.tile_density_milli)
+                                     max_tiles=opts.tile_max_tiles, density_milli=opts.tile_density_milli,
+                                     pool_milli=opts.tile_pool_density_milli)
     ref = dict(b, **sel)
     for arr in ("win_tile_ptr", "tile_cols", "tile_bits", "win_nnz", "win_flags", "tile_windows", "core_windows"):
         got = plan.export(arr)
@@ -247,7 +257,6 @@ def test_tile_selection_bit_exact(name, make, H, kw):
     assert got_items.shape == want_items.shape and np.array_equal(got_items, want_items), "tile_items"
     if "bsb_smem_edges" in kw:
         assert st["large_windows"] > 0
-    if name != "batched_dense_full_default":
-        assert st["tile_windows"] > 0
-    if name.startswith("mixed"):
+    assert (st["tile_windows"] > 0) == tiled
+    if name.startswith("mixed") and tiled:
         assert 0 < st["tile_windows"] < st["windows"]

@@ -20,7 +20,7 @@ def test_bounded_wait_times_out_and_context_survives():
     ensure_built()
     g, vals, w = graphgen.make_workload("batched_dense", "small")
     plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant,
-                          plan_kw=dict(tile_path=1, tile_density_milli=150))
+                          plan_kw=dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0))
     lib = g3s.load_library()
     stream = torch.cuda.current_stream().cuda_stream
     t0 = time.perf_counter()
@@ -29,4 +29,4 @@ def test_bounded_wait_times_out_and_context_survives():
     assert st == 6, lib.g3s_last_error()  # G3S_ERR_TIMEOUT
     assert 0.04 < dt < 5.0
     plan.check()  # the flag was cleared
-    run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, plan_kw=dict(tile_path=1, tile_density_milli=150))
+    run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, plan_kw=dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0))

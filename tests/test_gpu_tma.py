@@ -97,7 +97,7 @@ def test_tma_with_tile_windows():
     g = graphgen.batched_dense(num_graphs=40, min_nodes=20, max_nodes=60, seed=21)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 2, 64, False, seed=22)
     plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard",
-                          plan_kw=dict(tile_path=1, tile_density_milli=300, tma_gather=1))
+                          plan_kw=dict(tile_path=1, tile_density_milli=300, tile_pool_density_milli=0, tma_gather=1))
     st = plan.stats()
     assert st["tma_gather"] == 1 and 0 < st["tile_windows"] < st["windows"]
 

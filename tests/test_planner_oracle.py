@@ -126,19 +126,26 @@ def test_heavy_chunks_cover_rows():
 def test_tile_selection_brute_force():
     g = graphgen.batched_dense(num_graphs=12, seed=11)
     b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
-    sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=40, max_tiles=6, density_milli=200)
     deg = g.degrees()
     W = b["win_nnz"].size
+    elig = []
     for w in range(W):
         nt = b["win_tile_ptr"][w + 1] - b["win_tile_ptr"][w]
         md = deg[16 * w:16 * w + 16].max()
-        ok = (not b["win_dup"][w]) and 1 <= nt <= 6 and md <= 40 and b["win_nnz"][w] / (128.0 * nt) >= 0.2
-        assert bool(sel["win_flags"][w] & planner.FLAG_TILE) == ok
-    assert np.array_equal(sel["tile_windows"], np.flatnonzero(sel["win_flags"] & planner.FLAG_TILE))
-    # every window is on exactly one of the two lists, each ascending
-    tile, core = list(sel["tile_windows"]), list(sel["core_windows"])
-    assert sorted(tile + core) == list(range(W)) and tile == sorted(tile) and core == sorted(core)
-    assert 0 < len(tile) < W
+        elig.append((not b["win_dup"][w]) and 1 <= nt <= 6 and md <= 40 and b["win_nnz"][w] / (128.0 * nt) >= 0.2)
+    nt = np.diff(b["win_tile_ptr"])
+    pooled = b["win_nnz"][elig].sum() / (128.0 * nt[elig].sum())
+    assert 0 < sum(elig) < W and 0.2 < pooled < 0.9
+    for pool_milli, take in ((0, True), (int(1000 * pooled) - 1, True), (int(1000 * pooled) + 1, False)):
+        sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=40, max_tiles=6, density_milli=200,
+                                     pool_milli=pool_milli)
+        for w in range(W):
+            assert bool(sel["win_flags"][w] & planner.FLAG_TILE) == (elig[w] and take)
+        assert np.array_equal(sel["tile_windows"], np.flatnonzero(sel["win_flags"] & planner.FLAG_TILE))
+        # every window is on exactly one of the two lists, each ascending
+        tile, core = list(sel["tile_windows"]), list(sel["core_windows"])
+        assert sorted(tile + core) == list(range(W)) and tile == sorted(tile) and core == sorted(core)
+        assert (0 < len(tile) < W) == take
 
 
 def test_tile_items_pairing():
