@@ -411,8 +411,6 @@ def parse_args():
     ap.add_argument("--aggregate", action="store_true",
                     help="also time g3s_aggregate (normalised weighted aggregation) on the workload's graph; "
                          "adds an 'aggregate' object")
-    ap.add_argument("--tma-gather", type=int, default=None, choices=[0, 1],
-                    help="feed the CUDA-core kernel through TMA gathers (default: the library's)")
     ap.add_argument("--pack-rows", type=int, default=None, choices=[0, 1],
                     help="short-row packs, one row per lane group (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -609,8 +607,6 @@ def main():
         plan_kw["tile_density_milli"] = args.tile_density_milli
     if args.tile_pool_density_milli is not None:
         plan_kw["tile_pool_density_milli"] = args.tile_pool_density_milli
-    if args.tma_gather is not None:
-        plan_kw["tma_gather"] = args.tma_gather
     if args.pack_rows is not None:
         plan_kw["pack_rows"] = args.pack_rows
     plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)
@@ -805,7 +801,7 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks, "plan_ms": plan_ms, "layer": layer,
             "aggregate": aggregate, "workloads": workloads,
-            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"], "tma_gather": st["tma_gather"],
+            "plan": {"heavy_rows": st["heavy_rows"], "chunks": st["chunks"],
                      "heavy_threshold": st["heavy_threshold"], "pack_rows": st["pack_rows"],
                      "tile_windows": st["tile_windows"],
                      "tiles": st["tiles"], "tile_window_nnz": st["tile_window_nnz"]},

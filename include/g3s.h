@@ -116,13 +116,12 @@ typedef enum g3s_variant {
  *  out_dtype       element type of O and Eout: G3S_F32 (default) or the input
  *                  dtype.  fp32 keeps the fp32 accumulation; a 16-bit store adds
  *                  up to one half-ulp of rounding (2^-8 relative for bf16)
- *  tma_gather      1: where supported (standard form, fp16/bf16 inputs,
- *                  H*d*2 = 128, 256 or 512 bytes per node row) the CUDA-core
- *                  kernel receives its K and V rows through TMA gathers into a
- *                  per-warp shared-memory ring; 0 (default): plain global
- *                  loads.  Both compute the same arithmetic in the same order.
- *                  The ring costs resident warps (shared memory, registers),
- *                  and on the measured workloads the plain loads are faster.
+ *  degree_buckets  1: also list the rows of each degree bucket (ascending
+ *                  id), readable with g3s_plan_export; 0 (default): only
+ *                  count them (stats.bucket_count).  No forward kernel reads
+ *                  the lists: rows run in id order, so neighbouring rows'
+ *                  sources meet in L2, heavy rows as chunks taken first, short
+ *                  rows in packs; the lists cost five stable scans of N rows
  *  pack_rows       short-row packs, where a node row is at most 256 bytes
  *                  (G = 32 * 16 / row bytes >= 2 lane groups per warp): a warp
  *                  takes G consecutive rows together, one per lane group,
@@ -148,15 +147,14 @@ typedef struct g3s_plan_options {
     float rtm_epsilon;
     int32_t validate_graph;
     int32_t out_dtype;
-    int32_t tma_gather;
     int32_t pack_rows;
     int32_t tile_pool_density_milli;
+    int32_t degree_buckets;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {
     int64_t num_nodes, num_edges;
     int32_t heads, head_dim, dtype, variant, out_dtype;
-    int32_t tma_gather; /* 1 when forward feeds the CUDA-core kernel through TMA gathers */
     int64_t bucket_count[G3S_NUM_BUCKETS];
     int64_t heavy_rows, chunks;
     int32_t has_bsb, tile_path;
@@ -175,7 +173,7 @@ typedef struct g3s_plan_stats {
 /* Planner arrays readable with g3s_plan_export (all int32 unless noted). */
 typedef enum g3s_plan_array {
     G3S_ARR_BUCKET_PTR = 0,      /* [G3S_NUM_BUCKETS+1] scan of bucket sizes */
-    G3S_ARR_BUCKET_ROWS = 1,     /* [N] rows by bucket, ascending id inside */
+    G3S_ARR_BUCKET_ROWS = 1,     /* [N] rows by bucket, ascending id inside (degree_buckets = 1) */
     G3S_ARR_HEAVY_ROWS = 2,      /* [heavy_rows] ascending */
     G3S_ARR_HEAVY_CHUNK_PTR = 3, /* [heavy_rows+1] */
     G3S_ARR_CHUNKS = 4,          /* [chunks][3] (row, e_begin, e_end) */
@@ -197,7 +195,8 @@ typedef enum g3s_plan_array {
 
 typedef struct g3s_plan g3s_plan; /* opaque */
 
-/* Library version string, e.g. "g3s 0.1 sm_103a". Never NULL. */
+/* Library version string, e.g. "g3s 0.1 sm_103a". Never NULL.
+ * (No counterpart on the pages: library plumbing, as are the next three.) */
 const char *g3s_version(void);
 
 /* Name of a status code. Never NULL. */
@@ -212,6 +211,9 @@ void g3s_plan_options_init(g3s_plan_options *opts);
 /*
  * Upper bound of the workspace bytes a plan for these sizes needs, for any
  * graph with N nodes and E edges.  opts may be NULL (defaults).
+ * No counterpart on the pages: every device array belongs to the caller here
+ * (the Triton article's "Conclusions": allocation on the host side costs more
+ * than the kernels), so the caller asks for the size first.
  * INVALID_ARG for negative sizes or a NULL *bytes; UNSUPPORTED for shapes
  * without a kernel.
  */
@@ -222,6 +224,14 @@ g3s_status g3s_plan_workspace_size(int64_t num_nodes, int64_t num_edges, int hea
 /*
  * Build a plan for one graph on the current CUDA device (the degree
  * buckets, heavy-row chunks and BSB tiles, all on the device).
+ * Sources: the BSB tiles are the Fused3S row-window compaction
+ * (sciencestack.ai/paper/2505.08098, Figure 1: a 16-row window compacted to
+ * its unique columns, tiled into 16x8 blocks with bitmaps); the per-node
+ * index ranges the CUDA-core kernel walks are the Triton article's CSC lookup
+ * (stondelli.it/articles/gattn-triton, "Using the CSC index for fast edge
+ * lookup"); the degree buckets and heavy-row chunks are this library's
+ * scheduling (the pages have no counterpart; Fused3S Figure 2 shows blocks
+ * sharing a row's work, which the chunks restate for heavy rows).
  *   row_ptr_d, col_idx_d  device CSR arrays; must outlive the plan
  *   workspace_d           device memory of workspace_bytes, 256-byte aligned,
  *                         owned by the caller, must outlive the plan
@@ -258,11 +268,12 @@ g3s_status g3s_plan_create(const int32_t *row_ptr_d, const int32_t *col_idx_d, i
 g3s_status g3s_plan_set_edge_ids(g3s_plan *plan, const int32_t *edge_id_d, int64_t num_edge_slots,
                                  g3s_stream_t stream);
 
-/* Sizes and counts of a plan. */
+/* Sizes and counts of a plan.  (No counterpart on the pages.) */
 g3s_status g3s_plan_get_stats(const g3s_plan *plan, g3s_plan_stats *stats);
 
 /*
- * Copy one planner array to host memory.  bytes_needed (may be NULL)
+ * Copy one planner array to host memory (no counterpart on the pages: it lets
+ * tests compare the device planner bit for bit).  bytes_needed (may be NULL)
  * receives its size; host_dst may be NULL to query only.  Otherwise bytes
  * must be at least that size.  Synchronous (blocks on the plan's stream).
  * UNSUPPORTED for BSB arrays of a plan built without BSB.
@@ -271,7 +282,12 @@ g3s_status g3s_plan_export(const g3s_plan *plan, g3s_plan_array which, void *hos
                            size_t *bytes_needed);
 
 /*
- * One fused forward pass over the whole graph, enqueued on `stream`.
+ * One fused forward pass over the whole graph, enqueued on `stream`: SDDMM,
+ * row softmax and SpMM in one pass with nothing of S written to memory (the
+ * Fused3S abstract and TL;DR, sciencestack.ai/paper/2505.08098), and for the
+ * RTMScore variant the fused kernel of the Triton article
+ * (stondelli.it/articles/gattn-triton, "Fusing the full graph attention"),
+ * whose outputs are the node features and the updated edge features.
  *   Q, K, V  device [N][H][d] inputs
  *   Eproj    device [E][H][d] edge projections; RTMScore only, else NULL
  *            ([slots][H][d] in physical edge order after g3s_plan_set_edge_ids)
@@ -327,7 +343,9 @@ g3s_status g3s_linear(const void *X, const void *W, int64_t M, int Kin, int Nout
                       void *const *Y, int seg_cols, g3s_dtype out_dtype, int32_t *status_d, g3s_stream_t stream);
 
 /*
- * One attention layer on the plan's graph: Q | K | V = X Wqkv^T with
+ * One attention layer on the plan's graph (the Triton article's closing
+ * remark on the projections around the fused attention; the Fused3S abstract's
+ * Graph Transformer layer; the layout is this library's): Q | K | V = X Wqkv^T with
  * g3s_linear (Wqkv is (3 H d, Kin), rows for Q, then K, then V), then
  * g3s_forward.  For an RTMScore plan also Eproj = Xe We^T (Xe (edge slots,
  * Ke), We (H d, Ke)) feeds the edge term; NULL Xe/We on a standard plan.
@@ -342,12 +360,15 @@ g3s_status g3s_layer_forward(const g3s_plan *plan, const void *X, const void *Wq
                              g3s_stream_t stream);
 
 /*
+ * (No counterpart on the pages, as g3s_forward_host.)
  * Bytes of device staging g3s_forward_host needs for this plan: room for
  * Q, K, V, O (and Eproj, Eout for RTMScore), each 256-byte aligned.
  */
 g3s_status g3s_host_staging_size(const g3s_plan *plan, size_t *bytes);
 
 /*
+ * No counterpart on the pages: a convenience for callers whose features live
+ * in host memory.
  * g3s_forward on HOST buffers: copies Q, K, V (and Eproj) host->device into
  * the caller's device staging area, runs the forward pass, and copies O (and
  * Eout when non-NULL) device->host, all enqueued on `stream` (one
@@ -359,6 +380,7 @@ g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K
                             size_t staging_bytes, g3s_stream_t stream);
 
 /*
+ * (No counterpart on the pages: error reporting of the bounded device waits.)
  * Synchronise `stream` and report whether a kernel of an earlier g3s_forward
  * on this plan gave up a bounded device-side wait (the tensor-core tile
  * kernel waits on its MMAs for at most about one second).  Returns
@@ -368,6 +390,7 @@ g3s_status g3s_forward_host(const g3s_plan *plan, const void *Q_h, const void *K
 g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
 
 /*
+ * (No counterpart on the pages.)
  * Self-test of the device-side timeout path: launches one CTA that waits, with
  * the same bounded wait the tile kernel uses, on an mbarrier that nothing ever
  * completes; after limit_ns (at most 2 s) it gives up and sets the plan's
@@ -376,7 +399,8 @@ g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
  */
 g3s_status g3s_selftest_wait_timeout(const g3s_plan *plan, uint64_t limit_ns, g3s_stream_t stream);
 
-/* Release the plan's host struct, stream and events (the caller still owns the workspace). NULL is a no-op. */
+/* Release the plan's host struct, stream and events (the caller still owns the workspace). NULL is a no-op.
+ * (No counterpart on the pages.) */
 void g3s_plan_destroy(g3s_plan *plan);
 
 /*

@@ -64,9 +64,9 @@ class PlanOptions(ctypes.Structure):
         ("rtm_epsilon", ctypes.c_float),
         ("validate_graph", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32),
-        ("tma_gather", ctypes.c_int32),
         ("pack_rows", ctypes.c_int32),
         ("tile_pool_density_milli", ctypes.c_int32),
+        ("degree_buckets", ctypes.c_int32),
     ]
 
 
@@ -75,7 +75,7 @@ class PlanStats(ctypes.Structure):
         ("num_nodes", ctypes.c_int64), ("num_edges", ctypes.c_int64),
         ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("variant", ctypes.c_int32),
-        ("out_dtype", ctypes.c_int32), ("tma_gather", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
         ("bucket_count", ctypes.c_int64 * NUM_BUCKETS),
         ("heavy_rows", ctypes.c_int64), ("chunks", ctypes.c_int64),
         ("has_bsb", ctypes.c_int32), ("tile_path", ctypes.c_int32),

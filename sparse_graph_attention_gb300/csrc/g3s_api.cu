@@ -72,8 +72,8 @@ void default_options(g3s_plan_options* o) {
     o->rtm_epsilon = 1e-6f;
     o->validate_graph = 1;
     o->out_dtype = G3S_F32;
-    o->tma_gather = 0;
     o->pack_rows = -1;
+    o->degree_buckets = 0;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -108,8 +108,8 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (!(o.rtm_epsilon >= 0.f)) return fail(G3S_ERR_INVALID_ARG, "rtm_epsilon must be >= 0");
     if (o.out_dtype != G3S_F32 && o.out_dtype != dtype)
         return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
-    if (o.tma_gather != 0 && o.tma_gather != 1) return fail(G3S_ERR_INVALID_ARG, "tma_gather must be 0 or 1");
     if (o.pack_rows < -1 || o.pack_rows > 1) return fail(G3S_ERR_INVALID_ARG, "pack_rows takes -1, 0 or 1");
+    if (o.degree_buckets != 0 && o.degree_buckets != 1) return fail(G3S_ERR_INVALID_ARG, "degree_buckets takes 0 or 1");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -131,6 +131,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->chunk_edges = o.chunk_edges;
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
+    s->bucket_lists = o.degree_buckets == 1;
     s->tile_density_milli = o.tile_density_milli;
     s->tile_pool_milli = o.tile_pool_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
@@ -158,9 +159,9 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     a->work_counter = c.take<unsigned long long>(1);
     a->tile_counter = c.take<unsigned int>(1);
     a->fwd_status = c.take<int32_t>(1);
-    a->bucket_of = c.take<uint8_t>(s.N);
+    a->bucket_of = s.bucket_lists ? c.take<uint8_t>(s.N) : nullptr;
     a->bucket_ptr = c.take<int32_t>(G3S_NUM_BUCKETS + 1);
-    a->bucket_rows = c.take<int32_t>(s.N);
+    a->bucket_rows = s.bucket_lists ? c.take<int32_t>(s.N) : nullptr;
     a->heavy_rows = c.take<int32_t>(s.max_heavy);
     a->heavy_chunk_ptr = c.take<int32_t>(s.max_heavy + 1);
     a->heavy_index = c.take<int32_t>(s.N);
@@ -346,10 +347,6 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->dtype = p->dtype;
     st->variant = p->variant;
     st->out_dtype = p->opts.out_dtype;
-    st->tma_gather = (p->opts.tma_gather && core_tma_supported(p->dtype, p->variant == G3S_RTMSCORE ? 1 : 0,
-                                                                p->shape.H * p->shape.D * dtype_size(p->dtype) / 16))
-                         ? 1
-                         : 0;
     for (int b = 0; b < G3S_NUM_BUCKETS; ++b) st->bucket_count[b] = p->counts.bucket_count[b];
     st->heavy_rows = p->counts.n_heavy;
     st->chunks = p->counts.n_chunks;
@@ -381,7 +378,11 @@ g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_d
     if (bsb_arr && !s.build_bsb) return fail(G3S_ERR_UNSUPPORTED, "plan was built without BSB tiles");
     switch (which) {
         case G3S_ARR_BUCKET_PTR: src = p->arr.bucket_ptr; n = 4 * (G3S_NUM_BUCKETS + 1); break;
-        case G3S_ARR_BUCKET_ROWS: src = p->arr.bucket_rows; n = 4 * (size_t)s.N; break;
+        case G3S_ARR_BUCKET_ROWS:
+            if (!s.bucket_lists) return fail(G3S_ERR_UNSUPPORTED, "plan was built without the bucket row lists");
+            src = p->arr.bucket_rows;
+            n = 4 * (size_t)s.N;
+            break;
         case G3S_ARR_HEAVY_ROWS: src = p->arr.heavy_rows; n = 4 * (size_t)c.n_heavy; break;
         case G3S_ARR_HEAVY_CHUNK_PTR: src = p->arr.heavy_chunk_ptr; n = 4 * ((size_t)c.n_heavy + 1); break;
         case G3S_ARR_CHUNKS: src = p->arr.chunks; n = 12 * (size_t)c.n_chunks; break;
@@ -481,14 +482,14 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         // then the tile kernel on the caller's stream; the two overlap
         CUDA_OR_FAIL(cudaEventRecord(p->ev_fork, stream), "cudaEventRecord(fork)");
         CUDA_OR_FAIL(cudaStreamWaitEvent(p->side, p->ev_fork, 0), "cudaStreamWaitEvent(fork)");
-        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, p->side),
+        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, p->side),
                      "fused kernel launch");
         CUDA_OR_FAIL(cudaEventRecord(p->ev_join, p->side), "cudaEventRecord(join)");
         CUDA_OR_FAIL(cudaMemsetAsync(p->arr.tile_counter, 0, sizeof(unsigned int), stream), "cudaMemsetAsync(tile queue)");
         CUDA_OR_FAIL(tile_launch(p->dtype, p->opts.out_dtype, tp, stream), "tile kernel launch");
         CUDA_OR_FAIL(cudaStreamWaitEvent(stream, p->ev_join, 0), "cudaStreamWaitEvent(join)");
     } else {
-        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, p->opts.tma_gather != 0, cp, stream),
+        CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream),
                      "fused kernel launch");
     }
     if (p->counts.n_chunks > 0) {
@@ -552,7 +553,7 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     cp.normalize = normalize ? 1 : 0;
     cp.status = p->arr.fwd_status;
     cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
-    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, false, cp, stream), "aggregation kernel launch");
+    CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, cp, stream), "aggregation kernel launch");
     if (p->counts.n_chunks > 0) {
         MergeParams mp{};
         mp.heavy_rows = p->arr.heavy_rows;

@@ -1,6 +1,6 @@
 // Dispatch of the fused CUDA-core kernel and the heavy-row merge by input and
-// output element type.  The kernels themselves are in g3s_core.cuh and
-// g3s_core_tma.cuh.
+// output element type (the kernels themselves are in g3s_core.cuh), and the
+// tensor-map encoder the projection GEMM's TMA copies use.
 #include <mutex>
 
 #include "g3s_internal.h"
@@ -31,32 +31,9 @@ EncodeTiledFn tensor_map_encoder() {
     return fn;
 }
 
-// The maps of the last K and V seen by this host thread (encoding is host
-// work of a few microseconds; repeated forwards on the same tensors reuse it).
-struct MapCache {
-    const void* K = nullptr;
-    const void* V = nullptr;
-    long long n = -1;
-    int row_vecs = 0;
-    CUtensorMap tk, tv;
-};
-thread_local MapCache map_cache;
-
 }  // namespace
 
 bool tensor_maps_available() { return tensor_map_encoder() != nullptr; }
-
-bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (enc == nullptr || rows < 1) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)box_elems, 1};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 bool encode_tile(CUtensorMap* m, const void* base, long long rows, int row_elems, int elem_bytes, int box_rows,
                  int box_elems) {
@@ -78,31 +55,9 @@ bool core_supported(int dtype, int row_vecs) {
     return true;
 }
 
-bool core_tma_supported(int dtype, int mode, int row_vecs) {
-    return mode == 0 && (dtype == 1 || dtype == 2) && (row_vecs == 8 || row_vecs == 16 || row_vecs == 32);
-}
-
-cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const CoreParams& p, cudaStream_t st) {
+cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st) {
     const bool out_f32 = out_dtype == 0;
     if (!out_f32 && out_dtype != dtype) return cudaErrorInvalidValue;
-    if (tma && p.N > 0 && p.status != nullptr && core_tma_supported(dtype, mode, p.row_vecs)) {
-        if (tensor_maps_available()) {
-            MapCache& c = map_cache;
-            if (c.K != p.K || c.V != p.V || c.n != p.N || c.row_vecs != p.row_vecs) {
-                c.K = nullptr;
-                // one node row per box: row_vecs * 8 16-bit elements
-                const int re = p.row_vecs * 8;
-                if (!encode_rows16(&c.tk, p.K, p.N, re, re, false) || !encode_rows16(&c.tv, p.V, p.N, re, re, false))
-                    return cudaErrorInvalidValue;
-                c.K = p.K;
-                c.V = p.V;
-                c.n = p.N;
-                c.row_vecs = p.row_vecs;
-            }
-            return dtype == 1 ? core_tma_launch_f16(out_f32, p, c.tk, c.tv, st)
-                              : core_tma_launch_bf16(out_f32, p, c.tk, c.tv, st);
-        }
-    }
     if (p.pack_rows && mode != 1 && p.row_vecs <= 16) {  // the short-row pack flavour
         switch (dtype) {
             case 0: return core_launch_pack_f32(true, mode, p, st);

@@ -53,9 +53,9 @@ struct PlanCounts {
 
 // Device views the planner writes into (all inside the caller's workspace).
 struct PlanArrays {
-    uint8_t* bucket_of;        // [N]
+    uint8_t* bucket_of;        // [N] (with the bucket lists only)
     int32_t* bucket_ptr;       // [NB+1]
-    int32_t* bucket_rows;      // [N]
+    int32_t* bucket_rows;      // [N] (with the bucket lists only)
     int32_t* heavy_rows;       // [max_heavy]
     int32_t* heavy_chunk_ptr;  // [max_heavy+1]
     int32_t* heavy_index;      // [N] scratch: heavy ordinal of a heavy row
@@ -91,7 +91,7 @@ struct PlanShape {
     int bounds[G3S_NUM_BUCKETS - 2];
     int bsb_smem_edges;
     int tile_density_milli, tile_max_tiles, tile_pool_milli;
-    bool build_bsb, tile_enabled;
+    bool build_bsb, tile_enabled, bucket_lists;
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
     int64_t scan_blocks;
     int pack_limit;  // most entries of a row a short-row pack takes (0: the row width does not pack)
@@ -177,12 +177,8 @@ struct MergeParams {
 // mode: 0 standard softmax, 1 RTMScore, 2 weighted aggregation.
 // Launchers return cudaErrorInvalidValue for shapes without a kernel.
 // Tensor maps for TMA, encoded through the driver entry point looked up at
-// run time (g3s_core.cu).  encode_rows16: a 2-D map over `rows` rows of
-// `row_elems` 16-bit elements (row stride row_elems * 2 bytes), box of
-// box_elems x 1 row (the shape tile::gather4 needs); swizzle128 selects the
-// 128-byte swizzle (box_elems * 2 must then be 128).
+// run time (g3s_core.cu).
 bool tensor_maps_available();
-bool encode_rows16(CUtensorMap* m, const void* base, long long rows, int row_elems, int box_elems, bool swizzle128);
 // A 2-D map over `rows` rows of `row_elems` elements of elem_bytes (2 or 4)
 // with a box of box_rows x box_elems and the 128-byte swizzle
 // (box_elems * elem_bytes == 128).
@@ -190,11 +186,7 @@ bool encode_tile(CUtensorMap* m, const void* base, long long rows, int row_elems
                  int box_elems);
 
 bool core_supported(int dtype, int row_vecs);
-// The TMA-fed form (g3s_core_tma.cuh): standard mode, 16-bit inputs, row_vecs 8, 16 or 32.
-bool core_tma_supported(int dtype, int mode, int row_vecs);
-// tma: use the TMA-fed form where core_tma_supported (and the driver offers
-// tensor-map encoding); otherwise the plain-load kernel.
-cudaError_t core_launch(int dtype, int out_dtype, int mode, bool tma, const CoreParams& p, cudaStream_t st);
+cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
@@ -206,10 +198,6 @@ cudaError_t core_launch_pack_bf16(bool out_f32, int mode, const CoreParams& p, c
 cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st);
-cudaError_t core_tma_launch_f16(bool out_f32, const CoreParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                cudaStream_t st);
-cudaError_t core_tma_launch_bf16(bool out_f32, const CoreParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 cudaStream_t st);
 
 // ---- tensor-core tile kernel (g3s_tile.cu) -------------------------------
 struct TileParams {

@@ -146,7 +146,7 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     cp.elementwise_clamp = o.rtm_elementwise_clamp ? 1 : 0;
     cp.status = a.fwd_status;
     cp.pack_rows = use_packs(o.pack_rows, s, hc) ? 1 : 0;
-    NOALLOC_CUDA(core_launch(dtype, o.out_dtype, rtm, o.tma_gather != 0, cp, stream), "fused kernel launch");
+    NOALLOC_CUDA(core_launch(dtype, o.out_dtype, rtm, cp, stream), "fused kernel launch");
     if (hc.n_chunks > 0) {
         MergeParams mp{};
         mp.heavy_rows = a.heavy_rows;

@@ -191,7 +191,7 @@ __global__ void k_bucket_classify(const int32_t* row_ptr, long long N, Bounds bd
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += (long long)gridDim.x * blockDim.x) {
         const int d = row_ptr[i + 1] - row_ptr[i];
         const int b = bucket_of_degree(d, bd);
-        bucket_of[i] = (uint8_t)b;
+        if (bucket_of != nullptr) bucket_of[i] = (uint8_t)b;
         atomicAdd(&cnt[b], 1);
         if (short_limit > 0 && d <= short_limit) atomicAdd(&cnt[G3S_NUM_BUCKETS], 1);
     }
@@ -688,7 +688,9 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
     }
     k_bucket_ptr<<<1, 32, 0, st>>>(c, a.bucket_ptr);
     G3S_TRY(cudaGetLastError());
-    for (int b = 0; b < G3S_NUM_BUCKETS; ++b)
+    // the per-bucket row lists (five stable scans) only on request: no forward
+    // kernel reads them (rows run in id order, heavy rows as chunks)
+    for (int b = 0; s.bucket_lists && b < G3S_NUM_BUCKETS; ++b)
         G3S_TRY(scan(BucketFlag{a.bucket_of, b}, BucketOut{a.bucket_ptr, a.bucket_rows, b}, s.N, a.scan_blocks,
                      nullptr, st));
 

@@ -1,5 +1,5 @@
 // Inline-PTX wrappers shared by the kernels (sm_100 family): mbarriers with
-// bounded waits, cp.async, TMA tiles and gathers, bulk groups, and tcgen05
+// bounded waits, cp.async, TMA tiles, bulk groups, and tcgen05
 // (tensor memory, the kind::f16 MMA, descriptors).
 #pragma once
 #include <cuda.h>  // CUtensorMap (the type only; no driver call is linked)
@@ -72,19 +72,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     while (!mbar_try_wait(bar, parity))
         if (globaltimer() - t0 > limit_ns) return false;
     return true;
-}
-
-// TMA gather of four rows (row indices r0..r3, starting at element column x,
-// which must be a multiple of 16 bytes) of a 2-D tensor map whose box is one
-// row high, into consecutive rows of shared memory at dst; completion is
-// counted on the mbarrier in bytes.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int r0, int r1, int r2, int r3,
-                                            uint32_t bar, int x = 0) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
 }
 
 // One arrival on the mbarrier (release at CTA scope).

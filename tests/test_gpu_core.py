@@ -192,7 +192,7 @@ def _planner_graphs():
 def test_planner_bit_exact(name, g, kw):
     ensure_built()
     rp, ci = upload_graph(g)
-    opts = dict(bsb=1, heavy_threshold=64, chunk_edges=32, bucket_bounds=(4, 16, 128))
+    opts = dict(bsb=1, heavy_threshold=64, chunk_edges=32, bucket_bounds=(4, 16, 128), degree_buckets=1)
     opts.update(kw)
     plan = g3s.Plan(rp, ci, g.num_nodes, 2, 32, "bf16", **opts)
     ref = ref_planner.full_plan(g.row_ptr, g.col_idx, g.num_nodes, bounds=(4, 16, 128), heavy_threshold=64,
@@ -207,6 +207,24 @@ def test_planner_bit_exact(name, g, kw):
     assert st["dup_windows"] == int(ref["win_dup"].sum())
     if "bsb_smem_edges" in kw:
         assert st["large_windows"] > 0
+
+
+def test_bucket_counts_without_lists():
+    """Default plans count the rows of each degree bucket (stats and the
+    bucket offsets) but build the per-bucket row lists only on request."""
+    ensure_built()
+    g = graphgen.powerlaw(num_nodes=20000, seed=4)
+    rp, ci = upload_graph(g)
+    plan = g3s.Plan(rp, ci, g.num_nodes, 2, 32, "bf16", bucket_bounds=(4, 16, 128))
+    ref = ref_planner.degree_buckets(g.row_ptr, (4, 16, 128))
+    assert np.array_equal(plan.export("bucket_ptr"), ref["bucket_ptr"])
+    assert plan.stats()["bucket_count"] == list(np.diff(ref["bucket_ptr"]))
+    with pytest.raises(g3s.G3SError) as ei:
+        plan.export("bucket_rows")
+    assert ei.value.status == 2
+    a = g3s.workspace_size(g.num_nodes, g.num_edges, 2, 32, "bf16")
+    b = g3s.workspace_size(g.num_nodes, g.num_edges, 2, 32, "bf16", degree_buckets=1)
+    assert b >= a + 5 * g.num_nodes
 
 
 def test_planner_default_heavy_threshold():
@@ -282,17 +300,16 @@ def test_argument_errors():
                                ws.data_ptr(), 1024, s, ctypes.byref(out)) == 4
 
 
-@pytest.mark.parametrize("tma", [0, 1])
-def test_repeated_persistent_launches(tma):
+def test_repeated_persistent_launches():
     """Forwards and aggregations on one plan, back to back in the persistent
     launch form (the work queue reused): every repeat gives the first one's
-    bits, with the plain or the TMA-fed forward."""
+    bits."""
     ensure_built()
     g = graphgen.lognormal_local(num_nodes=120_000, radius=1024, seed=61)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 4, 32, False, seed=62)
     t = {k: v.to(device()) for k, v in cast_values(vals, "bf16").items()}
     rp, ci = upload_graph(g)
-    plan = g3s.Plan(rp, ci, g.num_nodes, 4, 32, "bf16", tma_gather=tma)
+    plan = g3s.Plan(rp, ci, g.num_nodes, 4, 32, "bf16")
     W = torch.ones(g.num_edges, 4, dtype=torch.bfloat16, device=device())
     first = plan.forward(t["Q"], t["K"], t["V"]).clone()
     agg0 = plan.aggregate(W, t["V"], normalize=True).clone()
