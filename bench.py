@@ -261,6 +261,42 @@ def oracle_timings(g, w, t, seconds_each: float):
 L2_FLUSH_BYTES = 256 << 20  # twice the L2 (126 MB): written between cold runs
 
 
+def gather_probe_rate(dev, footprint_bytes: int, row_bytes: int, runs: int = 7):
+    """GB/s at which random rows of row_bytes are read from an array of about
+    footprint_bytes (rounded down to a power-of-two row count; rows spread
+    uniformly by multiplicative hashing; eight 512-byte warp loads in flight per
+    warp, 32 warps per SM; g3s_gather_probe), median of `runs` timed launches
+    after two warm-ups.  With the footprint of a workload's K and V this is
+    the rate its gathers could be served at with no locality beyond the
+    footprint fitting (or not fitting) in L2."""
+    import torch
+
+    import sparse_graph_attention_gb300 as g3s
+    rows = 2
+    while rows * 2 * row_bytes <= footprint_bytes:
+        rows *= 2
+    src = torch.empty(rows * row_bytes // 4, dtype=torch.int32, device=dev)
+    src.random_(0, 1 << 30)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ctas = sms * 4
+    sink = torch.empty(ctas * 8, dtype=torch.int32, device=dev)
+    gathers = max(1, (512 << 20) // row_bytes)  # 512 MB per launch
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        g3s.gather_probe(src, row_bytes, gathers, ctas, sink)
+    times, n = [], 0
+    for _ in range(runs):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        n = g3s.gather_probe(src, row_bytes, gathers, ctas, sink)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    del src, sink
+    return n * row_bytes / (ms / 1e3) / 1e9
+
+
 def median_ms(step, runs: int, stream, flush=None):
     """Median over ``runs`` of one call's CUDA-event time on ``stream``; with
     ``flush`` (a device buffer larger than L2) it is overwritten before each
@@ -346,6 +382,18 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
                      "(outside the events) to evict L2; warm: back-to-back" % (runs, L2_FLUSH_BYTES >> 20),
            "plan": {"tile_windows": st["tile_windows"], "windows": st["windows"], "chunks": st["chunks"],
                     "pack_rows": st["pack_rows"], "heavy_threshold": st["heavy_threshold"]}}
+    # the gathers' own roofline: random rows of this row width over a footprint
+    # the size of K and V (L2-resident here unless noted)
+    row_bytes = w.heads * w.head_dim * ELT[w.dtype]
+    kv_bytes = 2 * g.num_nodes * row_bytes
+    probe = gather_probe_rate(dev, kv_bytes, row_bytes)
+    gathered_rows = 2.0 * g.num_edges * row_bytes
+    rec["gather_probe"] = {"row_bytes": row_bytes, "footprint_bytes": kv_bytes, "gbs": probe,
+                           "kv_gathers_gbs": gathered_rows / sec / 1e9,
+                           "kv_gathers_frac_of_probe": gathered_rows / sec / 1e9 / probe,
+                           "note": "K and V rows gathered per edge (the gathered model without CSR, Q, O, E) "
+                                   "against the rate of uniform random rows of the same width over the same "
+                                   "footprint"}
     prof = recorded_profile(name)
     if prof is not None:
         rec["dram_bytes"] = prof["dram_bytes_per_forward"]
@@ -417,6 +465,8 @@ def parse_args():
     ap.add_argument("--e2e-streams", type=int, default=3,
                     help="plans (each with its own staging) taking e2e steps in turn, one stream each")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gather-probe", action="store_true",
+                    help="only run the gather-rate probe over a range of footprints and row widths; print JSON")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the 'workloads' record (the other benchmark graphs, timed warm and cold)")
     ap.add_argument("--workload-runs", type=int, default=20, help="timed runs per workload (median)")
@@ -580,6 +630,17 @@ def main():
 
     import sparse_graph_attention_gb300 as g3s
 
+    if args.gather_probe:
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        res = []
+        for footprint in (16 << 20, 32 << 20, 64 << 20, 128 << 20, 256 << 20, 1 << 30):
+            for rb in (128, 256, 512, 1024):
+                res.append({"footprint_mb": footprint >> 20, "row_bytes": rb,
+                            "gbs": gather_probe_rate(dev, footprint, rb)})
+        print(json.dumps({"gather_probe": res}), flush=True)
+        return
+
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -695,6 +756,13 @@ def main():
     if prof is not None and "dominant_kernel" in prof:
         roofline["dominant_kernel"] = prof["dominant_kernel"]
         roofline["dominant_share"] = prof.get("dominant_share")
+    if not args.no_workloads:
+        rb = w.heads * w.head_dim * ELT[w.dtype]
+        rate = gather_probe_rate(dev, 2 * g.num_nodes * rb, rb)
+        roofline["random_row_gather_gbs"] = rate
+        roofline["random_row_gather_note"] = ("uniform random %d-byte rows over the %.2f GB K+V footprint "
+                                             "(g3s_gather_probe): the rate the 40%% non-local gathers can be "
+                                             "served at" % (rb, 2 * g.num_nodes * rb / 1e9))
 
     # ---- optional: a whole layer (projection on the tensor cores + forward) ----
     layer = None

@@ -399,6 +399,20 @@ g3s_status g3s_forward_check(const g3s_plan *plan, g3s_stream_t stream);
  */
 g3s_status g3s_selftest_wait_timeout(const g3s_plan *plan, uint64_t limit_ns, g3s_stream_t stream);
 
+/*
+ * Gather-rate probe (no counterpart on the pages: a measurement aid for the
+ * roofline of the CUDA-core kernel where K and V stay in L2).  Reads at least
+ * `gathers` rows of row_bytes each (a power of two in [16, 4096]) from src
+ * ([rows][row_bytes], 16-byte aligned, rows a power of two >= 2): the j-th row
+ * read is (j + 1) * 0x9E3779B97F4A7C15 >> (64 - log2 rows) (64-bit wrap-around
+ * product), spread uniformly over the rows.  `ctas` CTAs of 8 warps, eight
+ * 512-byte warp loads in flight per warp; what is read is XOR-ed into one word
+ * per warp of sink (ctas * 8 uint32).  *rows_read (may be NULL) receives the
+ * rows read (whole warp steps).  Enqueued on `stream`; time it with events.
+ */
+g3s_status g3s_gather_probe(const void *src, int64_t rows, int row_bytes, int64_t gathers, int ctas, uint32_t *sink,
+                            int64_t *rows_read, g3s_stream_t stream);
+
 /* Release the plan's host struct, stream and events (the caller still owns the workspace). NULL is a no-op.
  * (No counterpart on the pages.) */
 void g3s_plan_destroy(g3s_plan *plan);

@@ -96,7 +96,7 @@ EXPORTED = ["g3s_version", "g3s_status_string", "g3s_last_error", "g3s_plan_opti
             "g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
             "g3s_forward", "g3s_host_staging_size", "g3s_forward_host", "g3s_plan_destroy",
             "g3s_forward_noalloc", "g3s_forward_check", "g3s_aggregate", "g3s_selftest_wait_timeout",
-            "g3s_plan_set_edge_ids", "g3s_linear", "g3s_layer_forward"]
+            "g3s_plan_set_edge_ids", "g3s_linear", "g3s_layer_forward", "g3s_gather_probe"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -142,6 +142,8 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_linear.restype = I
         lib.g3s_layer_forward.argtypes = [P, P, P, I, P, P, I, P, P, P, P, P, P, P]
         lib.g3s_layer_forward.restype = I
+        lib.g3s_gather_probe.argtypes = [P, I64, I, I64, I, P, ctypes.POINTER(I64), P]
+        lib.g3s_gather_probe.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
             getattr(lib, name).restype = I
@@ -463,6 +465,21 @@ def linear(X, W, seg_cols: Optional[int] = None, out_dtype: Optional[str] = None
     return outs
 
 
+def gather_probe(src, row_bytes: int, gathers: int, ctas: int, sink, stream=None) -> int:
+    """``g3s_gather_probe``: read ``gathers`` (rounded up) hashed random rows of
+    ``row_bytes`` from the CUDA tensor ``src`` (a power-of-two number of rows);
+    returns the rows read.  A measurement aid (no attention arithmetic): the
+    rate at which the CUDA-core kernel's gathers can be served."""
+    lib = load_library()
+    nbytes = src.numel() * src.element_size()
+    if nbytes % row_bytes:
+        raise ValueError("src size must be a multiple of row_bytes")
+    got = ctypes.c_int64()
+    _check(lib.g3s_gather_probe(_dev_ptr(src, "src"), nbytes // row_bytes, int(row_bytes), int(gathers), int(ctas),
+                                _dev_ptr(sink, "sink"), ctypes.byref(got), _stream_handle(stream)))
+    return got.value
+
+
 def forward_noalloc(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant, Q, K, V, E=None, O=None,
                     Eout=None, stream=None):
     """``g3s_forward_noalloc``: plan + forward in one call using the library's
@@ -488,5 +505,5 @@ def forward_noalloc(row_ptr, col_idx, num_nodes, heads, head_dim, dtype, variant
     return (O, Eout) if Eout is not None else O
 
 
-__all__ = ["forward_noalloc", "linear", "Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
+__all__ = ["gather_probe", "forward_noalloc", "linear", "Plan", "G3SError", "load_library", "version", "workspace_size", "make_options", "default_options",
            "DTYPES", "VARIANTS", "ARRAYS", "EXPORTED", "LIB_PATH"]
