@@ -87,13 +87,18 @@ def _strip_comments(src: str) -> str:
     return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
+# sources outside g3s_forward's kernels (the gather-rate probe, the projection GEMM)
+NOT_FORWARD_SOURCES = ("g3s_probe.cu", "g3s_linear.cu")
+
+
 def kernel_sources_hash() -> str:
-    """Hash of the CUDA sources' code (comments and blank lines left out, so a
-    comment edit does not void a DRAM-traffic record of the same kernels)."""
+    """Hash of the code of the CUDA sources g3s_forward runs (comments and
+    blank lines left out, so a comment edit does not void a DRAM-traffic
+    record of the same kernels)."""
     csrc = os.path.join(ROOT, "sparse_graph_attention_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".h", ".cuh")):
+        if f.endswith((".cu", ".h", ".cuh")) and f not in NOT_FORWARD_SOURCES:
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(f.encode())
                 h.update(_strip_comments(fh.read()).encode())
@@ -261,14 +266,12 @@ def oracle_timings(g, w, t, seconds_each: float):
 L2_FLUSH_BYTES = 256 << 20  # twice the L2 (126 MB): written between cold runs
 
 
-def gather_probe_rate(dev, footprint_bytes: int, row_bytes: int, runs: int = 7):
+def gather_probe_rate(dev, footprint_bytes: int, row_bytes: int, runs: int = 7, plain_loads: bool = False):
     """GB/s at which random rows of row_bytes are read from an array of about
     footprint_bytes (rounded down to a power-of-two row count; rows spread
     uniformly by multiplicative hashing; eight 512-byte warp loads in flight per
-    warp, 32 warps per SM; g3s_gather_probe), median of `runs` timed launches
-    after two warm-ups.  With the footprint of a workload's K and V this is
-    the rate its gathers could be served at with no locality beyond the
-    footprint fitting (or not fitting) in L2."""
+    warp, 32 warps per SM; g3s_gather_probe through the read-only path or plain
+    loads), median of `runs` timed launches after two warm-ups."""
     import torch
 
     import sparse_graph_attention_gb300 as g3s
@@ -283,18 +286,26 @@ def gather_probe_rate(dev, footprint_bytes: int, row_bytes: int, runs: int = 7):
     gathers = max(1, (512 << 20) // row_bytes)  # 512 MB per launch
     stream = torch.cuda.current_stream(dev)
     for _ in range(2):
-        g3s.gather_probe(src, row_bytes, gathers, ctas, sink)
+        g3s.gather_probe(src, row_bytes, gathers, ctas, sink, plain_loads)
     times, n = [], 0
     for _ in range(runs):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        n = g3s.gather_probe(src, row_bytes, gathers, ctas, sink)
+        n = g3s.gather_probe(src, row_bytes, gathers, ctas, sink, plain_loads)
         b.record(stream)
         torch.cuda.synchronize(dev)
         times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     del src, sink
     return n * row_bytes / (ms / 1e3) / 1e9
+
+
+def gather_peak(dev, footprint_bytes: int, row_bytes: int) -> dict:
+    """The higher of the two probe paths' rates: the random-row gather roofline
+    of a footprint (the read-only path is the one the CUDA-core kernel uses)."""
+    ro = gather_probe_rate(dev, footprint_bytes, row_bytes)
+    pl = gather_probe_rate(dev, footprint_bytes, row_bytes, plain_loads=True)
+    return {"gbs": max(ro, pl), "read_only_gbs": ro, "plain_gbs": pl}
 
 
 def median_ms(step, runs: int, stream, flush=None):
@@ -386,9 +397,11 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
     # the size of K and V (L2-resident here unless noted)
     row_bytes = w.heads * w.head_dim * ELT[w.dtype]
     kv_bytes = 2 * g.num_nodes * row_bytes
-    probe = gather_probe_rate(dev, kv_bytes, row_bytes)
+    peak = gather_peak(dev, kv_bytes, row_bytes)
+    probe = peak["gbs"]
     gathered_rows = 2.0 * g.num_edges * row_bytes
     rec["gather_probe"] = {"row_bytes": row_bytes, "footprint_bytes": kv_bytes, "gbs": probe,
+                           "read_only_gbs": peak["read_only_gbs"], "plain_gbs": peak["plain_gbs"],
                            "kv_gathers_gbs": gathered_rows / sec / 1e9,
                            "kv_gathers_frac_of_probe": gathered_rows / sec / 1e9 / probe,
                            "note": "K and V rows gathered per edge (the gathered model without CSR, Q, O, E) "
@@ -636,8 +649,7 @@ def main():
         res = []
         for footprint in (16 << 20, 32 << 20, 64 << 20, 128 << 20, 256 << 20, 1 << 30):
             for rb in (128, 256, 512, 1024):
-                res.append({"footprint_mb": footprint >> 20, "row_bytes": rb,
-                            "gbs": gather_probe_rate(dev, footprint, rb)})
+                res.append(dict(gather_peak(dev, footprint, rb), footprint_mb=footprint >> 20, row_bytes=rb))
         print(json.dumps({"gather_probe": res}), flush=True)
         return
 
@@ -758,7 +770,7 @@ def main():
         roofline["dominant_share"] = prof.get("dominant_share")
     if not args.no_workloads:
         rb = w.heads * w.head_dim * ELT[w.dtype]
-        rate = gather_probe_rate(dev, 2 * g.num_nodes * rb, rb)
+        rate = gather_peak(dev, 2 * g.num_nodes * rb, rb)["gbs"]
         roofline["random_row_gather_gbs"] = rate
         roofline["random_row_gather_note"] = ("uniform random %d-byte rows over the %.2f GB K+V footprint "
                                              "(g3s_gather_probe): the rate the 40%% non-local gathers can be "

@@ -406,12 +406,14 @@ g3s_status g3s_selftest_wait_timeout(const g3s_plan *plan, uint64_t limit_ns, g3
  * ([rows][row_bytes], 16-byte aligned, rows a power of two >= 2): the j-th row
  * read is (j + 1) * 0x9E3779B97F4A7C15 >> (64 - log2 rows) (64-bit wrap-around
  * product), spread uniformly over the rows.  `ctas` CTAs of 8 warps, eight
- * 512-byte warp loads in flight per warp; what is read is XOR-ed into one word
+ * 512-byte warp loads in flight per warp, through the read-only path the
+ * CUDA-core kernel uses (plain_loads = 0) or plain global loads
+ * (plain_loads = 1); what is read is XOR-ed into one word
  * per warp of sink (ctas * 8 uint32).  *rows_read (may be NULL) receives the
  * rows read (whole warp steps).  Enqueued on `stream`; time it with events.
  */
-g3s_status g3s_gather_probe(const void *src, int64_t rows, int row_bytes, int64_t gathers, int ctas, uint32_t *sink,
-                            int64_t *rows_read, g3s_stream_t stream);
+g3s_status g3s_gather_probe(const void *src, int64_t rows, int row_bytes, int64_t gathers, int ctas, int plain_loads,
+                            uint32_t *sink, int64_t *rows_read, g3s_stream_t stream);
 
 /* Release the plan's host struct, stream and events (the caller still owns the workspace). NULL is a no-op.
  * (No counterpart on the pages.) */

@@ -142,7 +142,7 @@ def load_library(path: str = LIB_PATH):
         lib.g3s_linear.restype = I
         lib.g3s_layer_forward.argtypes = [P, P, P, I, P, P, I, P, P, P, P, P, P, P]
         lib.g3s_layer_forward.restype = I
-        lib.g3s_gather_probe.argtypes = [P, I64, I, I64, I, P, ctypes.POINTER(I64), P]
+        lib.g3s_gather_probe.argtypes = [P, I64, I, I64, I, I, P, ctypes.POINTER(I64), P]
         lib.g3s_gather_probe.restype = I
         for name in ("g3s_plan_workspace_size", "g3s_plan_create", "g3s_plan_get_stats", "g3s_plan_export",
                      "g3s_forward", "g3s_host_staging_size", "g3s_forward_host"):
@@ -465,7 +465,7 @@ def linear(X, W, seg_cols: Optional[int] = None, out_dtype: Optional[str] = None
     return outs
 
 
-def gather_probe(src, row_bytes: int, gathers: int, ctas: int, sink, stream=None) -> int:
+def gather_probe(src, row_bytes: int, gathers: int, ctas: int, sink, plain_loads: bool = False, stream=None) -> int:
     """``g3s_gather_probe``: read ``gathers`` (rounded up) hashed random rows of
     ``row_bytes`` from the CUDA tensor ``src`` (a power-of-two number of rows);
     returns the rows read.  A measurement aid (no attention arithmetic): the
@@ -476,7 +476,8 @@ def gather_probe(src, row_bytes: int, gathers: int, ctas: int, sink, stream=None
         raise ValueError("src size must be a multiple of row_bytes")
     got = ctypes.c_int64()
     _check(lib.g3s_gather_probe(_dev_ptr(src, "src"), nbytes // row_bytes, int(row_bytes), int(gathers), int(ctas),
-                                _dev_ptr(sink, "sink"), ctypes.byref(got), _stream_handle(stream)))
+                                1 if plain_loads else 0, _dev_ptr(sink, "sink"), ctypes.byref(got),
+                                _stream_handle(stream)))
     return got.value
 
 

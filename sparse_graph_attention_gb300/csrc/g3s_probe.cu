@@ -22,6 +22,7 @@ __device__ __forceinline__ unsigned long long probe_row(unsigned long long j, in
     return ((j + 1ull) * 0x9E3779B97F4A7C15ull) >> (64 - lg_rows);
 }
 
+template <bool kPlain>
 __global__ void __launch_bounds__(kProbeThreads) gather_probe_kernel(const uint4* src, int lg_rows, int row_vecs,
                                                                      long long gathers, uint32_t* sink) {
     const int lane = threadIdx.x & 31;
@@ -44,7 +45,8 @@ __global__ void __launch_bounds__(kProbeThreads) gather_probe_kernel(const uint4
             const int r_in_step = row_vecs >= 32 ? (k / slices) : k * rows_per_load + my_row;
             const int slice = row_vecs >= 32 ? k % slices : 0;
             const unsigned long long r = probe_row(base + (unsigned)r_in_step, lg_rows);
-            v[k] = __ldg(src + r * (unsigned)row_vecs + slice * 32 + my_vec);
+            const uint4* q = src + r * (unsigned)row_vecs + slice * 32 + my_vec;
+            v[k] = kPlain ? *q : __ldg(q);
         }
 #pragma unroll
         for (int k = 0; k < kInFlight; ++k) {
@@ -77,7 +79,7 @@ using namespace g3s;
 using namespace g3s::api;
 
 extern "C" g3s_status g3s_gather_probe(const void* src, int64_t rows, int row_bytes, int64_t gathers, int ctas,
-                                       uint32_t* sink, int64_t* rows_read, g3s_stream_t stream) {
+                                       int plain_loads, uint32_t* sink, int64_t* rows_read, g3s_stream_t stream) {
     if (!src || !sink) return fail(G3S_ERR_INVALID_ARG, "src and sink must be non-NULL");
     if (rows < 2 || (rows & (rows - 1)) || rows > (1ll << 40))
         return fail(G3S_ERR_INVALID_ARG, "rows must be a power of two in [2, 2^40]");
@@ -90,8 +92,13 @@ extern "C" g3s_status g3s_gather_probe(const void* src, int64_t rows, int row_by
     int lg = 0;
     while ((1ll << lg) < rows) ++lg;
     if (rows_read) *rows_read = probe_rows(gathers, row_bytes / 16, ctas);
-    gather_probe_kernel<<<ctas, kProbeThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(src), lg, row_bytes / 16, gathers, sink);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (plain_loads)
+        gather_probe_kernel<true><<<ctas, kProbeThreads, 0, st>>>(static_cast<const uint4*>(src), lg, row_bytes / 16,
+                                                                  gathers, sink);
+    else
+        gather_probe_kernel<false><<<ctas, kProbeThreads, 0, st>>>(static_cast<const uint4*>(src), lg, row_bytes / 16,
+                                                                   gathers, sink);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? G3S_OK : cuda_fail(e, "gather probe launch");
 }

@@ -13,8 +13,9 @@ from gpu_helpers import ensure_built
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("plain", [False, True])
 @pytest.mark.parametrize("row_bytes", [16, 128, 512, 1024, 4096])
-def test_gather_probe_reads_the_listed_rows(row_bytes):
+def test_gather_probe_reads_the_listed_rows(row_bytes, plain):
     if not torch.cuda.is_available():
         pytest.fail("a CUDA GPU is required for the gpu tests")
     ensure_built()
@@ -25,7 +26,7 @@ def test_gather_probe_reads_the_listed_rows(row_bytes):
     src = torch.from_numpy(src_h).cuda()
     ctas = 3
     sink = torch.zeros(ctas * 8, dtype=torch.int32, device="cuda")
-    n = g3s.gather_probe(src, row_bytes, 5000, ctas, sink)
+    n = g3s.gather_probe(src, row_bytes, 5000, ctas, sink, plain)
     torch.cuda.synchronize()
     assert n >= 5000
     j = np.arange(n, dtype=np.uint64) + np.uint64(1)
