@@ -376,23 +376,61 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
         warm = median_ms(step, runs, stream)
         cold = median_ms(step, runs, stream, flush)
         plan.check()
-        return warm, cold
+        return warm, cold, step
+
+    def graph_ms(step, n=20):
+        """GPU time per forward inside one CUDA graph of n forwards: no host
+        submission between them (the host cost of a call is timed apart)."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for _ in range(n):
+                step()
+        for _ in range(2):
+            gr.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    def host_us(step, n=200):
+        """Host time of one forward call through this binding (enqueue only)."""
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            step()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(dev)
+        return 1e6 * (t1 - t0) / n
 
     plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant)
     st = plan.stats()
-    warm, cold = measure(plan)
+    warm, cold, step0 = measure(plan)
+    in_graph = graph_ms(step0)
+    call_us = host_us(step0)
     gathered, compulsory = byte_counts(g, w, plan.out_dtype)
     sec = cold / 1e3
     rec = {"num_nodes": g.num_nodes, "num_edges": g.num_edges, "heads": w.heads, "head_dim": w.head_dim,
            "dtype": w.dtype, "variant": w.variant, "out_dtype": plan.out_dtype,
-           "ms_warm": warm, "ms_cold": cold,
+           "ms_warm": warm, "ms_cold": cold, "ms_in_cuda_graph": in_graph, "host_us_per_call": call_us,
            "edges_per_s": g.num_edges / sec, "gflops": flops / sec / 1e9,
            "compulsory_frac": compulsory / sec / 1e9 / hbm, "gathered_frac": gathered / sec / 1e9 / hbm,
            "peak_gbs": hbm, "peak_source": hbm_src,
            "timing": "median of %d single-forward CUDA-event times; cold: %d MB written between runs "
-                     "(outside the events) to evict L2; warm: back-to-back" % (runs, L2_FLUSH_BYTES >> 20),
+                     "(outside the events) to evict L2; warm: back-to-back; in CUDA graph: one graph of 20 "
+                     "forwards, GPU time per forward; host_us_per_call: the Python binding's enqueue time"
+                     % (runs, L2_FLUSH_BYTES >> 20),
            "plan": {"tile_windows": st["tile_windows"], "windows": st["windows"], "chunks": st["chunks"],
-                    "pack_rows": st["pack_rows"], "heavy_threshold": st["heavy_threshold"]}}
+                    "pack_rows": st["pack_rows"], "heavy_threshold": st["heavy_threshold"],
+                    "small_graph": st["small_graph"]}}
     # the gathers' own roofline: random rows of this row width over a footprint
     # the size of K and V (L2-resident here unless noted)
     row_bytes = w.heads * w.head_dim * ELT[w.dtype]
@@ -426,7 +464,7 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
                           ("tile_only", dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))):
             p2 = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **kw)
             s2 = p2.stats()
-            w2, c2 = measure(p2)
+            w2, c2, _ = measure(p2)
             entry = {"ms_warm": w2, "ms_cold": c2, "tile_windows": s2["tile_windows"], "windows": s2["windows"]}
             if s2["tile_windows"] > 0:
                 useful = 4.0 * w.heads * w.head_dim * s2["tile_window_nnz"]

@@ -122,6 +122,12 @@ typedef enum g3s_variant {
  *                  the lists: rows run in id order, so neighbouring rows'
  *                  sources meet in L2, heavy rows as chunks taken first, short
  *                  rows in packs; the lists cost five stable scans of N rows
+ *  small_graph_rows  graphs of at most this many rows, with no window on
+ *                  the tile path, run one CTA per row: its eight warps each
+ *                  take an eighth of the row's entries and merge their partial
+ *                  softmax states in shared memory, so the forward is one
+ *                  launch whose latency is about one step of edges per row
+ *                  (default 1024; 0: never; heavy-row chunks are then not used)
  *  pack_rows       short-row packs, where a node row is at most 256 bytes
  *                  (G = 32 * 16 / row bytes >= 2 lane groups per warp): a warp
  *                  takes G consecutive rows together, one per lane group,
@@ -150,6 +156,7 @@ typedef struct g3s_plan_options {
     int32_t pack_rows;
     int32_t tile_pool_density_milli;
     int32_t degree_buckets;
+    int32_t small_graph_rows;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {
@@ -168,6 +175,7 @@ typedef struct g3s_plan_stats {
     int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
     int64_t tile_items;      /* work items of the tile kernel: one or two tile-path windows each */
+    int32_t small_graph;     /* 1 when forwards and aggregations run the small-graph flavour */
 } g3s_plan_stats;
 
 /* Planner arrays readable with g3s_plan_export (all int32 unless noted). */

@@ -67,6 +67,7 @@ class PlanOptions(ctypes.Structure):
         ("pack_rows", ctypes.c_int32),
         ("tile_pool_density_milli", ctypes.c_int32),
         ("degree_buckets", ctypes.c_int32),
+        ("small_graph_rows", ctypes.c_int32),
     ]
 
 
@@ -86,6 +87,7 @@ class PlanStats(ctypes.Structure):
         ("heavy_threshold", ctypes.c_int32), ("chunk_edges", ctypes.c_int32), ("short_rows", ctypes.c_int64),
         ("workspace_used", ctypes.c_size_t),
         ("tile_items", ctypes.c_int64),
+        ("small_graph", ctypes.c_int32),
     ]
 
 

@@ -74,6 +74,7 @@ void default_options(g3s_plan_options* o) {
     o->out_dtype = G3S_F32;
     o->pack_rows = -1;
     o->degree_buckets = 0;
+    o->small_graph_rows = kSmallGraphRows;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -110,6 +111,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
         return fail(G3S_ERR_INVALID_ARG, "out_dtype must be G3S_F32 or the input dtype");
     if (o.pack_rows < -1 || o.pack_rows > 1) return fail(G3S_ERR_INVALID_ARG, "pack_rows takes -1, 0 or 1");
     if (o.degree_buckets != 0 && o.degree_buckets != 1) return fail(G3S_ERR_INVALID_ARG, "degree_buckets takes 0 or 1");
+    if (o.small_graph_rows < 0) return fail(G3S_ERR_INVALID_ARG, "small_graph_rows must be >= 0");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -132,6 +134,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
     s->bucket_lists = o.degree_buckets == 1;
+    s->small_rows = o.small_graph_rows;
     s->tile_density_milli = o.tile_density_milli;
     s->tile_pool_milli = o.tile_pool_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
@@ -365,6 +368,7 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->short_rows = p->counts.n_short;
     st->workspace_used = p->ws_used;
     st->tile_items = p->counts.n_tile_items;
+    st->small_graph = p->shape.N <= p->shape.small_rows && p->counts.n_tile_windows == 0 ? 1 : 0;
     return G3S_OK;
 }
 
@@ -463,6 +467,10 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
     cp.status = p->arr.fwd_status;
     cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
+    if (s.N <= s.small_rows && p->counts.n_tile_windows == 0) {  // one launch: a CTA per row
+        CUDA_OR_FAIL(core_small_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream), "small-graph kernel launch");
+        return G3S_OK;
+    }
     if (p->counts.n_tile_windows > 0) {
         TileParams tp{};
         tp.Q = Q;
@@ -553,6 +561,10 @@ g3s_status g3s_aggregate(const g3s_plan* p, const void* W, const void* X, void* 
     cp.normalize = normalize ? 1 : 0;
     cp.status = p->arr.fwd_status;
     cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
+    if (s.N <= s.small_rows) {  // one launch: a CTA per row
+        CUDA_OR_FAIL(core_small_launch(p->dtype, p->opts.out_dtype, 2, cp, stream), "small-graph kernel launch");
+        return G3S_OK;
+    }
     CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, 2, cp, stream), "aggregation kernel launch");
     if (p->counts.n_chunks > 0) {
         MergeParams mp{};

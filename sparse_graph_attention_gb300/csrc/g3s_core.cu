@@ -74,6 +74,17 @@ cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p,
     }
 }
 
+cudaError_t core_small_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st) {
+    const bool out_f32 = out_dtype == 0;
+    if (!out_f32 && out_dtype != dtype) return cudaErrorInvalidValue;
+    switch (dtype) {
+        case 0: return core_small_launch_f32(true, mode, p, st);
+        case 1: return core_small_launch_f16(out_f32, mode, p, st);
+        case 2: return core_small_launch_bf16(out_f32, mode, p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st) {
     switch (out_dtype) {
         case 0: return merge_launch_f32(plain, p, st);

@@ -749,6 +749,95 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
 }
 
 
+// ---------------------------------------------------------------------------
+// Small graphs (a few hundred rows: far fewer rows than resident warps): one
+// CTA per row, its eight warps each walking one eighth of the row's CSR
+// positions as a chunk whose partial (m, l, acc) goes to shared memory; the
+// CTA then merges the eight partials in warp order, as the heavy-row merge
+// does, and writes the row.  A row's latency chain is then about one step of
+// edges instead of deg / (edges per step) steps.  Every row, heavy or not, is
+// done this way (no chunks, no merge launch); same arithmetic per edge.
+// ---------------------------------------------------------------------------
+template <typename T, typename OutT, int NV, int MODE, int LPH>
+__global__ void __launch_bounds__(kWarpsPerCta * 32) small_kernel(const CoreParams p) {
+    extern __shared__ float part[];  // [warp][H*d] accumulators, then [warp][H][2] (m, l)
+    const int row = blockIdx.x;
+    const int w = threadIdx.x >> 5;
+    const Lanes L(threadIdx.x & 31, p.row_vecs, p.lph);
+    const int HD = p.row_vecs * Vec<T>::N;
+    const int e0 = p.row_ptr[row], e1 = p.row_ptr[row + 1];
+    const int per = (e1 - e0 + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int a = min(e0 + w * per, e1), b = min(a + per, e1);
+    CoreParams q = p;
+    q.part_acc = part;
+    q.part_ml = part + kWarpsPerCta * HD;
+    process_item<T, OutT, NV, MODE, LPH>(q, L, row, a, b, (long long)w);
+    __syncthreads();
+    for (int x = threadIdx.x; x < HD; x += kWarpsPerCta * 32) {
+        const int h = x / p.D;
+        const float* ml = q.part_ml + h * 2;  // warp c: ml[c * 2H], ml[c * 2H + 1]
+        float o;
+        if constexpr (MODE != kModeStd) {
+            float acc = 0.f, sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kWarpsPerCta; ++c) {
+                acc += part[c * HD + x];
+                sum += ml[c * 2 * p.H + 1];
+            }
+            o = (MODE == kModeRtm || p.normalize) ? acc / (sum + p.eps) : acc;
+        } else {
+            float mx = kNegBig;
+#pragma unroll
+            for (int c = 0; c < kWarpsPerCta; ++c) mx = fmaxf(mx, ml[c * 2 * p.H]);
+            float acc = 0.f, sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kWarpsPerCta; ++c) {
+                const float f = ex2(ml[c * 2 * p.H] - mx);
+                sum += ml[c * 2 * p.H + 1] * f;
+                acc += part[c * HD + x] * f;
+            }
+            o = sum > 0.f ? acc / sum : 0.f;
+        }
+        Vec<OutT>::store1(p.O, (long long)row * HD + x, o);
+    }
+}
+
+template <typename T, typename OutT, int NV, int MODE, int LPH>
+cudaError_t launch_small_nv(const CoreParams& p, cudaStream_t st) {
+    if (p.N <= 0) return cudaSuccess;
+    const int HD = p.row_vecs * Vec<T>::N;
+    const size_t smem = (size_t)kWarpsPerCta * ((size_t)HD + 2 * (size_t)p.H) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(small_kernel<T, OutT, NV, MODE, LPH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    small_kernel<T, OutT, NV, MODE, LPH><<<(unsigned)p.N, kWarpsPerCta * 32, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, typename OutT, int MODE>
+cudaError_t launch_small(const CoreParams& p, cudaStream_t st) {
+    const int nv = p.row_vecs <= 32 ? 1 : p.row_vecs / 32;
+    switch (nv) {
+        case 1: return launch_small_nv<T, OutT, 1, MODE, 0>(p, st);
+        case 2: return launch_small_nv<T, OutT, 2, MODE, 0>(p, st);
+        case 4: return launch_small_nv<T, OutT, 4, MODE, 0>(p, st);
+        case 8: return launch_small_nv<T, OutT, 8, MODE, 0>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, typename OutT>
+cudaError_t launch_small_mode(int mode, const CoreParams& p, cudaStream_t st) {
+    switch (mode) {
+        case kModeStd: return launch_small<T, OutT, kModeStd>(p, st);
+        case kModeRtm: return launch_small<T, OutT, kModeRtm>(p, st);
+        case kModeAgg: return launch_small<T, OutT, kModeAgg>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename T, typename OutT, int NV, int MODE, int LPH, bool PACK, bool WINS = false>
 cudaError_t launch_core_nv(const CoreParams& p_in, cudaStream_t st) {
     CoreParams p = p_in;

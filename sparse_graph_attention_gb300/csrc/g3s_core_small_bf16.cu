@@ -1,0 +1,12 @@
+// Instantiations of the small-graph flavour of the fused CUDA-core kernel
+// (one CTA per row) for __nv_bfloat16 inputs.
+#include "g3s_core.cuh"
+
+namespace g3s {
+
+cudaError_t core_small_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st) {
+    using namespace core_detail;
+    return out_f32 ? launch_small_mode<__nv_bfloat16, float>(mode, p, st) : launch_small_mode<__nv_bfloat16, __nv_bfloat16>(mode, p, st);
+}
+
+}  // namespace g3s

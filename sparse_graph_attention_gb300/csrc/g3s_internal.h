@@ -95,6 +95,7 @@ struct PlanShape {
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
     int64_t scan_blocks;
     int pack_limit;  // most entries of a row a short-row pack takes (0: the row width does not pack)
+    long long small_rows;  // graphs of at most this many rows take the small-graph flavour
 };
 
 // Most CSR entries of a row that a short-row pack takes, for node rows of
@@ -187,6 +188,11 @@ bool encode_tile(CUtensorMap* m, const void* base, long long rows, int row_elems
 
 bool core_supported(int dtype, int row_vecs);
 cudaError_t core_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st);
+// The default of the small_graph_rows option: graphs of at most this many
+// rows run the small-graph flavour (one CTA per row) when no window takes the
+// tile path, so the whole forward is one launch.
+constexpr int kSmallGraphRows = 1024;
+cudaError_t core_small_launch(int dtype, int out_dtype, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t merge_launch(int out_dtype, bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t core_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
@@ -195,6 +201,10 @@ cudaError_t core_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaSt
 cudaError_t core_launch_pack_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_pack_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t core_launch_pack_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+// the small-graph flavour (one CTA per row, no chunks or merge launch)
+cudaError_t core_small_launch_f32(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_small_launch_f16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
+cudaError_t core_small_launch_bf16(bool out_f32, int mode, const CoreParams& p, cudaStream_t st);
 cudaError_t merge_launch_f32(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_f16(bool plain, const MergeParams& p, cudaStream_t st);
 cudaError_t merge_launch_bf16(bool plain, const MergeParams& p, cudaStream_t st);

@@ -146,6 +146,10 @@ extern "C" g3s_status g3s_forward_noalloc(const int32_t* row_ptr_d, const int32_
     cp.elementwise_clamp = o.rtm_elementwise_clamp ? 1 : 0;
     cp.status = a.fwd_status;
     cp.pack_rows = use_packs(o.pack_rows, s, hc) ? 1 : 0;
+    if (s.N <= s.small_rows) {  // as g3s_forward: one launch, a CTA per row
+        NOALLOC_CUDA(core_small_launch(dtype, o.out_dtype, rtm, cp, stream), "small-graph kernel launch");
+        return G3S_OK;
+    }
     NOALLOC_CUDA(core_launch(dtype, o.out_dtype, rtm, cp, stream), "fused kernel launch");
     if (hc.n_chunks > 0) {
         MergeParams mp{};

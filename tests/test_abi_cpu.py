@@ -71,7 +71,7 @@ def test_default_options(lib):
     assert o.tile_density_milli == 150 and o.tile_pool_density_milli == 300 and o.tile_max_tiles == 16 \
         and o.out_dtype == 0
     assert abs(o.rtm_epsilon - 1e-6) < 1e-12 and o.rtm_elementwise_clamp == 1
-    assert o.pack_rows == -1 and o.degree_buckets == 0
+    assert o.pack_rows == -1 and o.degree_buckets == 0 and o.small_graph_rows == 1024
 
 
 @pytest.mark.parametrize("args,status", [
@@ -100,7 +100,7 @@ def test_workspace_grows_with_bsb(lib):
 def test_bad_options_rejected(lib):
     for kw in (dict(bucket_bounds=[10, 5, 20]), dict(heavy_threshold=-1), dict(chunk_edges=0),
                dict(bsb_smem_edges=100000), dict(tile_path=2), dict(pack_rows=2), dict(tile_pool_density_milli=-1),
-               dict(degree_buckets=2)):
+               dict(degree_buckets=2), dict(small_graph_rows=-1)):
         with pytest.raises(g3s.G3SError) as ei:
             g3s.workspace_size(100, 1000, 4, 32, "bf16", **kw)
         assert ei.value.status == 1

@@ -52,9 +52,9 @@ def test_aggregate_popcornbench_shape():
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_aggregate_heavy_rows(dtype):
     g = graphgen.powerlaw(num_nodes=5000, max_degree=4000, seed=8)
-    plan = _case(g, 2, 32, dtype, True, positive=True, seed=9, plan_kw=dict(heavy_threshold=40, chunk_edges=13))
+    plan = _case(g, 2, 32, dtype, True, positive=True, seed=9, plan_kw=dict(heavy_threshold=40, chunk_edges=13, small_graph_rows=0))
     assert plan.stats()["chunks"] > 0
-    _case(g, 2, 32, dtype, False, positive=False, seed=10, plan_kw=dict(heavy_threshold=40, chunk_edges=13))
+    _case(g, 2, 32, dtype, False, positive=False, seed=10, plan_kw=dict(heavy_threshold=40, chunk_edges=13, small_graph_rows=0))
 
 
 def test_aggregate_full_powerlaw():
@@ -106,7 +106,7 @@ def test_aggregate_32_byte_rows(dtype, pack):
     rp[1:] = np.cumsum(deg)
     g = graphgen.Graph(rp.astype(np.int32), np.concatenate(rows).astype(np.int32))
     plan = _case(g, 1, 16, dtype, True, positive=True, seed=22, plan_kw=dict(pack_rows=pack, heavy_threshold=500,
-                                                                              chunk_edges=130))
+                                                                              chunk_edges=130, small_graph_rows=0))
     st = plan.stats()
     assert st["chunks"] > 0 and st["pack_rows"] == pack
     _case(g, 1, 16, dtype, False, positive=False, seed=23, plan_kw=dict(pack_rows=pack))

@@ -52,7 +52,7 @@ def test_sixteen_bit_output(name):
     """O stored in the 16-bit input type (plan option out_dtype)."""
     g, vals, w = graphgen.make_workload(name, "small")
     plan, O, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant,
-                          plan_kw=dict(out_dtype=w.dtype, heavy_threshold=64, chunk_edges=40))
+                          plan_kw=dict(out_dtype=w.dtype, heavy_threshold=64, chunk_edges=40, small_graph_rows=0))
     assert O.dtype == {"bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
 
 
@@ -60,8 +60,8 @@ def test_sixteen_bit_rtmscore_eout():
     g = graphgen.rtmscore_batch(num_graphs=3, min_nodes=30, max_nodes=60, seed=16)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 8, 16, True, seed=17)
     for dt in ("bf16", "f16"):
-        run_case(g, vals, 8, 16, dt, "rtmscore", plan_kw=dict(out_dtype=dt, heavy_threshold=8, chunk_edges=5))
-        run_case(g, vals, 8, 16, dt, "rtmscore", plan_kw=dict(heavy_threshold=8, chunk_edges=5))
+        run_case(g, vals, 8, 16, dt, "rtmscore", plan_kw=dict(out_dtype=dt, heavy_threshold=8, chunk_edges=5, small_graph_rows=0))
+        run_case(g, vals, 8, 16, dt, "rtmscore", plan_kw=dict(heavy_threshold=8, chunk_edges=5, small_graph_rows=0))
 
 
 # ---------------------------------------------------------------------------
@@ -72,7 +72,7 @@ def test_sixteen_bit_rtmscore_eout():
 def test_heavy_split_matches_oracle(dtype, variant):
     g = graphgen.powerlaw(num_nodes=3000, max_degree=2000, seed=5)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 2, 32, variant == "rtmscore", seed=6)
-    plan, O, _ = run_case(g, vals, 2, 32, dtype, variant, plan_kw=dict(heavy_threshold=20, chunk_edges=7))
+    plan, O, _ = run_case(g, vals, 2, 32, dtype, variant, plan_kw=dict(heavy_threshold=20, chunk_edges=7, small_graph_rows=0))
     st = plan.stats()
     assert st["heavy_rows"] > 50 and st["chunks"] > st["heavy_rows"]
 
@@ -90,7 +90,7 @@ SHAPES = [("f32", 1, 16), ("f32", 2, 32), ("f32", 8, 32), ("f32", 4, 128), ("f32
 def test_shapes(dtype, H, d, variant):
     g = graphgen.random_csr(133, 45, seed=H * 1000 + d, zero_frac=0.15)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, H, d, variant == "rtmscore", seed=d + H)
-    run_case(g, vals, H, d, dtype, variant, plan_kw=dict(heavy_threshold=30, chunk_edges=9))
+    run_case(g, vals, H, d, dtype, variant, plan_kw=dict(heavy_threshold=30, chunk_edges=9, small_graph_rows=0))
 
 
 # ---------------------------------------------------------------------------
@@ -132,7 +132,7 @@ def test_single_node_self_loop():
 def test_multigraph_and_unsorted(multigraph, sorted_rows):
     g = graphgen.random_csr(211, 60, seed=21, zero_frac=0.1, multigraph=multigraph, sorted_rows=sorted_rows)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, 4, 32, False, seed=22)
-    run_case(g, vals, 4, 32, "bf16", "standard", plan_kw=dict(heavy_threshold=40, chunk_edges=16))
+    run_case(g, vals, 4, 32, "bf16", "standard", plan_kw=dict(heavy_threshold=40, chunk_edges=16, small_graph_rows=0))
 
 
 def test_deterministic_and_edge_order_invariant():
@@ -192,7 +192,7 @@ def _planner_graphs():
 def test_planner_bit_exact(name, g, kw):
     ensure_built()
     rp, ci = upload_graph(g)
-    opts = dict(bsb=1, heavy_threshold=64, chunk_edges=32, bucket_bounds=(4, 16, 128), degree_buckets=1)
+    opts = dict(bsb=1, heavy_threshold=64, chunk_edges=32, small_graph_rows=0, bucket_bounds=(4, 16, 128), degree_buckets=1)
     opts.update(kw)
     plan = g3s.Plan(rp, ci, g.num_nodes, 2, 32, "bf16", **opts)
     ref = ref_planner.full_plan(g.row_ptr, g.col_idx, g.num_nodes, bounds=(4, 16, 128), heavy_threshold=64,

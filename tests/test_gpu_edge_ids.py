@@ -36,7 +36,8 @@ def test_rtmscore_reads_and_writes_physical_slots(dtype):
     t = {n: graphgen.to_dtype(a, dtype) for n, a in (("Q", q), ("K", k), ("V", v), ("E", e_phys))}
     dev = device()
     rp, ci = upload_graph(g)
-    plan = g3s.Plan(rp, ci, g.num_nodes, H, d, dtype, "rtmscore", heavy_threshold=8, chunk_edges=5)
+    plan = g3s.Plan(rp, ci, g.num_nodes, H, d, dtype, "rtmscore", heavy_threshold=8, chunk_edges=5,
+                    small_graph_rows=0)
     plan.set_edge_ids(torch.from_numpy(ids).to(dev), slots)
     Eout = torch.full((slots, H, d), 7.0, dtype=torch.float32, device=dev)
     O, Eout = plan.forward(t["Q"].to(dev), t["K"].to(dev), t["V"].to(dev), t["E"].to(dev), Eout=Eout,
@@ -60,7 +61,8 @@ def test_aggregate_reads_physical_weights():
     w_phys = (np.abs(rng.standard_normal((slots, H))) + 0.1).astype(np.float32)
     dev = device()
     rp, ci = upload_graph(g)
-    plan = g3s.Plan(rp, ci, g.num_nodes, H, d, "f32", heavy_threshold=50, chunk_edges=17)
+    plan = g3s.Plan(rp, ci, g.num_nodes, H, d, "f32", heavy_threshold=50, chunk_edges=17,
+                    small_graph_rows=0)
     plan.set_edge_ids(torch.from_numpy(ids).to(dev), slots)
     O = plan.aggregate(torch.from_numpy(w_phys).to(dev), torch.from_numpy(x).to(dev), normalize=True)
     torch.cuda.synchronize()

@@ -76,7 +76,7 @@ def test_pack_matches_oracle(dtype, H, d, pack):
     g = graph_with_degrees(short_mix(n, limit, seed=1), n, seed=2)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, H, d, False, seed=3)
     plan, _, _ = run_case(g, vals, H, d, dtype, "standard",
-                          plan_kw=dict(heavy_threshold=300, chunk_edges=37, pack_rows=pack))
+                          plan_kw=dict(heavy_threshold=300, chunk_edges=37, small_graph_rows=0, pack_rows=pack))
     st = plan.stats()
     assert st["chunks"] > 0 and st["pack_rows"] == pack
 
@@ -90,7 +90,7 @@ def test_pack_heavy_threshold_below_limit(dtype, H, d):
     g = graph_with_degrees(rng.integers(0, 12, n), n, seed=5)
     vals = graphgen.make_values(g.num_nodes, g.num_edges, H, d, False, seed=6)
     plan, _, _ = run_case(g, vals, H, d, dtype, "standard",
-                          plan_kw=dict(heavy_threshold=3, chunk_edges=2, pack_rows=1))
+                          plan_kw=dict(heavy_threshold=3, chunk_edges=2, small_graph_rows=0, pack_rows=1))
     st = plan.stats()
     assert st["heavy_rows"] > 0 and st["pack_rows"] == 1 and st["pack_limit"] == 3
 

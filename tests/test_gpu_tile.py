@@ -70,7 +70,7 @@ def test_tile_mixed_with_core_rows():
     rp = np.concatenate([a.row_ptr, a.row_ptr[-1] + b.row_ptr[1:]]).astype(np.int32)
     col = np.concatenate([a.col_idx, b.col_idx + off]).astype(np.int32)
     g = graphgen.Graph(rp, col)
-    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0, heavy_threshold=60, chunk_edges=25))
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, tile_density_milli=150, tile_pool_density_milli=0, heavy_threshold=60, chunk_edges=25, small_graph_rows=0))
     st = plan.stats()
     assert 0 < st["tile_windows"] < st["windows"] and st["chunks"] > 0
 
@@ -219,10 +219,10 @@ def _selection_cases():
     yield "batched_dense_full_per_window_global_bitmap", dense_full, 8, dict(per_window, bsb_smem_edges=64), True
     yield "batched_complete_small", complete_small, 8, {}, True
     yield "batched_complete_small_global_bitmap", complete_small, 8, dict(bsb_smem_edges=100), True
-    yield "mixed_heavy", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25), True
+    yield "mixed_heavy", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25, small_graph_rows=0), True
     yield "mixed_heavy_pooled_out", _mixed_graph, 2, dict(tile_pool_density_milli=500, heavy_threshold=60,
-                                                         chunk_edges=25), False
-    yield "mixed_heavy_global_bitmap", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25,
+                                                         chunk_edges=25, small_graph_rows=0), False
+    yield "mixed_heavy_global_bitmap", _mixed_graph, 2, dict(per_window, heavy_threshold=60, chunk_edges=25, small_graph_rows=0,
                                                             bsb_smem_edges=48), True
     yield "mixed_max_tiles", _mixed_graph, 2, dict(tile_density_milli=0, tile_pool_density_milli=0,
                                                    tile_max_tiles=5), True
