@@ -90,19 +90,21 @@ typedef enum g3s_variant {
  *                  is the standard form with fp16/bf16 inputs and d = 64,
  *                  unless bsb = 0)
  *  tile_density_milli  a window is eligible for the tile path when
- *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 150)
+ *                  1000 * nnz >= tile_density_milli * 128 * tiles (default 100)
  *                  and it has no repeated (row, source) pair, at most
  *                  tile_max_tiles tiles and no heavy row
  *  tile_pool_density_milli  the eligible windows take the tile path together
  *                  when 1000 * (their CSR entries) >= tile_pool_density_milli *
- *                  128 * (their tiles), and none does otherwise (default 300).
+ *                  128 * (their tiles), and none does otherwise (default 180).
  *                  Measured on one GB300 with batched 20-60-node graphs (8 x 64
- *                  bf16): the tensor-core kernel wins from a pooled density of
- *                  about 0.3 (edge probability 0.4: 0.127 ms against 0.139 ms;
- *                  complete graphs 0.139 against 0.302), loses slightly below it
- *                  (p = 0.3, pooled 0.24: 0.133 against 0.119); a plan that
- *                  splits a batch between the two kernels pays the slower
- *                  one's tail, so the choice is made for the batch
+ *                  bf16, ms per forward, CUDA-core kernel against tensor-core
+ *                  kernel): edge probability 0.18 (pooled density 0.16-0.18)
+ *                  0.084 against 0.086, 0.22 (0.18-0.20) 0.094 against 0.088,
+ *                  0.3 (0.24) 0.115 against 0.091, complete graphs 0.305
+ *                  against 0.098; a plan that splits a batch between the two
+ *                  kernels pays the slower one's tail (edge probability 0.3
+ *                  with a per-window floor of 0.15: 0.095), so the choice is
+ *                  made for the batch
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 16, i.e. 128 source columns,
  *                  the M side of the kernel's tcgen05 product)

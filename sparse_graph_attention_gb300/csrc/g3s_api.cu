@@ -64,8 +64,8 @@ void default_options(g3s_plan_options* o) {
     o->chunk_edges = 512;
     o->bsb = -1;
     o->tile_path = -1;
-    o->tile_density_milli = 150;
-    o->tile_pool_density_milli = 300;
+    o->tile_density_milli = 100;
+    o->tile_pool_density_milli = 180;
     o->tile_max_tiles = 16;
     o->bsb_smem_edges = 2048;
     o->rtm_elementwise_clamp = 1;

@@ -68,7 +68,7 @@ def test_default_options(lib):
     o = g3s.default_options()
     assert list(o.bucket_bounds) == [32, 256, 2048]
     assert o.heavy_threshold == 0 and o.chunk_edges == 512 and o.validate_graph == 1
-    assert o.tile_density_milli == 150 and o.tile_pool_density_milli == 300 and o.tile_max_tiles == 16 \
+    assert o.tile_density_milli == 100 and o.tile_pool_density_milli == 180 and o.tile_max_tiles == 16 \
         and o.out_dtype == 0
     assert abs(o.rtm_epsilon - 1e-6) < 1e-12 and o.rtm_elementwise_clamp == 1
     assert o.pack_rows == -1 and o.degree_buckets == 0 and o.small_graph_rows == 1024

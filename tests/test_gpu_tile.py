@@ -213,8 +213,8 @@ def _selection_cases():
     dense_full = lambda: graphgen.make_workload("batched_dense", "full")[0]  # noqa: E731
     complete_small = lambda: graphgen.make_workload("batched_complete", "small")[0]  # noqa: E731
     per_window = dict(tile_density_milli=150, tile_pool_density_milli=0)
-    yield "batched_dense_full_default", dense_full, 8, {}, False  # pooled density 0.24 < 0.3
-    yield "batched_dense_full_pool_200", dense_full, 8, dict(tile_pool_density_milli=200), True
+    yield "batched_dense_full_default", dense_full, 8, {}, True  # pooled density 0.24 >= 0.18
+    yield "batched_dense_full_pool_300", dense_full, 8, dict(tile_pool_density_milli=300), False
     yield "batched_dense_full_per_window", dense_full, 8, per_window, True
     yield "batched_dense_full_per_window_global_bitmap", dense_full, 8, dict(per_window, bsb_smem_edges=64), True
     yield "batched_complete_small", complete_small, 8, {}, True
