@@ -327,24 +327,26 @@ def median_ms(step, runs: int, stream, flush=None):
 
 def tile_mma_flops(plan, heads: int, head_dim: int) -> int:
     """FLOPs the tile kernel issues on the tensor cores for one forward.  Per
-    tile-path window and head: S^T = K_cols Q_w^T as one 128 x 16 x head_dim
-    product, and O^T = V_cols^T P^T as a 128 x 16 product (the 64 feature
-    rows issued twice) over the window's columns rounded up to 16."""
-    tw = plan.export("tile_windows")
-    if tw.size == 0:
+    item (one or two windows, or one slice of a split window) and head:
+    S^T = K_cols Q^T as one 128 x 16 nwin x head_dim product, and per window
+    O^T = V_cols^T P^T as 128 x 16 products (the 64 feature rows issued twice)
+    over its 16-column units."""
+    if not plan.stats()["tile_items"]:
         return 0
-    ptr = plan.export("win_tile_ptr").astype(np.int64)
-    cols = 8 * (ptr[tw + 1] - ptr[tw])
-    ksteps = (cols + 15) // 16
-    per_window = 2 * 128 * 16 * head_dim + 2 * 128 * 16 * 16 * ksteps
-    return int(per_window.sum() * heads)
+    items = plan.export("tile_items").astype(np.int64)
+    nwin = items[:, 3] & 0xFF
+    units0 = (items[:, 3] >> 8) & 0xFF
+    units1 = np.where(nwin == 2, (np.minimum(items[:, 6], 16) + 1) // 2, 0)
+    per_item = 2 * 128 * 16 * nwin * head_dim + 2 * 128 * 16 * 16 * (units0 + units1)
+    return int(per_item.sum() * heads)
 
 
 def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_paths: bool):
     """One workload at full size through the default plan: warm and
     cold-L2 medians, rates, byte and FLOP fractions, the ncu record when it
     matches the sources, the oracle on one thread and on all cores; for
-    the batched family also the CUDA-core-only and tile-only plans."""
+    the batched family and the clustered heavy rows also the CUDA-core-only
+    and tile-only plans."""
     import torch
 
     import sparse_graph_attention_gb300 as g3s
@@ -428,7 +430,8 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
                      "(outside the events) to evict L2; warm: back-to-back; in CUDA graph: one graph of 20 "
                      "forwards, GPU time per forward; host_us_per_call: the Python binding's enqueue time"
                      % (runs, L2_FLUSH_BYTES >> 20),
-           "plan": {"tile_windows": st["tile_windows"], "windows": st["windows"], "chunks": st["chunks"],
+           "plan": {"tile_windows": st["tile_windows"], "split_windows": st["split_windows"],
+                    "tile_items": st["tile_items"], "windows": st["windows"], "chunks": st["chunks"],
                     "pack_rows": st["pack_rows"], "heavy_threshold": st["heavy_threshold"],
                     "small_graph": st["small_graph"]}}
     # the gathers' own roofline: random rows of this row width over a footprint
@@ -465,7 +468,8 @@ def time_workload(name: str, dev, runs: int, oracle_seconds: float, flush, with_
             p2 = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **kw)
             s2 = p2.stats()
             w2, c2, _ = measure(p2)
-            entry = {"ms_warm": w2, "ms_cold": c2, "tile_windows": s2["tile_windows"], "windows": s2["windows"]}
+            entry = {"ms_warm": w2, "ms_cold": c2, "tile_windows": s2["tile_windows"],
+                     "split_windows": s2["split_windows"], "windows": s2["windows"]}
             if s2["tile_windows"] > 0:
                 useful = 4.0 * w.heads * w.head_dim * s2["tile_window_nnz"]
                 issued = tile_mma_flops(p2, w.heads, w.head_dim)
@@ -898,10 +902,11 @@ def main():
     if rank == 0 and not args.no_workloads:
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         workloads = {}
-        for name in ("tiny_poisson", "rtmscore_batch64", "batched_dense", "powerlaw", "batched_complete"):
+        for name in ("tiny_poisson", "rtmscore_batch64", "batched_dense", "powerlaw", "batched_complete",
+                     "clustered_heavy"):
             workloads[name] = time_workload(name, dev, args.workload_runs,
                                             0.0 if args.no_cpu_baseline else args.workload_oracle_seconds, flush,
-                                            with_paths=name.startswith("batched"))
+                                            with_paths=name.startswith("batched") or name == "clustered_heavy")
         del flush
 
     if rank == 0:

@@ -252,6 +252,36 @@ def lognormal_local(num_nodes: int = 2_000_000, mu: float = 3.6, sigma: float = 
 
 
 # ---------------------------------------------------------------------------
+# Clustered heavy rows (not one of the five benchmark configurations): row
+# window c (rows 16c .. 16c+15) is a community whose heavy rows each take
+# `degree` distinct sources from a pool of `pool` distinct nodes shared by the
+# window (uniform over all nodes); a fraction `light_frac` of the rows are
+# light instead, `light_degree` distinct uniform sources from anywhere, and
+# `empty_frac` of them have no entries.  The dense end of power-law graphs
+# whose heavy rows cluster: windows much wider than 128 columns.
+# ---------------------------------------------------------------------------
+def clustered_heavy(num_windows: int = 1024, pool: int = 2048, degree: int = 1024, light_frac: float = 0.25,
+                    light_degree: int = 8, empty_frac: float = 0.0, num_nodes: int = 0,
+                    seed: int = 1007) -> Graph:
+    rng = _rng(seed)
+    n = num_nodes if num_nodes > 0 else 16 * num_windows
+    degs, cols = [], []
+    for w in range((n + 15) // 16):
+        shared = rng.choice(n, size=min(pool, n), replace=False)
+        for r in range(16 * w, min(16 * w + 16, n)):
+            u = rng.random()
+            if u < empty_frac:
+                src = np.zeros(0, np.int64)
+            elif u < empty_frac + light_frac:
+                src = rng.choice(n, size=min(light_degree, n), replace=False)
+            else:
+                src = rng.choice(shared, size=min(degree, shared.size), replace=False)
+            degs.append(src.size)
+            cols.append(np.sort(src))
+    return _finish(np.asarray(degs, np.int64), np.concatenate(cols) if cols else np.zeros(0, np.int64))
+
+
+# ---------------------------------------------------------------------------
 # Generic random CSR for edge cases (zero-degree rows, multigraphs, unsorted
 # rows).  Used only by tests.
 # ---------------------------------------------------------------------------
@@ -333,6 +363,14 @@ WORKLOADS: Dict[str, Workload] = {
         Workload(6, "batched_complete", batched_dense, dict(num_graphs=1024, p=1.0), dict(num_graphs=24, p=1.0),
                  8, 64, "bf16", "standard",
                  "1024 complete graphs of U[20,60] nodes (with self loops), 8x64 bf16"),
+        # not one of the five either: heavy rows clustered in 16-row windows
+        # (pool 2048, degree 1024), where windows are wider than the tile
+        # kernel's 128 columns and run as split windows
+        Workload(7, "clustered_heavy", clustered_heavy, dict(num_windows=1024),
+                 dict(num_windows=12, pool=400, degree=200, empty_frac=0.05, num_nodes=187),
+                 8, 64, "bf16", "standard",
+                 "1024 windows of 16 rows; 3/4 of the rows take 1024 sources from a 2048-node pool shared "
+                 "by the window, the rest 8 uniform sources; 8x64 bf16"),
     ]
 }
 

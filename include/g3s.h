@@ -108,6 +108,25 @@ typedef enum g3s_variant {
  *  tile_max_tiles  most 16x8 tiles a tile-path window may have (default and
  *                  maximum with the tile path on: 16, i.e. 128 source columns,
  *                  the M side of the kernel's tcgen05 product)
+ *  tile_split_density_milli  windows wider than 16 tiles (128 source
+ *                  columns) whose density reaches tile_split_density_milli /
+ *                  1000 take the tile path as split windows: each 128-column
+ *                  slice is a work item of its own, written as a partial
+ *                  softmax state (row max, row sum, unnormalised output) and
+ *                  merged per row after the kernels, the way heavy-row chunks
+ *                  are (the edge-parallel form of the Fused3S page's Figure 2
+ *                  caption, with the columns split as in its Figure 3 caption).
+ *                  Heavy rows inside a split window are computed there, not
+ *                  as chunks.  Decided per window, outside the pooled rule.
+ *                  0 turns split windows off; otherwise 100..1000 (default
+ *                  250).  The partial states take workspace: up to
+ *                  2000 * E / (128 * tile_split_density_milli) rows of
+ *                  4 * H * (d + 2) bytes when the tile path is on.  Measured on
+ *                  one GB300 (windows whose 16 rows each draw 1024 sources from
+ *                  a pool shared by the window, 4.2 M entries, 8 x 64 bf16, ms
+ *                  per forward, CUDA-core chunks against split windows before
+ *                  the merge): density 1 0.87 against 0.11, 0.5 0.85 against
+ *                  0.21, 0.25 0.85 against 0.40
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
  *                  the global-bitmap planner kernel instead of the shared-
  *                  memory sort (default 2048; a testing knob)
@@ -159,6 +178,7 @@ typedef struct g3s_plan_options {
     int32_t tile_pool_density_milli;
     int32_t degree_buckets;
     int32_t small_graph_rows;
+    int32_t tile_split_density_milli;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {
@@ -176,8 +196,14 @@ typedef struct g3s_plan_stats {
     int32_t chunk_edges;     /* CSR positions per heavy-row chunk */
     int64_t short_rows;      /* rows with at most pack_limit entries */
     size_t workspace_used;
-    int64_t tile_items;      /* work items of the tile kernel: one or two tile-path windows each */
+    int64_t tile_items;      /* work items of the tile kernel: one or two tile-path windows each,
+                                or one 128-column slice of a split window */
     int32_t small_graph;     /* 1 when forwards and aggregations run the small-graph flavour */
+    int64_t split_windows;   /* tile-path windows cut into 128-column slices (included in
+                                tile_windows) */
+    int64_t split_items;     /* items of the split windows (included in tile_items) */
+    int64_t merge_rows;      /* rows a forward merges from partial states: heavy rows outside
+                                split windows and every row of a split window */
 } g3s_plan_stats;
 
 /* Planner arrays readable with g3s_plan_export (all int32 unless noted). */
@@ -191,16 +217,26 @@ typedef enum g3s_plan_array {
     G3S_ARR_TILE_COLS = 6,       /* [tiles][8], -1 padded */
     G3S_ARR_TILE_BITS = 7,       /* uint32 [tiles][4], bit r*8+c of a 128-bit word */
     G3S_ARR_WIN_NNZ = 8,         /* [W] CSR entries per window */
-    G3S_ARR_WIN_FLAGS = 9,       /* uint8 [W]: bit0 repeated edge, bit1 tile path */
-    G3S_ARR_TILE_WINDOWS = 10,   /* [tile_windows] ascending */
+    G3S_ARR_WIN_FLAGS = 9,       /* uint8 [W]: bit0 repeated edge, bit1 tile path, bit3 split
+                                    window (with bit1) */
+    G3S_ARR_TILE_WINDOWS = 10,   /* [tile_windows - split_windows] ascending: the tile-path
+                                    windows of at most 16 tiles */
     G3S_ARR_CORE_WINDOWS = 11,   /* [windows - tile_windows] ascending: the windows whose rows the
                                     CUDA-core kernel takes (every window without bit 1) */
-    G3S_ARR_TILE_ITEMS = 12      /* [tile_items][8]: the tile kernel's items.  Tile-path list
-                                    entries 2k and 2k+1 share an item when ceil(T/2) of both
-                                    (16-column units of T tiles) sum to <= 8.  Per item
-                                    (w0, first tile of w0, T0, nwin | units0 << 8,
-                                     w1, first tile of w1, T1, 0), the second window zero
-                                    when nwin = 1 */
+    G3S_ARR_TILE_ITEMS = 12,     /* [tile_items][8]: the tile kernel's items.  First the pairs:
+                                    tile-path list entries 2k and 2k+1 share an item when
+                                    ceil(T/2) of both (16-column units of T tiles) sum to <= 8;
+                                    per item (w0, first tile of w0, T0, nwin | units0 << 8,
+                                    w1, first tile of w1, T1, 0), the second window zero when
+                                    nwin = 1.  Then the split windows in ascending order, one
+                                    item per 128-column slice s of S = ceil(T/16):
+                                    (w, first tile + 16 s, its tiles, 1 | units << 8 | 1 << 16,
+                                     chunks + B_w + s, S, 0, 0), where B_w = 16 x (the slices of
+                                    the split windows before w); row r of the window writes its
+                                    partial state to partial index chunks + B_w + r S + s */
+    G3S_ARR_MERGE_ROWS = 13,     /* [merge_rows] ascending: the rows a forward merges */
+    G3S_ARR_MERGE_RANGES = 14    /* [merge_rows][2]: partial indices [begin, end) of each merged
+                                    row (heavy-row chunks, or the slices of a split window) */
 } g3s_plan_array;
 
 typedef struct g3s_plan g3s_plan; /* opaque */

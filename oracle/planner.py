@@ -34,6 +34,20 @@ Three outputs, all integer, all unique under the canonical orderings below.
    their T_w), and none does otherwise.  ``tile_windows`` lists them in
    ascending order, ``core_windows`` the other windows (whose rows the
    CUDA-core kernel takes), also ascending.
+
+4. Split windows (the edge-parallel form of the Fused3S Figure 2 caption,
+   columns split as in its Figure 3 caption).  With split_milli > 0, a window
+   with no repeated pair, T_w > 16 and 1000 * nnz >= split_milli * 128 * T_w
+   takes the tile path on its own (bits 1 and 3 of ``win_flags``), heavy rows
+   included; it is not in ``tile_windows`` (the pairs' list) nor in
+   ``core_windows``.  It is cut into S_w = ceil(T_w / 16) slices of 16 tiles,
+   one tile item each, after the pairs' items, windows ascending.  Window w's
+   partial states occupy indices n_chunks + 16 B_w .. n_chunks + 16 (B_w + S_w)
+   - 1, B_w = the slices of the split windows before w: row r, slice s at
+   n_chunks + 16 B_w + r S_w + s.  A forward then merges (``merge_rows``,
+   ascending, with ``merge_ranges`` [begin, end)) every row of a split window
+   over its S_w partials and every heavy row outside split windows over its
+   chunks.
 """
 from __future__ import annotations
 
@@ -43,6 +57,9 @@ WIN_ROWS = 16
 TILE_COLS = 8
 FLAG_DUP = 1
 FLAG_TILE = 2
+FLAG_SPLIT = 8
+SPLIT_TILES = 16   # tiles per slice of a split window (128 columns)
+ITEM_PARTIAL = 1 << 16
 
 
 def degrees(row_ptr: np.ndarray) -> np.ndarray:
@@ -142,9 +159,14 @@ def bsb(row_ptr: np.ndarray, col_idx: np.ndarray, num_nodes: int) -> dict:
 
 
 def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold: int,
-                   max_tiles: int, density_milli: int, pool_milli: int = 0) -> dict:
+                   max_tiles: int, density_milli: int, pool_milli: int = 0, split_milli: int = 0) -> dict:
     W = b["win_nnz"].shape[0]
     flags = np.where(b["win_dup"], FLAG_DUP, 0).astype(np.uint8)
+    if enabled and split_milli > 0:
+        nt = np.diff(b["win_tile_ptr"].astype(np.int64))
+        nnz = b["win_nnz"].astype(np.int64)
+        split = (~b["win_dup"]) & (nt > SPLIT_TILES) & (1000 * nnz >= int(split_milli) * 128 * nt)
+        flags = flags | np.where(split, FLAG_TILE | FLAG_SPLIT, 0).astype(np.uint8)
     if enabled:
         deg = degrees(row_ptr)
         n = deg.shape[0]
@@ -159,18 +181,21 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
         take = pool_tiles > 0 and 1000 * pool_nnz >= int(pool_milli) * 128 * pool_tiles
         if take:
             flags = flags | np.where(elig, FLAG_TILE, 0).astype(np.uint8)
-    tile_windows = np.flatnonzero(flags & FLAG_TILE).astype(np.int32)
+    tile_windows = np.flatnonzero((flags & (FLAG_TILE | FLAG_SPLIT)) == FLAG_TILE).astype(np.int32)
+    split_windows = np.flatnonzero(flags & FLAG_SPLIT).astype(np.int32)
     core_windows = np.flatnonzero((flags & FLAG_TILE) == 0).astype(np.int32)
-    return dict(win_flags=flags, tile_windows=tile_windows, core_windows=core_windows)
+    return dict(win_flags=flags, tile_windows=tile_windows, split_windows=split_windows, core_windows=core_windows)
 
 
-def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray) -> np.ndarray:
+def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_windows=(), n_chunks: int = 0) -> np.ndarray:
     """Work items of the tile kernel, (n_items, 8) int32.  Entries 2k and
     2k+1 of the tile-path list share an item when ceil(T/2) of each (T = the
     window's tile count, so 16-column units) sum to at most 8; otherwise each
     is an item of its own, as is a last unpaired entry.  Per item:
     (w0, first tile of w0, T0, nwin | units0 << 8, w1, first tile of w1, T1, 0),
-    the second half zero when nwin = 1."""
+    the second half zero when nwin = 1.  Then one item per slice s of each
+    split window w (point 4 above): (w, first tile + 16 s, its tiles t_s,
+    1 | ceil(t_s/2) << 8 | 1 << 16, n_chunks + 16 B_w + s, S_w, 0, 0)."""
     ptr = b["win_tile_ptr"].astype(np.int64)
     out = []
 
@@ -191,7 +216,47 @@ def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray) -> np.nda
                 out.append([w1, f1, t1, 1 | (((t1 + 1) // 2) << 8), 0, 0, 0, 0])
         else:
             out.append([w0, f0, t0, 1 | (u0 << 8), 0, 0, 0, 0])
+    slices_before = 0
+    for w in split_windows:
+        w = int(w)
+        first, T = int(ptr[w]), int(ptr[w + 1] - ptr[w])
+        S = -(-T // SPLIT_TILES)
+        for sl in range(S):
+            ts = min(SPLIT_TILES, T - SPLIT_TILES * sl)
+            out.append([w, first + SPLIT_TILES * sl, ts, 1 | (((ts + 1) // 2) << 8) | ITEM_PARTIAL,
+                        n_chunks + WIN_ROWS * slices_before + sl, S, 0, 0])
+        slices_before += S
     return np.asarray(out, np.int32).reshape(-1, 8)
+
+
+def merge_list(row_ptr: np.ndarray, b: dict, win_flags: np.ndarray, heavy_threshold: int,
+               heavy_chunk_ptr: np.ndarray, n_chunks: int) -> dict:
+    """The rows a forward merges when the plan has split windows (point 4):
+    ``merge_rows`` ascending and ``merge_ranges`` (n, 2) [begin, end) partial
+    indices -- a split window's row r: n_chunks + 16 B_w + r S_w + [0, S_w);
+    a heavy row outside split windows: its chunks."""
+    deg = degrees(row_ptr)
+    ptr = b["win_tile_ptr"].astype(np.int64)
+    W = len(win_flags)
+    S = np.zeros(W, np.int64)
+    split = (win_flags & FLAG_SPLIT) != 0
+    S[split] = -(-(ptr[1:][split] - ptr[:-1][split]) // SPLIT_TILES)
+    base = np.concatenate([[0], np.cumsum(S)[:-1]])  # slices before each window
+    rows, ranges = [], []
+    heavy_ordinal = 0
+    for r in range(len(deg)):
+        w = r // WIN_ROWS
+        heavy = deg[r] > heavy_threshold
+        if split[w]:
+            lo = n_chunks + WIN_ROWS * int(base[w]) + (r % WIN_ROWS) * int(S[w])
+            rows.append(r)
+            ranges.append([lo, lo + int(S[w])])
+        elif heavy:
+            rows.append(r)
+            ranges.append([int(heavy_chunk_ptr[heavy_ordinal]), int(heavy_chunk_ptr[heavy_ordinal + 1])])
+        heavy_ordinal += int(heavy)
+    return dict(merge_rows=np.asarray(rows, np.int32),
+                merge_ranges=np.asarray(ranges, np.int32).reshape(-1, 2))
 
 
 def full_plan(row_ptr, col_idx, num_nodes, bounds=(32, 256, 2048), heavy_threshold=512,

@@ -41,6 +41,8 @@ ARRAYS = {  # name -> (enum, numpy dtype, trailing shape)
     "tile_windows": (10, np.int32, ()),
     "core_windows": (11, np.int32, ()),
     "tile_items": (12, np.int32, (8,)),
+    "merge_rows": (13, np.int32, ()),
+    "merge_ranges": (14, np.int32, (2,)),
 }
 
 
@@ -68,6 +70,7 @@ class PlanOptions(ctypes.Structure):
         ("tile_pool_density_milli", ctypes.c_int32),
         ("degree_buckets", ctypes.c_int32),
         ("small_graph_rows", ctypes.c_int32),
+        ("tile_split_density_milli", ctypes.c_int32),
     ]
 
 
@@ -88,6 +91,9 @@ class PlanStats(ctypes.Structure):
         ("workspace_used", ctypes.c_size_t),
         ("tile_items", ctypes.c_int64),
         ("small_graph", ctypes.c_int32),
+        ("split_windows", ctypes.c_int64),
+        ("split_items", ctypes.c_int64),
+        ("merge_rows", ctypes.c_int64),
     ]
 
 

@@ -75,6 +75,7 @@ void default_options(g3s_plan_options* o) {
     o->pack_rows = -1;
     o->degree_buckets = 0;
     o->small_graph_rows = kSmallGraphRows;
+    o->tile_split_density_milli = 250;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -112,6 +113,8 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (o.pack_rows < -1 || o.pack_rows > 1) return fail(G3S_ERR_INVALID_ARG, "pack_rows takes -1, 0 or 1");
     if (o.degree_buckets != 0 && o.degree_buckets != 1) return fail(G3S_ERR_INVALID_ARG, "degree_buckets takes 0 or 1");
     if (o.small_graph_rows < 0) return fail(G3S_ERR_INVALID_ARG, "small_graph_rows must be >= 0");
+    if (o.tile_split_density_milli != 0 && (o.tile_split_density_milli < 100 || o.tile_split_density_milli > 1000))
+        return fail(G3S_ERR_INVALID_ARG, "tile_split_density_milli takes 0 (off) or 100..1000");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -138,6 +141,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->tile_density_milli = o.tile_density_milli;
     s->tile_pool_milli = o.tile_pool_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
+    s->tile_split_milli = o.tile_split_density_milli;
     // automatic: on where compiled, unless the caller turned the BSB tiles off
     s->tile_enabled = tile_ok && (o.tile_path == 1 || (o.tile_path == -1 && o.bsb != 0));
     if (s->tile_enabled && o.tile_max_tiles > kTileMaxTilesPerWindow)
@@ -150,6 +154,15 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->max_chunks = E / o.chunk_edges + s->max_heavy;
     s->W = (N + kWinRows - 1) / kWinRows;
     s->max_tiles = s->build_bsb ? (E + 7 * s->W) / kTileCols : 0;
+    // A split window of T > 16 tiles has S = ceil(T / 16) slices, 16 S < 2 T
+    // partial rows, and T <= 1000 nnz / (128 split_milli) tiles.
+    if (s->tile_enabled && s->tile_split_milli > 0) {
+        s->max_split_rows = 2000LL * E / (128LL * s->tile_split_milli) + 16;
+        s->max_split_items = s->max_split_rows / 16 + 1;
+    } else {
+        s->tile_split_milli = 0;
+        s->max_split_rows = s->max_split_items = 0;
+    }
     s->bitmap_words = s->build_bsb ? (N + 31) / 32 : 0;
     const long long scan_n = N > s->W ? N : s->W;
     s->scan_blocks = (scan_n + 1023) / 1024 + 2;
@@ -169,8 +182,8 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
     a->heavy_chunk_ptr = c.take<int32_t>(s.max_heavy + 1);
     a->heavy_index = c.take<int32_t>(s.N);
     a->chunks = c.take<int32_t>(3 * s.max_chunks);
-    a->part_acc = c.take<float>(s.max_chunks * s.H * s.D);
-    a->part_ml = c.take<float>(s.max_chunks * s.H * 2);
+    a->part_acc = c.take<float>((s.max_chunks + s.max_split_rows) * s.H * s.D);
+    a->part_ml = c.take<float>((s.max_chunks + s.max_split_rows) * s.H * 2);
     a->scan_blocks = c.take<int32_t>(s.scan_blocks);
     if (s.build_bsb) {
         a->win_tile_ptr = c.take<int32_t>(s.W + 1);
@@ -178,13 +191,19 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->win_nnz = c.take<int32_t>(s.W);
         a->win_flags = c.take<uint8_t>(s.W);
         a->tile_windows = c.take<int32_t>(s.W);
-        a->tile_items = c.take<int4>(2 * s.W);
+        a->tile_items = c.take<int4>(2 * (s.W + s.max_split_items));
         a->core_windows = c.take<int32_t>(s.W);
         a->large_windows = c.take<int32_t>(s.W);
         a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
         a->tile_bits = c.take<uint32_t>(s.max_tiles * 4);
         a->bitmap_scratch = c.take<uint32_t>((long long)kLargeCtas * 3 * s.bitmap_words);
+        const bool split = s.max_split_rows > 0;
+        a->win_split_base = split ? c.take<int32_t>(s.W) : nullptr;
+        a->merge_rows = split ? c.take<int32_t>(s.N) : nullptr;
+        a->merge_range = split ? c.take<int2>(s.N) : nullptr;
     } else {
+        a->win_split_base = a->merge_rows = nullptr;
+        a->merge_range = nullptr;
         a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
         a->core_windows = nullptr;
         a->tile_items = nullptr;
@@ -323,7 +342,7 @@ g3s_status g3s_plan_create(const int32_t* row_ptr_d, const int32_t* col_idx_d, i
     p->ws_used = need;
     p->edge_id = nullptr;
     p->edge_slots = num_edges;
-    if (hc.n_tile_windows > 0) {
+    if (any_tile(hc)) {
         // the CUDA-core kernel runs here, at the highest priority, so its few
         // CTAs are placed before the tile kernel's waves take every SM
         int least = 0, greatest = 0;
@@ -357,18 +376,21 @@ g3s_status g3s_plan_get_stats(const g3s_plan* p, g3s_plan_stats* st) {
     st->tile_path = p->shape.tile_enabled ? 1 : 0;
     st->windows = p->shape.build_bsb ? p->shape.W : 0;
     st->tiles = p->counts.n_tiles;
-    st->tile_windows = p->counts.n_tile_windows;
+    st->tile_windows = p->counts.n_tile_windows + p->counts.n_split_windows;
     st->dup_windows = p->counts.n_dup_windows;
     st->large_windows = p->counts.n_large_windows;
-    st->tile_window_nnz = p->counts.tile_window_nnz;
+    st->tile_window_nnz = p->counts.tile_window_nnz + p->counts.split_nnz;
     st->pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
     st->pack_limit = p->shape.pack_limit;
     st->heavy_threshold = p->shape.heavy_threshold;
     st->chunk_edges = p->shape.chunk_edges;
     st->short_rows = p->counts.n_short;
     st->workspace_used = p->ws_used;
-    st->tile_items = p->counts.n_tile_items;
-    st->small_graph = p->shape.N <= p->shape.small_rows && p->counts.n_tile_windows == 0 ? 1 : 0;
+    st->tile_items = p->counts.n_tile_items + p->counts.n_split_items;
+    st->small_graph = p->shape.N <= p->shape.small_rows && !any_tile(p->counts) ? 1 : 0;
+    st->split_windows = p->counts.n_split_windows;
+    st->split_items = p->counts.n_split_items;
+    st->merge_rows = p->counts.n_split_windows > 0 ? p->counts.n_merge : p->counts.n_heavy;
     return G3S_OK;
 }
 
@@ -396,11 +418,21 @@ g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_d
         case G3S_ARR_WIN_NNZ: src = p->arr.win_nnz; n = 4 * (size_t)s.W; break;
         case G3S_ARR_WIN_FLAGS: src = p->arr.win_flags; n = (size_t)s.W; break;
         case G3S_ARR_TILE_WINDOWS: src = p->arr.tile_windows; n = 4 * (size_t)c.n_tile_windows; break;
-        case G3S_ARR_CORE_WINDOWS: src = p->arr.core_windows; n = 4 * (size_t)(s.W - c.n_tile_windows); break;
+        case G3S_ARR_CORE_WINDOWS:
+            src = p->arr.core_windows;
+            n = 4 * (size_t)(s.W - c.n_tile_windows - c.n_split_windows);
+            break;
         case G3S_ARR_TILE_ITEMS:
             if (!s.tile_enabled) return fail(G3S_ERR_UNSUPPORTED, "plan was built without the tile path");
             src = p->arr.tile_items;
-            n = 32 * (size_t)c.n_tile_items;
+            n = 32 * (size_t)(c.n_tile_items + c.n_split_items);
+            break;
+        case G3S_ARR_MERGE_ROWS:
+        case G3S_ARR_MERGE_RANGES:
+            if (s.max_split_rows == 0)
+                return fail(G3S_ERR_UNSUPPORTED, "plan was built without split windows (tile path or option off)");
+            src = which == G3S_ARR_MERGE_ROWS ? (const void*)p->arr.merge_rows : (const void*)p->arr.merge_range;
+            n = (which == G3S_ARR_MERGE_ROWS ? 4 : 8) * (size_t)(c.n_split_windows > 0 ? c.n_merge : 0);
             break;
         default: return fail(G3S_ERR_INVALID_ARG, "unknown plan array %d", (int)which);
     }
@@ -448,10 +480,12 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.chunks = p->arr.chunks;
     cp.part_acc = p->arr.part_acc;
     cp.part_ml = p->arr.part_ml;
-    cp.win_flags = p->counts.n_tile_windows > 0 ? p->arr.win_flags : nullptr;
-    if (p->counts.n_tile_windows > 0) {
+    const bool tiles = any_tile(p->counts);
+    const bool split = p->counts.n_split_windows > 0;
+    cp.win_flags = tiles ? p->arr.win_flags : nullptr;
+    if (tiles) {
         cp.core_windows = p->arr.core_windows;
-        cp.n_core_windows = s.W - p->counts.n_tile_windows;
+        cp.n_core_windows = s.W - p->counts.n_tile_windows - p->counts.n_split_windows;
     }
     cp.work_counter = p->arr.work_counter;
     cp.N = s.N;
@@ -467,11 +501,11 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
     cp.elementwise_clamp = p->opts.rtm_elementwise_clamp ? 1 : 0;
     cp.status = p->arr.fwd_status;
     cp.pack_rows = use_packs(p->opts.pack_rows, p->shape, p->counts) ? 1 : 0;
-    if (s.N <= s.small_rows && p->counts.n_tile_windows == 0) {  // one launch: a CTA per row
+    if (s.N <= s.small_rows && !tiles) {  // one launch: a CTA per row
         CUDA_OR_FAIL(core_small_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream), "small-graph kernel launch");
         return G3S_OK;
     }
-    if (p->counts.n_tile_windows > 0) {
+    if (tiles) {
         TileParams tp{};
         tp.Q = Q;
         tp.K = K;
@@ -480,7 +514,9 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.N = s.N;
         tp.H = s.H;
         tp.tile_items = p->arr.tile_items;
-        tp.n_tile_items = p->counts.n_tile_items;
+        tp.n_tile_items = p->counts.n_tile_items + p->counts.n_split_items;
+        tp.part_acc = p->arr.part_acc;
+        tp.part_ml = p->arr.part_ml;
         tp.tile_cols = p->arr.tile_cols;
         tp.tile_bits = p->arr.tile_bits;
         tp.scale_log2 = inv_sqrt_d * 1.4426950408889634f;
@@ -500,14 +536,17 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         CUDA_OR_FAIL(core_launch(p->dtype, p->opts.out_dtype, rtm, cp, stream),
                      "fused kernel launch");
     }
-    if (p->counts.n_chunks > 0) {
+    if (split ? p->counts.n_merge > 0 : p->counts.n_chunks > 0) {
+        // with split windows the merge list holds the heavy rows outside them
+        // (their chunks) and every row of a split window (its slices)
         MergeParams mp{};
-        mp.heavy_rows = p->arr.heavy_rows;
+        mp.heavy_rows = split ? p->arr.merge_rows : p->arr.heavy_rows;
         mp.heavy_chunk_ptr = p->arr.heavy_chunk_ptr;
+        mp.ranges = split ? p->arr.merge_range : nullptr;
         mp.part_acc = p->arr.part_acc;
         mp.part_ml = p->arr.part_ml;
         mp.O = O;
-        mp.n_heavy = p->counts.n_heavy;
+        mp.n_heavy = split ? p->counts.n_merge : p->counts.n_heavy;
         mp.H = s.H;
         mp.D = s.D;
         mp.eps = p->opts.rtm_epsilon;

@@ -647,6 +647,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
     auto run = [&](unsigned long long it) {
         if (it < n_chunks) {
             const int32_t* c = p.chunks + 3 * it;
+            // a heavy row inside a split window is the tile kernel's (its slices)
+            if constexpr (WINS)
+                if (p.win_flags[c[0] >> 4] & kFlagSplit) return;
             process_item<T, OutT, NV, MODE, LPH>(p, L, c[0], c[1], c[2], (long long)it);
             return;
         }
@@ -704,7 +707,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NV == 1 ? (MODE == kModeRtm
 // ---------------------------------------------------------------------------
 // Merge of heavy-row partials: one warp per heavy row and 32-column block,
 // chunks combined in ascending order (m = max m_c, l = sum l_c 2^(m_c - m), O = sum acc_c 2^(m_c - m) / l;
-// RTMScore: plain sums, epsilon added once).
+// RTMScore: plain sums, epsilon added once).  The same merge serves the rows
+// of split windows (their slices' partial states, from the tile kernel; an
+// empty slice has m = -inf and l = 0).
 // ---------------------------------------------------------------------------
 template <typename OutT, bool PLAIN>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergeParams p) {
@@ -719,7 +724,15 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) merge_kernel(const MergePar
     const int x = (int)(w - k * col_blocks) * 32 + lane;
     if (x >= HD) return;
     const int row = p.heavy_rows[k];
-    const int c0 = p.heavy_chunk_ptr[k], c1 = p.heavy_chunk_ptr[k + 1];
+    int c0, c1;
+    if (p.ranges != nullptr) {  // explicit partial ranges (plans with split windows)
+        const int2 r = p.ranges[k];
+        c0 = r.x;
+        c1 = r.y;
+    } else {
+        c0 = p.heavy_chunk_ptr[k];
+        c1 = p.heavy_chunk_ptr[k + 1];
+    }
     const int h = x / p.D;
     const float* ml = p.part_ml + (long long)h * 2;     // chunk c: ml[c * 2H], ml[c * 2H + 1]
     const float* acc = p.part_acc + x;                  // chunk c: acc[c * HD]

@@ -14,6 +14,7 @@ constexpr int kTileCols = 8;   // columns per BSB tile (16x8 tiles)
 constexpr int kFlagDup = 1;    // window holds a repeated (row, source) pair
 constexpr int kFlagTile = 2;   // window takes the tensor-core tile path
 constexpr int kFlagElig = 4;   // planner scratch: window eligible for the tile path (cleared before the plan is done)
+constexpr int kFlagSplit = 8;  // tile-path window cut into 128-column slices (set with kFlagTile)
 constexpr int kWarpsPerCta = 8;
 
 // Error bits written by the CSR validation kernel.
@@ -32,8 +33,12 @@ constexpr int kTileMaxTilesPerWindow = 16;  // tile-path windows have at most th
 // 128 columns: a window of T tiles takes ceil(T/2) units of 16 columns, and a
 // pair is formed from list entries (2k, 2k+1) when their units sum to <= 8.
 // Stored as two int4: (w0, first tile of w0, T0, nwin | units0 << 8) and
-// (w1, first tile of w1, T1, 0).
+// (w1, first tile of w1, T1, 0).  A slice s of a split window w (one item
+// per 16 tiles) is (w, first tile + 16 s, its tiles, 1 | units << 8 |
+// kItemPartial) and (partial index of its row 0, rows' stride S, 0, 0): row
+// r writes its partial softmax state to index base + r S.
 constexpr int kTileItemUnits = 8;
+constexpr int kItemPartial = 1 << 16;
 
 // Small device-resident counters filled by the planner and read back once.
 struct PlanCounts {
@@ -49,6 +54,10 @@ struct PlanCounts {
     long long tile_window_nnz;
     long long elig_nnz, elig_tiles;  // CSR entries and tiles of the tile-eligible windows
     int32_t n_tile_items;  // work items of the tile kernel (one or two tile-path windows each)
+    int32_t n_split_windows;  // tile-path windows cut into 128-column slices
+    int32_t n_split_items;    // their slices (tile items after the n_tile_items pairs)
+    int32_t n_merge;          // rows a forward merges (with split windows; else the heavy rows)
+    long long split_nnz;      // CSR entries of the split windows
 };
 
 // Device views the planner writes into (all inside the caller's workspace).
@@ -60,15 +69,18 @@ struct PlanArrays {
     int32_t* heavy_chunk_ptr;  // [max_heavy+1]
     int32_t* heavy_index;      // [N] scratch: heavy ordinal of a heavy row
     int32_t* chunks;           // [max_chunks][3]
-    float* part_acc;           // [max_chunks][H*d]
-    float* part_ml;            // [max_chunks][H][2]
+    float* part_acc;           // [max_chunks + max_split_rows][H*d]
+    float* part_ml;            // [max_chunks + max_split_rows][H][2]
     // BSB
     int32_t* win_tile_ptr;     // [W+1]
     int32_t* win_ucount;       // [W] unique sources per window (scratch)
     int32_t* win_nnz;          // [W]
     uint8_t* win_flags;        // [W]
     int32_t* tile_windows;     // [W]
-    int4* tile_items;          // [2W] tile kernel items: two int4 per item (see kTileItem* below)
+    int4* tile_items;          // [2 (W + max_split_items)] tile kernel items: two int4 per item (kTileItemUnits)
+    int32_t* win_split_base;   // [W] split windows: slices of the split windows before this one
+    int32_t* merge_rows;       // [N] rows a forward merges when the plan has split windows
+    int2* merge_range;         // [N] their partial index ranges
     int32_t* core_windows;     // [W] the other windows, ascending (rows left to the CUDA-core kernel)
     int32_t* large_windows;    // [W]
     int32_t* tile_cols;        // [max_tiles][8]
@@ -90,9 +102,10 @@ struct PlanShape {
     int heavy_threshold, chunk_edges;
     int bounds[G3S_NUM_BUCKETS - 2];
     int bsb_smem_edges;
-    int tile_density_milli, tile_max_tiles, tile_pool_milli;
+    int tile_density_milli, tile_max_tiles, tile_pool_milli, tile_split_milli;
     bool build_bsb, tile_enabled, bucket_lists;
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
+    int64_t max_split_rows, max_split_items;  // partial rows and items of split windows (0: none possible)
     int64_t scan_blocks;
     int pack_limit;  // most entries of a row a short-row pack takes (0: the row width does not pack)
     long long small_rows;  // graphs of at most this many rows take the small-graph flavour
@@ -116,6 +129,9 @@ inline bool use_packs(int option, const PlanShape& s, const PlanCounts& c) {
     if (s.pack_limit <= 0 || option == 0) return false;
     return option == 1 || 4LL * c.n_short >= s.N;
 }
+
+// Whether a plan has windows on the tile path (pairs or split windows).
+inline bool any_tile(const PlanCounts& c) { return c.n_tile_windows + c.n_split_windows > 0; }
 
 // ---- planner (g3s_planner.cu) --------------------------------------------
 cudaError_t plan_validate(const int32_t* row_ptr, const int32_t* col_idx, const PlanShape& s,
@@ -165,6 +181,7 @@ struct CoreParams {
 struct MergeParams {
     const int32_t* heavy_rows;
     const int32_t* heavy_chunk_ptr;
+    const int2* ranges;  // when set: entry k merges partials [ranges[k].x, ranges[k].y), not the chunk_ptr range
     const float* part_acc;
     const float* part_ml;
     void* O;
@@ -224,6 +241,8 @@ struct TileParams {
     float scale_log2;  // log2(e)/sqrt(d)
     int32_t* status;   // kErrTimeout is OR-ed in when a wait gives up
     unsigned int* work_counter;  // zeroed before the launch; CTAs take work indices from it
+    float* part_acc;             // partial states of split-window slices: [index][H*d] unnormalised output,
+    float* part_ml;              // [index][H][2] (row max in the log2 domain, row sum)
 };
 bool tile_supported(int dtype, int variant, int head_dim);
 cudaError_t wait_selftest_launch(unsigned long long limit_ns, int32_t* status, cudaStream_t st);

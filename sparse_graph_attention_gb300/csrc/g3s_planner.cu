@@ -551,12 +551,15 @@ __global__ void k_tile_ptr_tail(const PlanCounts* c, int32_t* win_tile_ptr, long
 // (their entries / (128 x their tiles)) reaches pool_milli / 1000, and none does
 // otherwise: the two kernels run concurrently but a plan that splits a batch of
 // similar windows between them pays the slower kernel's tail, so the choice is
-// made for the batch.
+// made for the batch.  A window of more than 16 tiles (wider than the kernel's
+// 128 columns) with no repeated pair and a density of at least split_milli /
+// 1000 takes the tile path on its own as a split window, heavy rows included
+// (split_milli = 0: never).
 __global__ void k_tile_eligible(const int32_t* row_ptr, long long N, long long W, const int32_t* win_tile_ptr,
                                 const int32_t* win_nnz, uint8_t* win_flags, bool enabled, int heavy_threshold,
-                                int max_tiles, int density_milli, PlanCounts* c) {
-    int ndup = 0;
-    unsigned long long nnz_sum = 0, tile_sum = 0;
+                                int max_tiles, int density_milli, int split_milli, PlanCounts* c) {
+    int ndup = 0, nsplit = 0;
+    unsigned long long nnz_sum = 0, tile_sum = 0, split_nnz = 0;
     for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < W; w += (long long)gridDim.x * blockDim.x) {
         uint8_t f = win_flags[w];
         if (f & kFlagDup) ++ndup;
@@ -566,8 +569,12 @@ __global__ void k_tile_eligible(const int32_t* row_ptr, long long N, long long W
             int md = 0;
             for (long long r = r0; r < r1; ++r) md = max(md, row_ptr[r + 1] - row_ptr[r]);
             const long long nnz = win_nnz[w];
-            if (nt >= 1 && nt <= max_tiles && md <= heavy_threshold &&
-                1000LL * nnz >= (long long)density_milli * 128LL * nt) {
+            if (split_milli > 0 && nt > kTileMaxTilesPerWindow && 1000LL * nnz >= (long long)split_milli * 128LL * nt) {
+                f |= kFlagTile | kFlagSplit;
+                ++nsplit;
+                split_nnz += (unsigned long long)nnz;
+            } else if (nt >= 1 && nt <= max_tiles && md <= heavy_threshold &&
+                       1000LL * nnz >= (long long)density_milli * 128LL * nt) {
                 f |= kFlagElig;
                 nnz_sum += (unsigned long long)nnz;
                 tile_sum += (unsigned long long)nt;
@@ -576,6 +583,8 @@ __global__ void k_tile_eligible(const int32_t* row_ptr, long long N, long long W
         win_flags[w] = f;
     }
     if (ndup) atomicAdd(&c->n_dup_windows, ndup);
+    if (nsplit) atomicAdd(&c->n_split_windows, nsplit);
+    if (split_nnz) atomicAdd(reinterpret_cast<unsigned long long*>(&c->split_nnz), split_nnz);
     if (nnz_sum) atomicAdd(reinterpret_cast<unsigned long long*>(&c->elig_nnz), nnz_sum);
     if (tile_sum) atomicAdd(reinterpret_cast<unsigned long long*>(&c->elig_tiles), tile_sum);
 }
@@ -633,9 +642,75 @@ struct TilePairOut {
     }
 };
 
-struct TileFlag {
+struct TileFlag {  // tile-path windows of at most 16 tiles (the pairs' list)
     const uint8_t* win_flags;
-    __device__ int operator()(long long w) const { return (win_flags[w] & kFlagTile) ? 1 : 0; }
+    __device__ int operator()(long long w) const { return (win_flags[w] & (kFlagTile | kFlagSplit)) == kFlagTile ? 1 : 0; }
+};
+
+// Split windows: S = ceil(T / 16) slices each, numbered in window order after
+// the pairs' items; the slices before window w (win_split_base) place its
+// partial states at chunks + 16 x base: row r, slice s at + r S + s.
+struct SplitCount {
+    const uint8_t* win_flags;
+    const int32_t* win_tile_ptr;
+    __device__ int operator()(long long w) const {
+        if (!(win_flags[w] & kFlagSplit)) return 0;
+        return (win_tile_ptr[w + 1] - win_tile_ptr[w] + kTileMaxTilesPerWindow - 1) / kTileMaxTilesPerWindow;
+    }
+};
+struct SplitOut {
+    const int32_t* win_tile_ptr;
+    const PlanCounts* c;
+    int32_t* win_split_base;
+    int4* items;
+    __device__ void operator()(long long w, int p, int v) const {
+        if (!v) return;
+        win_split_base[w] = p;
+        const int t0 = win_tile_ptr[w], T = win_tile_ptr[w + 1] - t0;
+        const int base = c->n_chunks + kWinRows * p;
+        int4* it = items + 2LL * (c->n_tile_items + p);
+        for (int sl = 0; sl < v; ++sl) {
+            const int ts = min(kTileMaxTilesPerWindow, T - kTileMaxTilesPerWindow * sl);
+            it[2 * sl] = make_int4((int)w, t0 + kTileMaxTilesPerWindow * sl, ts, 1 | (((ts + 1) / 2) << 8) | kItemPartial);
+            it[2 * sl + 1] = make_int4(base + sl, v, 0, 0);
+        }
+    }
+};
+
+// The rows a forward merges when the plan has split windows: every row of a
+// split window (its slices' partial states) and the heavy rows outside split
+// windows (their chunks), with the partial index range of each.
+struct MergeFlag {
+    const int32_t* row_ptr;
+    const uint8_t* win_flags;
+    int threshold;
+    __device__ int operator()(long long r) const {
+        if (win_flags[r / kWinRows] & kFlagSplit) return 1;
+        return (row_ptr[r + 1] - row_ptr[r]) > threshold ? 1 : 0;
+    }
+};
+struct MergeOut {
+    const uint8_t* win_flags;
+    const int32_t* win_tile_ptr;
+    const int32_t* win_split_base;
+    const int32_t* heavy_index;
+    const int32_t* heavy_chunk_ptr;
+    const PlanCounts* c;
+    int32_t* merge_rows;
+    int2* merge_range;
+    __device__ void operator()(long long r, int p, int v) const {
+        if (!v) return;
+        merge_rows[p] = (int32_t)r;
+        const long long w = r / kWinRows;
+        if (win_flags[w] & kFlagSplit) {
+            const int S = (win_tile_ptr[w + 1] - win_tile_ptr[w] + kTileMaxTilesPerWindow - 1) / kTileMaxTilesPerWindow;
+            const int b = c->n_chunks + kWinRows * win_split_base[w] + (int)(r % kWinRows) * S;
+            merge_range[p] = make_int2(b, b + S);
+        } else {
+            const int h = heavy_index[r];
+            merge_range[p] = make_int2(heavy_chunk_ptr[h], heavy_chunk_ptr[h + 1]);
+        }
+    }
 };
 struct CoreWindowFlag {
     const uint8_t* win_flags;
@@ -748,7 +823,7 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
     if (W > 0) {
         k_tile_eligible<<<grid_for(W, 256), 256, 0, st>>>(row_ptr, s.N, W, a.win_tile_ptr, a.win_nnz, a.win_flags,
                                                           s.tile_enabled, s.heavy_threshold, s.tile_max_tiles,
-                                                          s.tile_density_milli, c);
+                                                          s.tile_density_milli, s.tile_split_milli, c);
         G3S_TRY(cudaGetLastError());
         k_tile_pool<<<grid_for(W, 256), 256, 0, st>>>(W, a.win_flags, s.tile_pool_milli, c);
         G3S_TRY(cudaGetLastError());
@@ -757,6 +832,15 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
     if (s.tile_enabled) {
         const TilePair pr{a.tile_windows, a.win_tile_ptr, c};
         G3S_TRY(scan(pr, TilePairOut{pr, a.tile_items}, (W + 1) / 2, a.scan_blocks, &c->n_tile_items, st));
+    }
+    if (s.max_split_rows > 0) {
+        G3S_TRY(scan(SplitCount{a.win_flags, a.win_tile_ptr},
+                     SplitOut{a.win_tile_ptr, c, a.win_split_base, a.tile_items}, W, a.scan_blocks, &c->n_split_items,
+                     st));
+        G3S_TRY(scan(MergeFlag{row_ptr, a.win_flags, s.heavy_threshold},
+                     MergeOut{a.win_flags, a.win_tile_ptr, a.win_split_base, a.heavy_index, a.heavy_chunk_ptr, c,
+                              a.merge_rows, a.merge_range},
+                     s.N, a.scan_blocks, &c->n_merge, st));
     }
     G3S_TRY(scan(CoreWindowFlag{a.win_flags}, ListOut{a.core_windows}, W, a.scan_blocks, nullptr, st));
     return cudaSuccess;

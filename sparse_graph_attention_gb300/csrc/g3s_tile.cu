@@ -80,6 +80,7 @@ struct TileSmem {
     float part[kHalfWarps][kRows];     // per half-warp: partial row maxima, later partial row sums
     float rowmax[kItemRows];           // row maxima of the item's windows (row 16 j + r)
     float inv_l[kItemRows];            // 1 / row sum of P (0 for a row without entries)
+    float rowsum[kItemRows];           // row sums of P (a split window's slice stores them)
     uint32_t bits[2][kTiles][4];       // tile bitmaps, item i in stage i % 2
     int cols[2][kCols];                // source ids of the item columns, item i in slot i % 2 (-1: none)
     int4 desc[kRing][2];               // item descriptors, item i in slot i % kRing (the head in [1].w)
@@ -145,9 +146,11 @@ __device__ __forceinline__ void store_out<__half>(void* O, long long idx, float 
 
 // An item descriptor: (w0, t0, T0, nwin | units0 << 8), (w1, t1, T1, head).
 // Window j of the item covers rows 16 w_j .. 16 w_j + 15 and tiles t_j ..
-// t_j + T_j - 1; window 1 starts at item column 16 units0.
+// t_j + T_j - 1; window 1 starts at item column 16 units0.  A slice of a
+// split window (kItemPartial set, one window) has (partial index of row 0,
+// row stride, 0, head) in place of the second window.
 __device__ __forceinline__ int item_nwin(const int4& a) { return a.w & 0xff; }
-__device__ __forceinline__ int item_split(const int4& a) { return 16 * (a.w >> 8); }
+__device__ __forceinline__ int item_split(const int4& a) { return 16 * ((a.w >> 8) & 0xff); }
 
 // Source id of item column c (-1: padding or no column).
 __device__ __forceinline__ int item_column(const TileParams& p, const int4& a, const int4& b, int c) {
@@ -307,6 +310,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
         const int nw = item_nwin(a);
         const int f = (warp & 1) * 32 + (tid & 31);
         const int r0 = (warp >> 1) * 8;
+        if (a.w & kItemPartial) {
+            // a split window's slice: the unnormalised rows, and (row max in the
+            // log2 domain, row sum) per row, -inf for a row without entries here
+            float o[kRows];
+            tmem_ld16(tmem + 32 + lane_base, o);
+            const long long rows_left = p.N - ((long long)a.x * kRows + r0);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float v = r0 == 0 ? o[r] : o[8 + r];  // static register indices
+                if (r < rows_left) {
+                    const long long idx = (long long)b.x + (long long)(r0 + r) * b.y;
+                    __stcs(p.part_acc + idx * node_stride + (long long)b.w * kD + f, v);
+                    if (f == 0) {
+                        const float l = sm.rowsum[r0 + r];
+                        const float2 ml = make_float2(l > 0.f ? sm.rowmax[r0 + r] : -INFINITY, l);
+                        *reinterpret_cast<float2*>(p.part_ml + idx * 2 * p.H + 2 * b.w) = ml;
+                    }
+                }
+            }
+            return;
+        }
         for (int j = 0; j < nw; ++j) {
             float o[kRows];
             tmem_ld16(tmem + 32 + 16 * j + lane_base, o);
@@ -469,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
             for (int g = 0; g < kHalfWarps; ++g)
                 if ((nw == 2 && 16 * g >= split) == (j == 1)) l += sm.part[g][r];
             sm.inv_l[tid] = l > 0.f ? 1.0f / l : 0.f;
+            sm.rowsum[tid] = l;
         }
         // read after the next iteration's first barrier
         sm.cols[i & 1][tid] = col2;

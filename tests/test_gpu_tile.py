@@ -99,8 +99,9 @@ def test_tile_full_windows():
 
 
 def test_tile_windows_over_the_limit_stay_on_core():
-    """A window with more than 16 tiles (over 128 unique sources) goes to the
-    CUDA-core kernel; the others of the same graph take the tile path."""
+    """With split windows off, a window with more than 16 tiles (over 128
+    unique sources) goes to the CUDA-core kernel; the others of the same graph
+    take the tile path."""
     rng = np.random.default_rng(14)
     n = 16 * 6
     cols, deg = [], np.zeros(n, np.int64)
@@ -115,7 +116,9 @@ def test_tile_windows_over_the_limit_stay_on_core():
     rp = np.concatenate([rp, np.full(nn - n, rp[-1], np.int32)])
     g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
     vals = graphgen.make_values(nn, g.num_edges, 2, 64, False, seed=15)
-    plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard", plan_kw=dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0))
+    plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard",
+                          plan_kw=dict(tile_path=1, tile_density_milli=0, tile_pool_density_milli=0,
+                                       tile_split_density_milli=0))
     plan.check()
     flags = plan.export("win_flags")
     assert not (flags[0] & 2) and all(flags[1:6] & 2)
@@ -200,6 +203,11 @@ def test_tile_mixed_full_size_persistent_core_rows(H):
 # ---------------------------------------------------------------------------
 # the device planner's tile-path selection, bit-exact with the tile path on
 # ---------------------------------------------------------------------------
+def _split_graph():
+    from test_planner_oracle import _split_graph as make  # the reference planner's split-window pin graph
+    return make()
+
+
 def _mixed_graph():
     a = graphgen.batched_dense(num_graphs=30, seed=11)
     b = graphgen.powerlaw(num_nodes=2003, max_degree=1500, seed=12)
@@ -226,6 +234,13 @@ def _selection_cases():
                                                             bsb_smem_edges=48), True
     yield "mixed_max_tiles", _mixed_graph, 2, dict(tile_density_milli=0, tile_pool_density_milli=0,
                                                    tile_max_tiles=5), True
+    split_kw = dict(heavy_threshold=100, chunk_edges=64, small_graph_rows=0)
+    yield "split_mixed", _split_graph, 2, split_kw, True
+    yield "split_mixed_global_bitmap", _split_graph, 2, dict(split_kw, bsb_smem_edges=256), True
+    yield "split_mixed_dense_only", _split_graph, 2, dict(split_kw, tile_split_density_milli=600), True
+    yield "split_off", _split_graph, 2, dict(split_kw, tile_split_density_milli=0), True
+    yield "clustered_small", lambda: graphgen.make_workload("clustered_heavy", "small")[0], 8, \
+        dict(heavy_threshold=150), True
 
 
 @pytest.mark.parametrize("name,make,H,kw,tiled", list(_selection_cases()), ids=[c[0] for c in _selection_cases()])
@@ -243,20 +258,107 @@ def test_tile_selection_bit_exact(name, make, H, kw, tiled):
     b = ref_planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
     sel = ref_planner.tile_selection(g.row_ptr, b, True, heavy_threshold=st["heavy_threshold"],
                                      max_tiles=opts.tile_max_tiles, density_milli=opts.tile_density_milli,
-                                     pool_milli=opts.tile_pool_density_milli)
+                                     pool_milli=opts.tile_pool_density_milli,
+                                     split_milli=opts.tile_split_density_milli)
+    hc = ref_planner.heavy_chunks(g.row_ptr, st["heavy_threshold"], st["chunk_edges"])
+    n_chunks = hc["chunks"].shape[0]
     ref = dict(b, **sel)
     for arr in ("win_tile_ptr", "tile_cols", "tile_bits", "win_nnz", "win_flags", "tile_windows", "core_windows"):
         got = plan.export(arr)
         want = ref[arr]
         assert got.shape == want.shape and np.array_equal(got, want.astype(got.dtype)), arr
-    assert st["tile_windows"] == sel["tile_windows"].size
-    assert st["tile_window_nnz"] == int(b["win_nnz"][sel["tile_windows"]].sum())
-    want_items = ref_planner.tile_items(g.row_ptr, b, sel["tile_windows"])
+    tw, sw = sel["tile_windows"], sel["split_windows"]
+    assert st["tile_windows"] == tw.size + sw.size and st["split_windows"] == sw.size
+    assert st["tile_window_nnz"] == int(b["win_nnz"][tw].sum() + b["win_nnz"][sw].sum())
+    want_items = ref_planner.tile_items(g.row_ptr, b, tw, sw, n_chunks)
     got_items = plan.export("tile_items")
     assert st["tile_items"] == want_items.shape[0]
     assert got_items.shape == want_items.shape and np.array_equal(got_items, want_items), "tile_items"
+    if sw.size:
+        ml = ref_planner.merge_list(g.row_ptr, b, sel["win_flags"], st["heavy_threshold"], hc["heavy_chunk_ptr"],
+                                    n_chunks)
+        assert st["merge_rows"] == ml["merge_rows"].size
+        assert np.array_equal(plan.export("merge_rows"), ml["merge_rows"]), "merge_rows"
+        assert np.array_equal(plan.export("merge_ranges"), ml["merge_ranges"]), "merge_ranges"
+    if name.startswith("split_mixed"):
+        assert sw.size > 0 and tw.size > 0 and st["chunks"] > 0
     if "bsb_smem_edges" in kw:
         assert st["large_windows"] > 0
     assert (st["tile_windows"] > 0) == tiled
     if name.startswith("mixed") and tiled:
         assert 0 < st["tile_windows"] < st["windows"]
+
+
+# ---------------------------------------------------------------------------
+# split windows: windows wider than 128 columns cut into 128-column slices
+# whose partial softmax states are merged per row
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,H", [("bf16", 2), ("f16", 4), ("bf16", 8)])
+def test_split_windows_parity(dtype, H):
+    """Split windows (heavy rows, light rows and empty rows in them), pairs,
+    CUDA-core windows and heavy-row chunks outside the split windows in one
+    plan, every row against the oracle."""
+    g = _split_graph()
+    plan, _, _ = _run(g, H, dtype, dict(tile_path=1, heavy_threshold=100, chunk_edges=64, small_graph_rows=0))
+    st = plan.stats()
+    assert st["split_windows"] > 0 and st["tile_windows"] > st["split_windows"]
+    assert st["windows"] > st["tile_windows"] and st["chunks"] > 0 and st["merge_rows"] > 0
+
+
+def test_split_windows_off():
+    g = _split_graph()
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, heavy_threshold=100, chunk_edges=64,
+                                         tile_split_density_milli=0))
+    assert plan.stats()["split_windows"] == 0
+
+
+def test_split_windows_sixteen_bit_output():
+    g = _split_graph()
+    plan, O, _ = _run(g, 2, "bf16", dict(tile_path=1, heavy_threshold=100, chunk_edges=64, out_dtype="bf16"))
+    assert O.dtype == torch.bfloat16 and plan.stats()["split_windows"] > 0
+
+
+def test_clustered_heavy_small_workload():
+    """Every window split (two slices of 16 and 8 tiles), every heavy row
+    inside a split window (its chunks skipped), a ragged last window, empty
+    rows."""
+    g, vals, w = graphgen.make_workload("clustered_heavy", "small")
+    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, plan_kw=dict(heavy_threshold=150))
+    plan.check()
+    st = plan.stats()
+    assert st["split_windows"] == st["windows"] and st["chunks"] > 0 and g.num_nodes % 16
+    assert st["merge_rows"] == g.num_nodes
+    assert np.any(g.degrees() == 0)
+
+
+def test_clustered_heavy_full_sampled_rows():
+    """The full clustered workload in the bench's launch configuration (default
+    plan), on every row of four windows and 2000 random rows."""
+    g, vals, w = graphgen.make_workload("clustered_heavy", "full")
+    W = (g.num_nodes + 15) // 16
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([np.arange(16), np.arange(16 * 500, 16 * 501), np.arange(16 * (W - 2), g.num_nodes),
+                                     rng.choice(g.num_nodes, 2000, replace=False)]))
+    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, rows=rows)
+    plan.check()
+    st = plan.stats()
+    # windows that drew many light rows fall under the split density and stay
+    # on the CUDA-core path
+    assert 0.9 * W < st["split_windows"] < W and st["split_items"] > 16 * st["split_windows"]
+
+
+def test_split_plan_aggregate():
+    """g3s_aggregate on a plan with split windows takes every row through the
+    CUDA-core kernel and the heavy-row chunks (the split windows are the
+    forward's alone)."""
+    g = _split_graph()
+    rp, ci = upload_graph(g)
+    plan = g3s.Plan(rp, ci, g.num_nodes, 2, 64, "bf16", tile_path=1, heavy_threshold=100, chunk_edges=64)
+    assert plan.stats()["split_windows"] > 0
+    rng = np.random.default_rng(5)
+    wt = torch.from_numpy(rng.random((g.num_edges, 2), dtype=np.float32) + 0.1).to(torch.bfloat16)
+    xt = torch.from_numpy(rng.standard_normal((g.num_nodes, 2, 64), dtype=np.float32)).to(torch.bfloat16)
+    O = plan.aggregate(wt.to(device()), xt.to(device()), normalize=True, eps=1e-6)
+    torch.cuda.synchronize()
+    want = oracle.aggregate(g.row_ptr, g.col_idx, g.num_nodes, 2, 64, "bf16", wt, xt, normalize=True, eps=1e-6)
+    assert_close(O, want, "bf16", "O (aggregate)")

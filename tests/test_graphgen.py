@@ -24,7 +24,7 @@ def test_small_workloads_are_valid_and_seeded(name):
     g2, v2, _ = graphgen.make_workload(name, "small")
     assert np.array_equal(g1.row_ptr, g2.row_ptr) and np.array_equal(g1.col_idx, g2.col_idx)
     assert all(np.array_equal(v1[k], v2[k]) for k in v1)
-    _check_csr(g1, self_loops_allowed=name in ("batched_dense", "batched_complete"))
+    _check_csr(g1, self_loops_allowed=name in ("batched_dense", "batched_complete", "clustered_heavy"))
     assert v1["Q"].shape == (g1.num_nodes, w.heads, w.head_dim)
     if w.variant == "rtmscore":
         assert v1["E"].shape == (g1.num_edges, w.heads, w.head_dim)
@@ -80,3 +80,17 @@ def test_powerlaw_small_structure():
     _check_csr(g)
     d = g.degrees()
     assert 13 < d.mean() < 15.5 and d.max() > 500
+
+
+def test_clustered_heavy_full():
+    """Heavy rows take 1024 distinct sources from their window's pool of 2048,
+    light rows 8 uniform ones, about 3 : 1."""
+    g = graphgen.clustered_heavy()
+    _check_csr(g, self_loops_allowed=True)
+    deg = g.degrees()
+    assert g.num_nodes == 16384 and set(np.unique(deg)) == {8, 1024}
+    assert 0.7 < np.mean(deg == 1024) < 0.8
+    w = 37
+    heavy_rows = [r for r in range(16 * w, 16 * w + 16) if deg[r] == 1024]
+    pool = np.unique(np.concatenate([g.col_idx[g.row_ptr[r]:g.row_ptr[r + 1]] for r in heavy_rows]))
+    assert pool.size <= 2048

@@ -179,3 +179,88 @@ def test_tile_items_pairing():
     pairs = sum(1 for it in items if (it[3] & 0xFF) == 2)
     want_pairs = sum(1 for k in range(0, len(tw) - 1, 2) if units[k] + units[k + 1] <= 8)
     assert pairs == want_pairs and 0 < pairs < len(tw) // 2 + 1
+
+
+def _split_graph():
+    """Windows of every kind: clustered heavy-row windows (split), a sparse
+    wide window (too sparse to split), batched windows (pairs) and a ragged
+    tail of random rows, with empty rows among them."""
+    parts = [graphgen.clustered_heavy(num_windows=12, pool=300, degree=150, light_frac=0.2, empty_frac=0.1, seed=21),
+             graphgen.clustered_heavy(num_windows=12, pool=1000, degree=30, light_frac=0.0, seed=22),
+             graphgen.batched_dense(num_graphs=6, seed=23),
+             graphgen.random_csr(37, 9, seed=24, zero_frac=0.3)]
+    n, rp, cols = 0, [np.zeros(1, np.int64)], []
+    for g in parts:
+        rp.append(rp[-1][-1] + g.row_ptr[1:])
+        cols.append(g.col_idx.astype(np.int64) + n)
+        n += g.num_nodes
+    return graphgen.Graph(np.concatenate(rp).astype(np.int32), np.concatenate(cols).astype(np.int32))
+
+
+def test_split_windows_invariants():
+    """Split selection, slice items and the merge list of the reference planner:
+    a split window is exactly a window of more than 16 tiles, no repeated pair
+    and density >= split_milli / 1000; its slices cover its tiles in order, 16
+    at a time; the partial indices of (slice, row) pairs cover [n_chunks,
+    n_chunks + 16 x slices) once each; the merge list holds every row of a split
+    window with the indices its slices write, and every other heavy row with its
+    chunks."""
+    g = _split_graph()
+    b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    deg = g.degrees()
+    T = 100
+    hc = planner.heavy_chunks(g.row_ptr, T, 64)
+    n_chunks = hc["chunks"].shape[0]
+    ptr = b["win_tile_ptr"].astype(np.int64)
+    nt = np.diff(ptr)
+    W = nt.size
+    for split_milli in (250, 500):
+        sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=T, max_tiles=16, density_milli=100,
+                                     pool_milli=0, split_milli=split_milli)
+        fl = sel["win_flags"]
+        split = [w for w in range(W) if fl[w] & planner.FLAG_SPLIT]
+        for w in range(W):
+            dense = b["win_nnz"][w] * 1000 >= split_milli * 128 * nt[w]
+            assert (w in split) == (bool(nt[w] > 16) and not b["win_dup"][w] and bool(dense)), w
+            if w in split:
+                assert fl[w] & planner.FLAG_TILE
+        assert 0 < len(split) < W
+        assert set(split).isdisjoint(sel["tile_windows"]) and set(split).isdisjoint(sel["core_windows"])
+        assert sorted(list(sel["tile_windows"]) + split + list(sel["core_windows"])) == list(range(W))
+        items = planner.tile_items(g.row_ptr, b, sel["tile_windows"], sel["split_windows"], n_chunks)
+        n_pair = planner.tile_items(g.row_ptr, b, sel["tile_windows"]).shape[0]
+        sitems = items[n_pair:]
+        assert np.all(sitems[:, 3] & planner.ITEM_PARTIAL) and not np.any(items[:n_pair, 3] & planner.ITEM_PARTIAL)
+        hit = {}
+        k = 0
+        for w in split:
+            S = -(-int(nt[w]) // 16)
+            mine = sitems[k:k + S]
+            k += S
+            assert np.all(mine[:, 0] == w) and np.all(mine[:, 5] == S)
+            assert mine[0, 1] == ptr[w] and np.all(mine[1:, 1] == mine[:-1, 1] + 16)
+            assert mine[:, 2].sum() == nt[w] and np.all(mine[:-1, 2] == 16)
+            assert np.all((mine[:, 3] & 0xFF) == 1) and np.all(((mine[:, 3] >> 8) & 0xFF) == (mine[:, 2] + 1) // 2)
+            for it in mine:
+                for r in range(16):
+                    hit.setdefault(int(it[4] + r * S), []).append((w, r))
+        assert k == len(sitems)
+        total = 16 * sum(-(-int(nt[w]) // 16) for w in split)
+        assert sorted(hit) == list(range(n_chunks, n_chunks + total)) and all(len(v) == 1 for v in hit.values())
+        ml = planner.merge_list(g.row_ptr, b, fl, T, hc["heavy_chunk_ptr"], n_chunks)
+        rows, ranges = list(ml["merge_rows"]), ml["merge_ranges"]
+        heavy = list(hc["heavy_rows"])
+        want = sorted(set(r for r in range(g.num_nodes) if (r // 16) in split) |
+                      set(r for r in heavy if (r // 16) not in split))
+        assert rows == want
+        for r, (lo, hi) in zip(rows, ranges):
+            if (r // 16) in split:
+                assert sorted(hit_r for hit_r, v in hit.items() if v[0] == (r // 16, r % 16)) == list(range(lo, hi))
+            else:
+                i = heavy.index(r)
+                assert (lo, hi) == (hc["heavy_chunk_ptr"][i], hc["heavy_chunk_ptr"][i + 1])
+                assert np.array_equal(hc["chunks"][lo:hi, 0], np.full(hi - lo, r))
+        # a heavy row inside a split window is merged from its slices, not its chunks
+        assert any(deg[r] > T and (r // 16) in split for r in range(g.num_nodes))
+    off = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=T, max_tiles=16, density_milli=100, split_milli=0)
+    assert not np.any(off["win_flags"] & planner.FLAG_SPLIT)
