@@ -504,6 +504,9 @@ def parse_args():
                     help="density cutoff of the tile path in 1/1000 (default: the library's)")
     ap.add_argument("--tile-pool-density-milli", type=int, default=None,
                     help="pooled density the tile-eligible windows need to take the tile path (default: the library's)")
+    ap.add_argument("--tile-split-parallel", type=int, default=None, choices=[0, 1],
+                    help="split windows (wider than 128 columns): 0 node-parallel chains, 1 edge-parallel slices "
+                         "merged (default: the library's)")
     ap.add_argument("--out-dtype", default=None, choices=["f32", "f16", "bf16"],
                     help="element type of O (default fp32)")
     ap.add_argument("--graph", action="store_true",
@@ -722,6 +725,8 @@ def main():
         plan_kw["tile_density_milli"] = args.tile_density_milli
     if args.tile_pool_density_milli is not None:
         plan_kw["tile_pool_density_milli"] = args.tile_pool_density_milli
+    if args.tile_split_parallel is not None:
+        plan_kw["tile_split_parallel"] = args.tile_split_parallel
     if args.pack_rows is not None:
         plan_kw["pack_rows"] = args.pack_rows
     plan = g3s.Plan(rp, ci, g.num_nodes, w.heads, w.head_dim, w.dtype, w.variant, **plan_kw)

@@ -179,6 +179,7 @@ typedef struct g3s_plan_options {
     int32_t degree_buckets;
     int32_t small_graph_rows;
     int32_t tile_split_density_milli;
+    int32_t tile_split_parallel;
 } g3s_plan_options;
 
 typedef struct g3s_plan_stats {

@@ -41,13 +41,16 @@ Three outputs, all integer, all unique under the canonical orderings below.
    takes the tile path on its own (bits 1 and 3 of ``win_flags``), heavy rows
    included; it is not in ``tile_windows`` (the pairs' list) nor in
    ``core_windows``.  It is cut into S_w = ceil(T_w / 16) slices of 16 tiles,
-   one tile item each, after the pairs' items, windows ascending.  Window w's
-   partial states occupy indices n_chunks + 16 B_w .. n_chunks + 16 (B_w + S_w)
-   - 1, B_w = the slices of the split windows before w: row r, slice s at
-   n_chunks + 16 B_w + r S_w + s.  A forward then merges (``merge_rows``,
-   ascending, with ``merge_ranges`` [begin, end)) every row of a split window
-   over its S_w partials and every heavy row outside split windows over its
-   chunks.
+   one tile item each, after the pairs' items, windows ascending.
+   Edge-parallel, window w's partial states occupy indices n_chunks + 16 B_w
+   .. n_chunks + 16 (B_w + S_w) - 1, B_w = the slices of the split windows
+   before w: row r, slice s at n_chunks + 16 B_w + r S_w + s, and a forward
+   merges (``merge_rows``, ascending, with ``merge_ranges`` [begin, end))
+   every row of a split window over its S_w partials and every heavy row
+   outside split windows over its chunks.  Node-parallel, one CTA takes a
+   window's slices in order (a slice carries s and S_w), the split windows'
+   rows need no merge, and the merge list holds the heavy rows outside split
+   windows only.
 """
 from __future__ import annotations
 
@@ -60,6 +63,7 @@ FLAG_TILE = 2
 FLAG_SPLIT = 8
 SPLIT_TILES = 16   # tiles per slice of a split window (128 columns)
 ITEM_PARTIAL = 1 << 16
+ITEM_CHAIN = 1 << 17
 
 
 def degrees(row_ptr: np.ndarray) -> np.ndarray:
@@ -187,7 +191,8 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
     return dict(win_flags=flags, tile_windows=tile_windows, split_windows=split_windows, core_windows=core_windows)
 
 
-def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_windows=(), n_chunks: int = 0) -> np.ndarray:
+def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_windows=(), n_chunks: int = 0,
+               edge_parallel: bool = False) -> np.ndarray:
     """Work items of the tile kernel, (n_items, 8) int32.  Entries 2k and
     2k+1 of the tile-path list share an item when ceil(T/2) of each (T = the
     window's tile count, so 16-column units) sum to at most 8; otherwise each
@@ -195,7 +200,9 @@ def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_win
     (w0, first tile of w0, T0, nwin | units0 << 8, w1, first tile of w1, T1, 0),
     the second half zero when nwin = 1.  Then one item per slice s of each
     split window w (point 4 above): (w, first tile + 16 s, its tiles t_s,
-    1 | ceil(t_s/2) << 8 | 1 << 16, n_chunks + 16 B_w + s, S_w, 0, 0)."""
+    1 | ceil(t_s/2) << 8 | 1 << 16, n_chunks + 16 B_w + s, S_w, 0, 0)
+    edge-parallel, (w, first tile + 16 s, t_s, 1 | ceil(t_s/2) << 8 | 1 << 17,
+    s, S_w, 0, 0) node-parallel."""
     ptr = b["win_tile_ptr"].astype(np.int64)
     out = []
 
@@ -223,18 +230,21 @@ def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_win
         S = -(-T // SPLIT_TILES)
         for sl in range(S):
             ts = min(SPLIT_TILES, T - SPLIT_TILES * sl)
-            out.append([w, first + SPLIT_TILES * sl, ts, 1 | (((ts + 1) // 2) << 8) | ITEM_PARTIAL,
-                        n_chunks + WIN_ROWS * slices_before + sl, S, 0, 0])
+            if edge_parallel:
+                out.append([w, first + SPLIT_TILES * sl, ts, 1 | (((ts + 1) // 2) << 8) | ITEM_PARTIAL,
+                            n_chunks + WIN_ROWS * slices_before + sl, S, 0, 0])
+            else:
+                out.append([w, first + SPLIT_TILES * sl, ts, 1 | (((ts + 1) // 2) << 8) | ITEM_CHAIN, sl, S, 0, 0])
         slices_before += S
     return np.asarray(out, np.int32).reshape(-1, 8)
 
 
 def merge_list(row_ptr: np.ndarray, b: dict, win_flags: np.ndarray, heavy_threshold: int,
-               heavy_chunk_ptr: np.ndarray, n_chunks: int) -> dict:
+               heavy_chunk_ptr: np.ndarray, n_chunks: int, edge_parallel: bool = False) -> dict:
     """The rows a forward merges when the plan has split windows (point 4):
     ``merge_rows`` ascending and ``merge_ranges`` (n, 2) [begin, end) partial
-    indices -- a split window's row r: n_chunks + 16 B_w + r S_w + [0, S_w);
-    a heavy row outside split windows: its chunks."""
+    indices -- edge-parallel, a split window's row r: n_chunks + 16 B_w + r S_w
+    + [0, S_w); a heavy row outside split windows: its chunks."""
     deg = degrees(row_ptr)
     ptr = b["win_tile_ptr"].astype(np.int64)
     W = len(win_flags)
@@ -248,9 +258,10 @@ def merge_list(row_ptr: np.ndarray, b: dict, win_flags: np.ndarray, heavy_thresh
         w = r // WIN_ROWS
         heavy = deg[r] > heavy_threshold
         if split[w]:
-            lo = n_chunks + WIN_ROWS * int(base[w]) + (r % WIN_ROWS) * int(S[w])
-            rows.append(r)
-            ranges.append([lo, lo + int(S[w])])
+            if edge_parallel:
+                lo = n_chunks + WIN_ROWS * int(base[w]) + (r % WIN_ROWS) * int(S[w])
+                rows.append(r)
+                ranges.append([lo, lo + int(S[w])])
         elif heavy:
             rows.append(r)
             ranges.append([int(heavy_chunk_ptr[heavy_ordinal]), int(heavy_chunk_ptr[heavy_ordinal + 1])])

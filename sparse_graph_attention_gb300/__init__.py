@@ -71,6 +71,7 @@ class PlanOptions(ctypes.Structure):
         ("degree_buckets", ctypes.c_int32),
         ("small_graph_rows", ctypes.c_int32),
         ("tile_split_density_milli", ctypes.c_int32),
+        ("tile_split_parallel", ctypes.c_int32),
     ]
 
 

@@ -76,6 +76,7 @@ void default_options(g3s_plan_options* o) {
     o->degree_buckets = 0;
     o->small_graph_rows = kSmallGraphRows;
     o->tile_split_density_milli = 250;
+    o->tile_split_parallel = 0;
 }
 
 bool tile_path_compiled(int dtype, int variant, int head_dim) { return tile_supported(dtype, variant, head_dim); }
@@ -115,6 +116,8 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     if (o.small_graph_rows < 0) return fail(G3S_ERR_INVALID_ARG, "small_graph_rows must be >= 0");
     if (o.tile_split_density_milli != 0 && (o.tile_split_density_milli < 100 || o.tile_split_density_milli > 1000))
         return fail(G3S_ERR_INVALID_ARG, "tile_split_density_milli takes 0 (off) or 100..1000");
+    if (o.tile_split_parallel != 0 && o.tile_split_parallel != 1)
+        return fail(G3S_ERR_INVALID_ARG, "tile_split_parallel takes 0 (node-parallel) or 1 (edge-parallel)");
 
     const bool tile_ok = tile_path_compiled(dtype, variant, head_dim);
     if (o.tile_path == 1 && !tile_ok)
@@ -142,6 +145,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     s->tile_pool_milli = o.tile_pool_density_milli;
     s->tile_max_tiles = o.tile_max_tiles;
     s->tile_split_milli = o.tile_split_density_milli;
+    s->split_edge_parallel = o.tile_split_parallel == 1;
     // automatic: on where compiled, unless the caller turned the BSB tiles off
     s->tile_enabled = tile_ok && (o.tile_path == 1 || (o.tile_path == -1 && o.bsb != 0));
     if (s->tile_enabled && o.tile_max_tiles > kTileMaxTilesPerWindow)
@@ -157,8 +161,9 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
     // A split window of T > 16 tiles has S = ceil(T / 16) slices, 16 S < 2 T
     // partial rows, and T <= 1000 nnz / (128 split_milli) tiles.
     if (s->tile_enabled && s->tile_split_milli > 0) {
-        s->max_split_rows = 2000LL * E / (128LL * s->tile_split_milli) + 16;
-        s->max_split_items = s->max_split_rows / 16 + 1;
+        const long long rows = 2000LL * E / (128LL * s->tile_split_milli) + 16;
+        s->max_split_items = rows / 16 + 1;
+        s->max_split_rows = s->split_edge_parallel ? rows : 0;  // partial states: edge-parallel only
     } else {
         s->tile_split_milli = 0;
         s->max_split_rows = s->max_split_items = 0;
@@ -197,13 +202,14 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
         a->tile_bits = c.take<uint32_t>(s.max_tiles * 4);
         a->bitmap_scratch = c.take<uint32_t>((long long)kLargeCtas * 3 * s.bitmap_words);
-        const bool split = s.max_split_rows > 0;
+        const bool split = s.max_split_items > 0;
         a->win_split_base = split ? c.take<int32_t>(s.W) : nullptr;
         a->merge_rows = split ? c.take<int32_t>(s.N) : nullptr;
         a->merge_range = split ? c.take<int2>(s.N) : nullptr;
+        a->chains = split && !s.split_edge_parallel ? c.take<int2>(s.W) : nullptr;
     } else {
         a->win_split_base = a->merge_rows = nullptr;
-        a->merge_range = nullptr;
+        a->merge_range = a->chains = nullptr;
         a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
         a->core_windows = nullptr;
         a->tile_items = nullptr;
@@ -429,7 +435,7 @@ g3s_status g3s_plan_export(const g3s_plan* p, g3s_plan_array which, void* host_d
             break;
         case G3S_ARR_MERGE_ROWS:
         case G3S_ARR_MERGE_RANGES:
-            if (s.max_split_rows == 0)
+            if (s.max_split_items == 0)
                 return fail(G3S_ERR_UNSUPPORTED, "plan was built without split windows (tile path or option off)");
             src = which == G3S_ARR_MERGE_ROWS ? (const void*)p->arr.merge_rows : (const void*)p->arr.merge_range;
             n = (which == G3S_ARR_MERGE_ROWS ? 4 : 8) * (size_t)(c.n_split_windows > 0 ? c.n_merge : 0);
@@ -514,7 +520,9 @@ g3s_status g3s_forward(const g3s_plan* p, const void* Q, const void* K, const vo
         tp.N = s.N;
         tp.H = s.H;
         tp.tile_items = p->arr.tile_items;
-        tp.n_tile_items = p->counts.n_tile_items + p->counts.n_split_items;
+        tp.n_single_items = p->counts.n_tile_items + (s.split_edge_parallel ? p->counts.n_split_items : 0);
+        tp.chains = p->arr.chains;
+        tp.n_chains = s.split_edge_parallel ? 0 : p->counts.n_split_windows;
         tp.part_acc = p->arr.part_acc;
         tp.part_ml = p->arr.part_ml;
         tp.tile_cols = p->arr.tile_cols;

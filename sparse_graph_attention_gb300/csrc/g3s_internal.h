@@ -33,12 +33,15 @@ constexpr int kTileMaxTilesPerWindow = 16;  // tile-path windows have at most th
 // 128 columns: a window of T tiles takes ceil(T/2) units of 16 columns, and a
 // pair is formed from list entries (2k, 2k+1) when their units sum to <= 8.
 // Stored as two int4: (w0, first tile of w0, T0, nwin | units0 << 8) and
-// (w1, first tile of w1, T1, 0).  A slice s of a split window w (one item
-// per 16 tiles) is (w, first tile + 16 s, its tiles, 1 | units << 8 |
-// kItemPartial) and (partial index of its row 0, rows' stride S, 0, 0): row
-// r writes its partial softmax state to index base + r S.
+// (w1, first tile of w1, T1, 0).  A slice s of the S slices of a split window
+// w (one item per 16 tiles) is (w, first tile + 16 s, its tiles, 1 | units <<
+// 8 | flag) and, edge-parallel (kItemPartial), (partial index of its row 0,
+// S, 0, 0): row r writes its partial softmax state to index base + r S; or,
+// node-parallel (kItemChain: the CTA takes the window's slices in order),
+// (s, S, 0, 0).
 constexpr int kTileItemUnits = 8;
 constexpr int kItemPartial = 1 << 16;
+constexpr int kItemChain = 1 << 17;
 
 // Small device-resident counters filled by the planner and read back once.
 struct PlanCounts {
@@ -81,6 +84,7 @@ struct PlanArrays {
     int32_t* win_split_base;   // [W] split windows: slices of the split windows before this one
     int32_t* merge_rows;       // [N] rows a forward merges when the plan has split windows
     int2* merge_range;         // [N] their partial index ranges
+    int2* chains;              // [W] node-parallel split windows: (first slice item, slices)
     int32_t* core_windows;     // [W] the other windows, ascending (rows left to the CUDA-core kernel)
     int32_t* large_windows;    // [W]
     int32_t* tile_cols;        // [max_tiles][8]
@@ -103,9 +107,10 @@ struct PlanShape {
     int bounds[G3S_NUM_BUCKETS - 2];
     int bsb_smem_edges;
     int tile_density_milli, tile_max_tiles, tile_pool_milli, tile_split_milli;
+    bool split_edge_parallel;  // split windows: slices merged from partial states (else chains)
     bool build_bsb, tile_enabled, bucket_lists;
     int64_t max_heavy, max_chunks, W, max_tiles, bitmap_words;
-    int64_t max_split_rows, max_split_items;  // partial rows and items of split windows (0: none possible)
+    int64_t max_split_rows, max_split_items;  // partial rows (edge-parallel) and items of split windows
     int64_t scan_blocks;
     int pack_limit;  // most entries of a row a short-row pack takes (0: the row width does not pack)
     long long small_rows;  // graphs of at most this many rows take the small-graph flavour
@@ -235,7 +240,9 @@ struct TileParams {
     long long N;
     int H;
     const int4* tile_items;  // two int4 per item (kTileItemUnits above)
-    long long n_tile_items;
+    long long n_single_items;  // items taken one work index each (pairs, edge-parallel slices)
+    const int2* chains;        // node-parallel split windows: (first slice item, slices), one work index each
+    int n_chains;
     const int32_t* tile_cols;
     const uint32_t* tile_bits;
     float scale_log2;  // log2(e)/sqrt(d)

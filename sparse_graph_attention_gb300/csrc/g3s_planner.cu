@@ -648,8 +648,10 @@ struct TileFlag {  // tile-path windows of at most 16 tiles (the pairs' list)
 };
 
 // Split windows: S = ceil(T / 16) slices each, numbered in window order after
-// the pairs' items; the slices before window w (win_split_base) place its
-// partial states at chunks + 16 x base: row r, slice s at + r S + s.
+// the pairs' items.  Edge-parallel, the slices before window w
+// (win_split_base) place its partial states at chunks + 16 x base: row r,
+// slice s at + r S + s; node-parallel, a slice carries (s, S) and the
+// window's chain entry (first slice item, S) is one work unit.
 struct SplitCount {
     const uint8_t* win_flags;
     const int32_t* win_tile_ptr;
@@ -663,6 +665,7 @@ struct SplitOut {
     const PlanCounts* c;
     int32_t* win_split_base;
     int4* items;
+    bool edge_parallel;
     __device__ void operator()(long long w, int p, int v) const {
         if (!v) return;
         win_split_base[w] = p;
@@ -671,21 +674,39 @@ struct SplitOut {
         int4* it = items + 2LL * (c->n_tile_items + p);
         for (int sl = 0; sl < v; ++sl) {
             const int ts = min(kTileMaxTilesPerWindow, T - kTileMaxTilesPerWindow * sl);
-            it[2 * sl] = make_int4((int)w, t0 + kTileMaxTilesPerWindow * sl, ts, 1 | (((ts + 1) / 2) << 8) | kItemPartial);
-            it[2 * sl + 1] = make_int4(base + sl, v, 0, 0);
+            it[2 * sl] = make_int4((int)w, t0 + kTileMaxTilesPerWindow * sl, ts,
+                                   1 | (((ts + 1) / 2) << 8) | (edge_parallel ? kItemPartial : kItemChain));
+            it[2 * sl + 1] = make_int4(edge_parallel ? base + sl : sl, v, 0, 0);
         }
     }
 };
+struct SplitFlag {
+    const uint8_t* win_flags;
+    __device__ int operator()(long long w) const { return (win_flags[w] & kFlagSplit) ? 1 : 0; }
+};
+struct ChainOut {
+    const int32_t* win_tile_ptr;
+    const int32_t* win_split_base;
+    const PlanCounts* c;
+    int2* chains;
+    __device__ void operator()(long long w, int p, int v) const {
+        if (!v) return;
+        const int S = (win_tile_ptr[w + 1] - win_tile_ptr[w] + kTileMaxTilesPerWindow - 1) / kTileMaxTilesPerWindow;
+        chains[p] = make_int2(c->n_tile_items + win_split_base[w], S);
+    }
+};
 
-// The rows a forward merges when the plan has split windows: every row of a
-// split window (its slices' partial states) and the heavy rows outside split
-// windows (their chunks), with the partial index range of each.
+// The rows a forward merges when the plan has split windows: the heavy rows
+// outside split windows (their chunks) and, edge-parallel, every row of a
+// split window (its slices' partial states), with the partial index range of
+// each.  (Node-parallel, a split window's rows are final in the tile kernel.)
 struct MergeFlag {
     const int32_t* row_ptr;
     const uint8_t* win_flags;
     int threshold;
+    bool edge_parallel;
     __device__ int operator()(long long r) const {
-        if (win_flags[r / kWinRows] & kFlagSplit) return 1;
+        if (win_flags[r / kWinRows] & kFlagSplit) return edge_parallel ? 1 : 0;
         return (row_ptr[r + 1] - row_ptr[r]) > threshold ? 1 : 0;
     }
 };
@@ -833,11 +854,14 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
         const TilePair pr{a.tile_windows, a.win_tile_ptr, c};
         G3S_TRY(scan(pr, TilePairOut{pr, a.tile_items}, (W + 1) / 2, a.scan_blocks, &c->n_tile_items, st));
     }
-    if (s.max_split_rows > 0) {
+    if (s.max_split_items > 0) {
         G3S_TRY(scan(SplitCount{a.win_flags, a.win_tile_ptr},
-                     SplitOut{a.win_tile_ptr, c, a.win_split_base, a.tile_items}, W, a.scan_blocks, &c->n_split_items,
-                     st));
-        G3S_TRY(scan(MergeFlag{row_ptr, a.win_flags, s.heavy_threshold},
+                     SplitOut{a.win_tile_ptr, c, a.win_split_base, a.tile_items, s.split_edge_parallel}, W,
+                     a.scan_blocks, &c->n_split_items, st));
+        if (!s.split_edge_parallel)
+            G3S_TRY(scan(SplitFlag{a.win_flags}, ChainOut{a.win_tile_ptr, a.win_split_base, c, a.chains}, W,
+                         a.scan_blocks, nullptr, st));
+        G3S_TRY(scan(MergeFlag{row_ptr, a.win_flags, s.heavy_threshold, s.split_edge_parallel},
                      MergeOut{a.win_flags, a.win_tile_ptr, a.win_split_base, a.heavy_index, a.heavy_chunk_ptr, c,
                               a.merge_rows, a.merge_range},
                      s.N, a.scan_blocks, &c->n_merge, st));

@@ -44,7 +44,16 @@
 // row maxima; S^T of item i+1 is issued as soon as its K and Q have landed,
 // and runs while item i forms P; O^T of item i follows once its V rows are
 // in.  Work indices come from one counter; one thread keeps the descriptors
-// of the next three items in a shared-memory ring.  Every mbarrier wait is
+// of the next three items in a shared-memory ring.
+//
+// Windows wider than 128 columns (split windows) are cut into 128-column
+// slices, taken either edge-parallel (each slice an item of its own that
+// writes a partial softmax state per row, merged per row afterwards) or
+// node-parallel (a chain: one CTA takes all slices of a window and head in a
+// row, O^T accumulating in TMEM across them, with a lazily moved reference
+// max per row: O^T and the row sums are rescaled only when a slice's max
+// exceeds the reference by more than 2^8; the rows are stored after the last
+// slice).  Every mbarrier wait is
 // bounded (about one second of %globaltimer); on expiry the CTA sets the
 // plan's status word, frees its TMEM and returns.
 #include <cuda_bf16.h>
@@ -70,6 +79,7 @@ constexpr int kItemRows = kMaxWin * kRows;     // 32
 constexpr int kHalfWarps = kCols / 16;         // 8 half-warps of 16 columns
 constexpr uint32_t kTmemCols = 64;             // S^T [0, 32), O^T [32, 64) (window j at +16 j)
 constexpr int kRing = 8;                       // item descriptor ring
+constexpr float kLazyRescale = 8.f;            // a chain moves its reference max only past +8 (P <= 2^8)
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 struct TileSmem {
@@ -81,6 +91,9 @@ struct TileSmem {
     float rowmax[kItemRows];           // row maxima of the item's windows (row 16 j + r)
     float inv_l[kItemRows];            // 1 / row sum of P (0 for a row without entries)
     float rowsum[kItemRows];           // row sums of P (a split window's slice stores them)
+    float mref[kRows];                 // a chain's reference row maxima (log2 domain), carried over its slices
+    float fac[kRows];                  // this slice's rescale of the chain's O and row sums (1: none)
+    float lacc[kRows];                 // a chain's row sums so far
     uint32_t bits[2][kTiles][4];       // tile bitmaps, item i in stage i % 2
     int cols[2][kCols];                // source ids of the item columns, item i in slot i % 2 (-1: none)
     int4 desc[kRing][2];               // item descriptors, item i in slot i % kRing (the head in [1].w)
@@ -196,7 +209,9 @@ __device__ __forceinline__ float halfwarp_reduce_scatter(const float (&x)[16]) {
 }
 
 // ---------------------------------------------------------------------------
-template <typename T, typename OutT>
+// kChains: the flavour for plans with node-parallel split windows (its chain
+// bookkeeping costs the other plans registers, so they run the one without).
+template <typename T, typename OutT, bool kChains>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     TileSmem& sm = *reinterpret_cast<TileSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -206,37 +221,61 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
     const T* V = static_cast<const T*>(p.V);
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescO = idesc_f16(kBf16, true, 128, kRows, true);  // A and B MN-major
-    const int n_work = (int)(p.n_tile_items * p.H);  // work index k H + h: item k, head h
+    // Work indices: k H + h for item k < n_single and head h (every item on its
+    // own); then, with node-parallel split windows, n_single H + j H + h for the
+    // chain of split window j (its slices, consecutive items, all taken by the
+    // CTA that drew the index).
+    const int n_single_work = (int)(p.n_single_items * p.H);
+    const int n_work = n_single_work + (kChains ? p.n_chains * p.H : 0);
     const long long node_stride = (long long)p.H * kD;
     constexpr int kFetcher = 96;  // the thread that takes work indices and loads item descriptors
 
-    // the descriptor of work index wk (an empty one past the end)
-    auto load_desc = [&](int wk, int4& a, int4& b) {
+    // The fetcher's state: the next work index (taken from the counter one
+    // item ahead) and the rest of the chain it is expanding.
+    int wk_next = 0, chain_k = 0, chain_left = 0, chain_h = 0;
+    // the next item's descriptor (an empty one past the end); true when it
+    // took wk_next, which the caller then replaces
+    auto next_desc = [&](int4& a, int4& b) {
+        if (kChains && chain_left > 0) {
+            a = p.tile_items[2 * chain_k];
+            b = p.tile_items[2 * chain_k + 1];
+            b.w = chain_h;
+            ++chain_k;
+            --chain_left;
+            return false;
+        }
         a = b = make_int4(0, 0, 0, 0);
-        if (wk < n_work) {
+        const int wk = wk_next;
+        if (wk < n_single_work) {
             const int k = wk / p.H;
             a = p.tile_items[2 * k];
             b = p.tile_items[2 * k + 1];
             b.w = wk - k * p.H;
+        } else if (kChains && wk < n_work) {
+            const int j = (wk - n_single_work) / p.H;
+            const int2 u = p.chains[j];  // (first slice item, slices)
+            chain_h = wk - n_single_work - j * p.H;
+            a = p.tile_items[2 * u.x];
+            b = p.tile_items[2 * u.x + 1];
+            b.w = chain_h;
+            chain_k = u.x + 1;
+            chain_left = u.y - 1;
         }
+        return true;
     };
 
     if (warp == 0) tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    int wk_next = 0;  // fetcher: the work index of the item whose descriptor it loads next
     if (tid == 0) {
         mbar_init(smem_u32(&sm.bar_s), 1);
         mbar_init(smem_u32(&sm.bar_o), 1);
         fence_mbar_init();
     }
     if (tid == kFetcher) {
-        // items 0-2 now, item 3's work index for the first iteration (a CTA that
-        // starts late takes fewer)
-        int wk[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) wk[j] = (int)atomicAdd(p.work_counter, 1u);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) load_desc(wk[j], sm.desc[j][0], sm.desc[j][1]);
-        wk_next = wk[3];
+        // items 0-2 now, and the next work index (a CTA that starts late takes fewer)
+        wk_next = (int)atomicAdd(p.work_counter, 1u);
+#pragma unroll 1
+        for (int j = 0; j < 3; ++j)
+            if (next_desc(sm.desc[j][0], sm.desc[j][1])) wk_next = (int)atomicAdd(p.work_counter, 1u);
     }
     tc_fence_before();
     __syncthreads();
@@ -307,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
     // lanes 0-63 and again 64-127 hold the 64 features; warps 0 and 1 take
     // rows 0-7 of each window, warps 2 and 3 rows 8-15, 32 features per warp.
     auto epilogue = [&](const int4& a, const int4& b) {
+        if (kChains && (a.w & kItemChain) && b.x != b.y - 1) return;  // a chain's rows are stored after its last slice
         const int nw = item_nwin(a);
         const int f = (warp & 1) * 32 + (tid & 31);
         const int r0 = (warp >> 1) * 8;
@@ -381,12 +421,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
             }
             tc_fence_after();
         }
-        // the fetcher: a work index three items ahead, the descriptor of item i+3
-        int grab = 0;
+        // the fetcher: the descriptor of item i+3 (and a new work index when it
+        // took the last one)
         int4 fa = make_int4(0, 0, 0, 0), fb = fa;
+        bool took = false;
+        int grab = 0;
         if (tid == kFetcher) {
-            grab = (int)atomicAdd(p.work_counter, 1u);
-            load_desc(wk_next, fa, fb);
+            took = next_desc(fa, fb);
+            if (took) grab = (int)atomicAdd(p.work_counter, 1u);
         }
         // (b) item i+1's K, Q and bitmaps, then item i's V rows
         const int4 a1 = sm.desc[(i + 1) % kRing][0], b1 = sm.desc[(i + 1) % kRing][1];
@@ -428,23 +470,48 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
                 x[r] = on ? x[r] * scale : -INFINITY;
             }
         }
-        // (e) row maxima: per half-warp, then over the half-warps of each window
+        // (e) row maxima: per half-warp, then over the half-warps of each window.  A
+        // slice of a chain (a split window taken node-parallel, one window) keeps a
+        // reference max per row over its slices, moved only when a slice's max
+        // exceeds it by more than 2^8; O and the row sums are rescaled then.
+        const bool chain = kChains && (a0.w & kItemChain);
+        const bool chain_first = chain && b0.x == 0;
         sm.part[hw][tid & 15] = halfwarp_reduce_scatter<true>(x);
         tc_fence_before();
         __syncthreads();
+        int rescale = 0;
         if (tid < kItemRows) {
             const int j = tid >> 4, r = tid & 15;
             float m = -INFINITY;
 #pragma unroll
             for (int g = 0; g < kHalfWarps; ++g)
                 if ((nw == 2 && 16 * g >= split) == (j == 1)) m = fmaxf(m, sm.part[g][r]);
+            if (chain && tid < kRows) {
+                const float mref = chain_first ? -INFINITY : sm.mref[tid];
+                const float mnew = m > mref + kLazyRescale ? m : mref;
+                const float f = mnew == mref ? 1.f : ex2(mref - mnew);
+                sm.mref[tid] = mnew;
+                sm.fac[tid] = f;
+                rescale = !chain_first && f != 1.f;
+                m = mnew;
+            }
             sm.rowmax[tid] = m == -INFINITY ? 0.f : m;  // a row without entries: every P is 0
         }
         cp_async_wait_group<1>();  // item i+1's K, Q and bitmaps (item i's V may still be in flight)
         fence_proxy_async_smem();
-        __syncthreads();
+        if constexpr (kChains)
+            rescale = __syncthreads_or(rescale);
+        else
+            __syncthreads();
         tc_fence_after();
         if (tid == 0 && item_nwin(a1) > 0) issue_s(a1);  // runs while item i forms P
+        if (kChains && rescale) {  // CTA-uniform: the chain's O rows (TMEM columns) times their factors
+            float o[kRows];
+            tmem_ld16(tmem + 32 + lane_base, o);
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) o[r] *= sm.fac[r];
+            tmem_st16(tmem + 32 + lane_base, o);
+        }
         // (f) this column's 16 values of P, one 32-byte row of P^T (rows 0-7 and 8-15 in
         // the two 16-byte halves, swapped on every other group of four columns), and
         // the row sums of the rounded values
@@ -481,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
                 for (int kk = 0; kk < ksteps; ++kk) {
                     const uint32_t va = vbase + (uint32_t)(c0 + 16 * kk) * 128;
                     mma_f16(tmem + 32 + 16 * j, sdesc_sw128(va, 0, 1024),
-                            sdesc_sw32(ptbase + (uint32_t)(c0 + 16 * kk) * 32, 0, 256), kIdescO, kk > 0 ? 1u : 0u);
+                            sdesc_sw32(ptbase + (uint32_t)(c0 + 16 * kk) * 32, 0, 256), kIdescO,
+                            kk > 0 || (chain && !chain_first) ? 1u : 0u);
                 }
             }
             mma_commit(smem_u32(&sm.bar_o));
@@ -492,6 +560,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
 #pragma unroll
             for (int g = 0; g < kHalfWarps; ++g)
                 if ((nw == 2 && 16 * g >= split) == (j == 1)) l += sm.part[g][r];
+            if (chain && tid < kRows) {
+                if (!chain_first) l += sm.lacc[tid] * sm.fac[tid];
+                sm.lacc[tid] = l;
+            }
             sm.inv_l[tid] = l > 0.f ? 1.0f / l : 0.f;
             sm.rowsum[tid] = l;
         }
@@ -500,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
         if (tid == kFetcher) {
             sm.desc[(i + 3) % kRing][0] = fa;
             sm.desc[(i + 3) % kRing][1] = fb;
-            wk_next = grab;
+            if (took) wk_next = grab;
         }
         ++done;
     }
@@ -535,14 +607,15 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns, int32_t* statu
     if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(status, kErrTimeout);
 }
 
-template <typename T, typename OutT>
-cudaError_t launch(const TileParams& p, cudaStream_t st) {
-    if (p.n_tile_items <= 0) return cudaSuccess;
+template <typename T, typename OutT, bool kChains>
+cudaError_t launch_flavour(const TileParams& p, cudaStream_t st) {
+    const long long work = (p.n_single_items + p.n_chains) * p.H;
+    if (work <= 0) return cudaSuccess;
     const size_t smem = sizeof(TileSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT, kChains>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // all of the SM's unified L1/shared storage as shared memory, so four CTAs fit
-    e = cudaFuncSetAttribute(tile_kernel<T, OutT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(tile_kernel<T, OutT, kChains>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     // resident CTAs per SM from shared memory, registers and TMEM (the
@@ -553,17 +626,21 @@ cudaError_t launch(const TileParams& p, cudaStream_t st) {
     if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, tile_kernel<T, OutT>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, tile_kernel<T, OutT, kChains>)) != cudaSuccess) return e;
     int per_sm = smem_sm / (int)(smem + reserved);
     const int regs = (fa.numRegs + 7) / 8 * 8 * kThreads;
     if (regs > 0 && 65536 / regs < per_sm) per_sm = 65536 / regs;
     if ((int)(512 / kTmemCols) < per_sm) per_sm = (int)(512 / kTmemCols);
     if (per_sm < 1) per_sm = 1;
-    const long long work = p.n_tile_items * p.H;
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (grid > work) grid = work;
-    tile_kernel<T, OutT><<<(unsigned)grid, kThreads, smem, st>>>(p);
+    tile_kernel<T, OutT, kChains><<<(unsigned)grid, kThreads, smem, st>>>(p);
     return cudaGetLastError();
+}
+
+template <typename T, typename OutT>
+cudaError_t launch(const TileParams& p, cudaStream_t st) {
+    return p.n_chains > 0 ? launch_flavour<T, OutT, true>(p, st) : launch_flavour<T, OutT, false>(p, st);
 }
 
 }  // namespace

@@ -72,7 +72,7 @@ def test_default_options(lib):
         and o.out_dtype == 0
     assert abs(o.rtm_epsilon - 1e-6) < 1e-12 and o.rtm_elementwise_clamp == 1
     assert o.pack_rows == -1 and o.degree_buckets == 0 and o.small_graph_rows == 1024
-    assert o.tile_split_density_milli == 250
+    assert o.tile_split_density_milli == 250 and o.tile_split_parallel == 0
 
 
 @pytest.mark.parametrize("args,status", [
@@ -102,22 +102,26 @@ def test_bad_options_rejected(lib):
     for kw in (dict(bucket_bounds=[10, 5, 20]), dict(heavy_threshold=-1), dict(chunk_edges=0),
                dict(bsb_smem_edges=100000), dict(tile_path=2), dict(pack_rows=2), dict(tile_pool_density_milli=-1),
                dict(degree_buckets=2), dict(small_graph_rows=-1), dict(tile_split_density_milli=-1),
-               dict(tile_split_density_milli=99), dict(tile_split_density_milli=1001)):
+               dict(tile_split_density_milli=99), dict(tile_split_density_milli=1001),
+               dict(tile_split_parallel=2), dict(tile_split_parallel=-1)):
         with pytest.raises(g3s.G3SError) as ei:
             g3s.workspace_size(100, 1000, 4, 32, "bf16", **kw)
         assert ei.value.status == 1
 
 
 def test_workspace_of_split_windows(lib):
-    """The partial states of split windows are workspace only where the tile
-    path can run (fp16/bf16, d = 64, standard form), bounded by the split
-    density: 2000 E / (128 split_milli) partial rows of 4 H (d + 2) bytes."""
+    """The partial states of edge-parallel split windows are workspace only
+    where the tile path can run (fp16/bf16, d = 64, standard form), bounded by
+    the split density: 2000 E / (128 split_milli) partial rows of 4 H (d + 2)
+    bytes; node-parallel chains need none."""
     args = (10_000, 500_000, 8, 64, "bf16")
     off = g3s.workspace_size(*args, tile_split_density_milli=0)
-    on = g3s.workspace_size(*args)
-    dense = g3s.workspace_size(*args, tile_split_density_milli=1000)
+    edge = g3s.workspace_size(*args, tile_split_parallel=1)
+    dense = g3s.workspace_size(*args, tile_split_parallel=1, tile_split_density_milli=1000)
+    node = g3s.workspace_size(*args)
     rows = 2000 * 500_000 // (128 * 250) + 16
-    assert on - off >= rows * 4 * 8 * 66 and on > dense > off
+    assert edge - off >= rows * 4 * 8 * 66 and edge > dense > off
+    assert off < node < off + rows * 4 * 8 * 66 // 10
     assert g3s.workspace_size(10_000, 500_000, 4, 32, "bf16") == \
         g3s.workspace_size(10_000, 500_000, 4, 32, "bf16", tile_split_density_milli=0)
 

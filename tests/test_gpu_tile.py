@@ -236,7 +236,10 @@ def _selection_cases():
                                                    tile_max_tiles=5), True
     split_kw = dict(heavy_threshold=100, chunk_edges=64, small_graph_rows=0)
     yield "split_mixed", _split_graph, 2, split_kw, True
+    yield "split_mixed_edge", _split_graph, 2, dict(split_kw, tile_split_parallel=1), True
     yield "split_mixed_global_bitmap", _split_graph, 2, dict(split_kw, bsb_smem_edges=256), True
+    yield "split_mixed_edge_global_bitmap", _split_graph, 2, dict(split_kw, bsb_smem_edges=256, tile_split_parallel=1), \
+        True
     yield "split_mixed_dense_only", _split_graph, 2, dict(split_kw, tile_split_density_milli=600), True
     yield "split_off", _split_graph, 2, dict(split_kw, tile_split_density_milli=0), True
     yield "clustered_small", lambda: graphgen.make_workload("clustered_heavy", "small")[0], 8, \
@@ -270,13 +273,14 @@ def test_tile_selection_bit_exact(name, make, H, kw, tiled):
     tw, sw = sel["tile_windows"], sel["split_windows"]
     assert st["tile_windows"] == tw.size + sw.size and st["split_windows"] == sw.size
     assert st["tile_window_nnz"] == int(b["win_nnz"][tw].sum() + b["win_nnz"][sw].sum())
-    want_items = ref_planner.tile_items(g.row_ptr, b, tw, sw, n_chunks)
+    edge = opts.tile_split_parallel == 1
+    want_items = ref_planner.tile_items(g.row_ptr, b, tw, sw, n_chunks, edge)
     got_items = plan.export("tile_items")
     assert st["tile_items"] == want_items.shape[0]
     assert got_items.shape == want_items.shape and np.array_equal(got_items, want_items), "tile_items"
     if sw.size:
         ml = ref_planner.merge_list(g.row_ptr, b, sel["win_flags"], st["heavy_threshold"], hc["heavy_chunk_ptr"],
-                                    n_chunks)
+                                    n_chunks, edge)
         assert st["merge_rows"] == ml["merge_rows"].size
         assert np.array_equal(plan.export("merge_rows"), ml["merge_rows"]), "merge_rows"
         assert np.array_equal(plan.export("merge_ranges"), ml["merge_ranges"]), "merge_ranges"
@@ -293,16 +297,22 @@ def test_tile_selection_bit_exact(name, make, H, kw, tiled):
 # split windows: windows wider than 128 columns cut into 128-column slices
 # whose partial softmax states are merged per row
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("parallel", [0, 1], ids=["node", "edge"])
 @pytest.mark.parametrize("dtype,H", [("bf16", 2), ("f16", 4), ("bf16", 8)])
-def test_split_windows_parity(dtype, H):
+def test_split_windows_parity(dtype, H, parallel):
     """Split windows (heavy rows, light rows and empty rows in them), pairs,
     CUDA-core windows and heavy-row chunks outside the split windows in one
-    plan, every row against the oracle."""
+    plan, every row against the oracle; node-parallel (chains) and
+    edge-parallel (slices merged)."""
     g = _split_graph()
-    plan, _, _ = _run(g, H, dtype, dict(tile_path=1, heavy_threshold=100, chunk_edges=64, small_graph_rows=0))
+    plan, _, _ = _run(g, H, dtype, dict(tile_path=1, heavy_threshold=100, chunk_edges=64, small_graph_rows=0,
+                                        tile_split_parallel=parallel))
     st = plan.stats()
     assert st["split_windows"] > 0 and st["tile_windows"] > st["split_windows"]
-    assert st["windows"] > st["tile_windows"] and st["chunks"] > 0 and st["merge_rows"] > 0
+    assert st["windows"] > st["tile_windows"] and st["chunks"] > 0
+    # every heavy row of this graph sits in a split window: merged from its
+    # slices edge-parallel, final in the tile kernel node-parallel
+    assert (st["merge_rows"] > 0) == (parallel == 1)
 
 
 def test_split_windows_off():
@@ -312,23 +322,54 @@ def test_split_windows_off():
     assert plan.stats()["split_windows"] == 0
 
 
-def test_split_windows_sixteen_bit_output():
+@pytest.mark.parametrize("parallel", [0, 1], ids=["node", "edge"])
+def test_split_windows_sixteen_bit_output(parallel):
     g = _split_graph()
-    plan, O, _ = _run(g, 2, "bf16", dict(tile_path=1, heavy_threshold=100, chunk_edges=64, out_dtype="bf16"))
+    plan, O, _ = _run(g, 2, "bf16", dict(tile_path=1, heavy_threshold=100, chunk_edges=64, out_dtype="bf16",
+                                         tile_split_parallel=parallel))
     assert O.dtype == torch.bfloat16 and plan.stats()["split_windows"] > 0
 
 
-def test_clustered_heavy_small_workload():
+@pytest.mark.parametrize("parallel", [0, 1], ids=["node", "edge"])
+def test_clustered_heavy_small_workload(parallel):
     """Every window split (two slices of 16 and 8 tiles), every heavy row
     inside a split window (its chunks skipped), a ragged last window, empty
     rows."""
     g, vals, w = graphgen.make_workload("clustered_heavy", "small")
-    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant, plan_kw=dict(heavy_threshold=150))
+    plan, _, _ = run_case(g, vals, w.heads, w.head_dim, w.dtype, w.variant,
+                          plan_kw=dict(heavy_threshold=150, tile_split_parallel=parallel))
     plan.check()
     st = plan.stats()
     assert st["split_windows"] == st["windows"] and st["chunks"] > 0 and g.num_nodes % 16
-    assert st["merge_rows"] == g.num_nodes
+    assert st["merge_rows"] == (g.num_nodes if parallel else 0)
     assert np.any(g.degrees() == 0)
+
+
+def test_chain_rescale_across_slices():
+    """Node-parallel chains whose later slices carry much larger logits than
+    the first (the reference max moves, O and the row sums are rescaled in
+    TMEM), and rows whose first slices are empty."""
+    rng = np.random.default_rng(31)
+    n = 16 * 8
+    cols, deg = [], np.zeros(n, np.int64)
+    for i in range(n):
+        lo = 0 if i % 3 else 256  # every third row has nothing in the first two slices
+        s = np.sort(rng.choice(np.arange(lo, 512), size=160, replace=False))
+        cols.append(s)
+        deg[i] = s.size
+    nn = 512
+    rp = np.zeros(nn + 1, np.int32)
+    rp[1:n + 1] = np.cumsum(deg)
+    rp[n + 1:] = rp[n]
+    g = graphgen.Graph(rp, np.concatenate(cols).astype(np.int32))
+    vals = graphgen.make_values(nn, g.num_edges, 2, 64, False, seed=32)
+    vals["K"][256:] *= 6.0  # logits of the last two slices' columns far above the first ones'
+    for parallel in (0, 1):
+        plan, _, _ = run_case(g, vals, 2, 64, "bf16", "standard",
+                              plan_kw=dict(tile_path=1, tile_split_parallel=parallel))
+        plan.check()
+        st = plan.stats()
+        assert st["split_windows"] == 8 and st["split_items"] == 8 * 4
 
 
 def test_clustered_heavy_full_sampled_rows():

@@ -197,14 +197,16 @@ def _split_graph():
     return graphgen.Graph(np.concatenate(rp).astype(np.int32), np.concatenate(cols).astype(np.int32))
 
 
-def test_split_windows_invariants():
+@pytest.mark.parametrize("edge_parallel", [True, False])
+def test_split_windows_invariants(edge_parallel):
     """Split selection, slice items and the merge list of the reference planner:
     a split window is exactly a window of more than 16 tiles, no repeated pair
     and density >= split_milli / 1000; its slices cover its tiles in order, 16
     at a time; the partial indices of (slice, row) pairs cover [n_chunks,
     n_chunks + 16 x slices) once each; the merge list holds every row of a split
     window with the indices its slices write, and every other heavy row with its
-    chunks."""
+    chunks.  Node-parallel, a slice carries (s, S) instead and the merge list
+    holds only the heavy rows outside split windows."""
     g = _split_graph()
     b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
     deg = g.degrees()
@@ -227,10 +229,12 @@ def test_split_windows_invariants():
         assert 0 < len(split) < W
         assert set(split).isdisjoint(sel["tile_windows"]) and set(split).isdisjoint(sel["core_windows"])
         assert sorted(list(sel["tile_windows"]) + split + list(sel["core_windows"])) == list(range(W))
-        items = planner.tile_items(g.row_ptr, b, sel["tile_windows"], sel["split_windows"], n_chunks)
+        items = planner.tile_items(g.row_ptr, b, sel["tile_windows"], sel["split_windows"], n_chunks, edge_parallel)
         n_pair = planner.tile_items(g.row_ptr, b, sel["tile_windows"]).shape[0]
         sitems = items[n_pair:]
-        assert np.all(sitems[:, 3] & planner.ITEM_PARTIAL) and not np.any(items[:n_pair, 3] & planner.ITEM_PARTIAL)
+        flag = planner.ITEM_PARTIAL if edge_parallel else planner.ITEM_CHAIN
+        assert np.all(sitems[:, 3] & flag) and not np.any(items[:n_pair, 3] & (planner.ITEM_PARTIAL | planner.ITEM_CHAIN))
+        assert not np.any(sitems[:, 3] & (planner.ITEM_PARTIAL ^ planner.ITEM_CHAIN ^ flag))
         hit = {}
         k = 0
         for w in split:
@@ -241,16 +245,20 @@ def test_split_windows_invariants():
             assert mine[0, 1] == ptr[w] and np.all(mine[1:, 1] == mine[:-1, 1] + 16)
             assert mine[:, 2].sum() == nt[w] and np.all(mine[:-1, 2] == 16)
             assert np.all((mine[:, 3] & 0xFF) == 1) and np.all(((mine[:, 3] >> 8) & 0xFF) == (mine[:, 2] + 1) // 2)
+            if not edge_parallel:
+                assert list(mine[:, 4]) == list(range(S))
+                continue
             for it in mine:
                 for r in range(16):
                     hit.setdefault(int(it[4] + r * S), []).append((w, r))
         assert k == len(sitems)
-        total = 16 * sum(-(-int(nt[w]) // 16) for w in split)
-        assert sorted(hit) == list(range(n_chunks, n_chunks + total)) and all(len(v) == 1 for v in hit.values())
-        ml = planner.merge_list(g.row_ptr, b, fl, T, hc["heavy_chunk_ptr"], n_chunks)
+        if edge_parallel:
+            total = 16 * sum(-(-int(nt[w]) // 16) for w in split)
+            assert sorted(hit) == list(range(n_chunks, n_chunks + total)) and all(len(v) == 1 for v in hit.values())
+        ml = planner.merge_list(g.row_ptr, b, fl, T, hc["heavy_chunk_ptr"], n_chunks, edge_parallel)
         rows, ranges = list(ml["merge_rows"]), ml["merge_ranges"]
         heavy = list(hc["heavy_rows"])
-        want = sorted(set(r for r in range(g.num_nodes) if (r // 16) in split) |
+        want = sorted(set(r for r in range(g.num_nodes) if (r // 16) in split and edge_parallel) |
                       set(r for r in heavy if (r // 16) not in split))
         assert rows == want
         for r, (lo, hi) in zip(rows, ranges):
