@@ -82,7 +82,11 @@ typedef enum g3s_variant {
  *                  so long rows do not finish last.  0 (default): ten times
  *                  the mean degree E/N, clamped to [64, 512] (stats.heavy_threshold
  *                  reports the value used)
- *  chunk_edges     CSR positions per chunk of a heavy row (default 512)
+ *  chunk_edges     CSR positions per chunk of a heavy row (default 0:
+ *                  automatic, 512 x 256 / (node row bytes) between 64 and 512:
+ *                  512 for rows up to 256 bytes, 128 for 1 KB rows, since a
+ *                  warp walks a chunk one edge step at a time and a step takes
+ *                  fewer edges of wider rows)
  *  bsb             build the 16x8 BSB tiles: 1 on, 0 off, -1 when the tile path
  *                  is eligible (default -1)
  *  tile_path       route dense row windows to the tensor-core kernel: 1 on,

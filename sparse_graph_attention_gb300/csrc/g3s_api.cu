@@ -61,7 +61,7 @@ void default_options(g3s_plan_options* o) {
     o->bucket_bounds[1] = 256;
     o->bucket_bounds[2] = 2048;
     o->heavy_threshold = 0;  // automatic: 10 x mean degree in [64, 512]
-    o->chunk_edges = 512;
+    o->chunk_edges = 0;  // automatic: 512 entries of rows up to 256 bytes, fewer for wider rows
     o->bsb = -1;
     o->tile_path = -1;
     o->tile_density_milli = 100;
@@ -100,7 +100,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
             return fail(G3S_ERR_INVALID_ARG, "bucket_bounds must be positive and increasing");
     }
     if (o.heavy_threshold < 0) return fail(G3S_ERR_INVALID_ARG, "heavy_threshold must be >= 0 (0: automatic)");
-    if (o.chunk_edges < 1) return fail(G3S_ERR_INVALID_ARG, "chunk_edges must be >= 1");
+    if (o.chunk_edges < 0) return fail(G3S_ERR_INVALID_ARG, "chunk_edges must be >= 0 (0: automatic)");
     if (o.bsb < -1 || o.bsb > 1 || o.tile_path < -1 || o.tile_path > 1)
         return fail(G3S_ERR_INVALID_ARG, "bsb and tile_path take -1, 0 or 1");
     if (o.tile_density_milli < 0 || o.tile_max_tiles < 1 || o.tile_pool_density_milli < 0)
@@ -136,7 +136,16 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
         s->heavy_threshold = (int)(t < 64 ? 64 : (t > 512 ? 512 : t));
     }
     s->pack_limit = pack_limit_for((int)row_vecs, s->heavy_threshold);
-    s->chunk_edges = o.chunk_edges;
+    // Automatic chunk length: one warp walks a chunk an edge step at a time,
+    // and a step gathers fewer edges the wider the node row (one edge per
+    // step from 512-byte rows on), so chunks hold 512 x 256 / row bytes
+    // entries, between 64 and 512: 512 up to 256-byte rows, 128 for 1 KB.
+    if (o.chunk_edges > 0) {
+        s->chunk_edges = o.chunk_edges;
+    } else {
+        const long long c = 512LL * 256 / (row_bytes > 256 ? row_bytes : 256);
+        s->chunk_edges = (int)(c < 64 ? 64 : c);
+    }
     for (int k = 0; k < G3S_NUM_BUCKETS - 2; ++k) s->bounds[k] = o.bucket_bounds[k];
     s->bsb_smem_edges = o.bsb_smem_edges;
     s->bucket_lists = o.degree_buckets == 1;
@@ -155,7 +164,7 @@ g3s_status check_shape(int64_t N, int64_t E, int heads, int head_dim, int dtype,
         return fail(G3S_ERR_INVALID_ARG, "the tile path needs the BSB tiles (bsb = 0 with tile_path on)");
     const long long T = s->heavy_threshold;
     s->max_heavy = N < E / (T + 1) ? N : E / (T + 1);
-    s->max_chunks = E / o.chunk_edges + s->max_heavy;
+    s->max_chunks = E / s->chunk_edges + s->max_heavy;
     s->W = (N + kWinRows - 1) / kWinRows;
     s->max_tiles = s->build_bsb ? (E + 7 * s->W) / kTileCols : 0;
     // A split window of T > 16 tiles has S = ceil(T / 16) slices, 16 S < 2 T

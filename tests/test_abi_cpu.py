@@ -67,7 +67,7 @@ def test_version_and_status_strings(lib):
 def test_default_options(lib):
     o = g3s.default_options()
     assert list(o.bucket_bounds) == [32, 256, 2048]
-    assert o.heavy_threshold == 0 and o.chunk_edges == 512 and o.validate_graph == 1
+    assert o.heavy_threshold == 0 and o.chunk_edges == 0 and o.validate_graph == 1
     assert o.tile_density_milli == 100 and o.tile_pool_density_milli == 180 and o.tile_max_tiles == 16 \
         and o.out_dtype == 0
     assert abs(o.rtm_epsilon - 1e-6) < 1e-12 and o.rtm_elementwise_clamp == 1
@@ -99,7 +99,7 @@ def test_workspace_grows_with_bsb(lib):
 
 
 def test_bad_options_rejected(lib):
-    for kw in (dict(bucket_bounds=[10, 5, 20]), dict(heavy_threshold=-1), dict(chunk_edges=0),
+    for kw in (dict(bucket_bounds=[10, 5, 20]), dict(heavy_threshold=-1), dict(chunk_edges=-1),
                dict(bsb_smem_edges=100000), dict(tile_path=2), dict(pack_rows=2), dict(tile_pool_density_milli=-1),
                dict(degree_buckets=2), dict(small_graph_rows=-1), dict(tile_split_density_milli=-1),
                dict(tile_split_density_milli=99), dict(tile_split_density_milli=1001),
