@@ -228,7 +228,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
     const int n_single_work = (int)(p.n_single_items * p.H);
     const int n_work = n_single_work + (kChains ? p.n_chains * p.H : 0);
     const long long node_stride = (long long)p.H * kD;
-    constexpr int kFetcher = 96;  // the thread that takes work indices and loads item descriptors
+    // Roles, spread over the four warps so no warp is the others' barrier wait:
+    // thread 0 polls the mbarriers and warp 0 combines the row maxima, thread 32
+    // issues S^T, thread 64 issues O^T, warp 3 combines the row sums and thread
+    // 96 takes work indices and loads item descriptors.
+    constexpr int kIssueS = 32, kIssueO = 64, kFetcher = 96;
 
     // The fetcher's state: the next work index (taken from the counter one
     // item ahead) and the rest of the chain it is expanding.
@@ -396,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && item_nwin(sm.desc[0][0]) > 0) issue_s(sm.desc[0][0]);
+    if (tid == kIssueS && item_nwin(sm.desc[0][0]) > 0) issue_s(sm.desc[0][0]);
     const float scale = p.scale_log2;
     const int hw = tid >> 4;  // this thread's half-warp: columns 16 hw .. 16 hw + 15
     bool failed = false;
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
 #pragma unroll
             for (int r = 0; r < kRows; ++r) {
                 const bool on = live && ((w4[r >> 2] >> ((r & 3) * 8 + (c & 7))) & 1u);
-                x[r] = on ? x[r] * scale : -INFINITY;
+                x[r] = on ? x[r] : -INFINITY;  // unscaled: the scale goes into the maxima and the exponent
             }
         }
         // (e) row maxima: per half-warp, then over the half-warps of each window.  A
@@ -486,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
 #pragma unroll
             for (int g = 0; g < kHalfWarps; ++g)
                 if ((nw == 2 && 16 * g >= split) == (j == 1)) m = fmaxf(m, sm.part[g][r]);
+            m *= scale;  // log2 domain (scale > 0 keeps the max)
             if (chain && tid < kRows) {
                 const float mref = chain_first ? -INFINITY : sm.mref[tid];
                 const float mnew = m > mref + kLazyRescale ? m : mref;
@@ -504,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
         else
             __syncthreads();
         tc_fence_after();
-        if (tid == 0 && item_nwin(a1) > 0) issue_s(a1);  // runs while item i forms P
+        if (tid == kIssueS && item_nwin(a1) > 0) issue_s(a1);  // runs while item i forms P
         if (kChains && rescale) {  // CTA-uniform: the chain's O rows (TMEM columns) times their factors
             float o[kRows];
             tmem_ld16(tmem + 32 + lane_base, o);
@@ -521,8 +526,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 const float4 m = mr[q4];
-                w[2 * q4] = Half2<T>::pack(ex2(x[4 * q4] - m.x), ex2(x[4 * q4 + 1] - m.y));
-                w[2 * q4 + 1] = Half2<T>::pack(ex2(x[4 * q4 + 2] - m.z), ex2(x[4 * q4 + 3] - m.w));
+                w[2 * q4] = Half2<T>::pack(ex2(fmaf(x[4 * q4], scale, -m.x)), ex2(fmaf(x[4 * q4 + 1], scale, -m.y)));
+                w[2 * q4 + 1] =
+                    Half2<T>::pack(ex2(fmaf(x[4 * q4 + 2], scale, -m.z)), ex2(fmaf(x[4 * q4 + 3], scale, -m.w)));
             }
             const uint32_t row = ptbase + c * 32, sw = (uint32_t)((c >> 2) & 1) << 4;
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + sw), "r"(w[0]), "r"(w[1]), "r"(w[2]),
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
+        if (tid == kIssueO) {
             for (int j = 0; j < nw; ++j) {
                 const int c0 = j ? split : 0;
                 const int ksteps = j ? (min(b0.z, kTiles) + 1) / 2 : split / 16;
@@ -554,18 +560,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) tile_kernel(const Til
             }
             mma_commit(smem_u32(&sm.bar_o));
         }
-        if (tid < kItemRows) {
-            const int j = tid >> 4, r = tid & 15;
+        if (warp == 3) {
+            const int t = tid - 96, j = t >> 4, r = t & 15;
             float l = 0.f;
 #pragma unroll
             for (int g = 0; g < kHalfWarps; ++g)
                 if ((nw == 2 && 16 * g >= split) == (j == 1)) l += sm.part[g][r];
-            if (chain && tid < kRows) {
-                if (!chain_first) l += sm.lacc[tid] * sm.fac[tid];
-                sm.lacc[tid] = l;
+            if (chain && t < kRows) {
+                if (!chain_first) l += sm.lacc[t] * sm.fac[t];
+                sm.lacc[t] = l;
             }
-            sm.inv_l[tid] = l > 0.f ? 1.0f / l : 0.f;
-            sm.rowsum[tid] = l;
+            sm.inv_l[t] = l > 0.f ? 1.0f / l : 0.f;
+            sm.rowsum[t] = l;
         }
         // read after the next iteration's first barrier
         sm.cols[i & 1][tid] = col2;
