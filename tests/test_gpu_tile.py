@@ -403,3 +403,48 @@ def test_split_plan_aggregate():
     torch.cuda.synchronize()
     want = oracle.aggregate(g.row_ptr, g.col_idx, g.num_nodes, 2, 64, "bf16", wt, xt, normalize=True, eps=1e-6)
     assert_close(O, want, "bf16", "O (aggregate)")
+
+
+def _wide_window_graph(nnz_first: int, dup: bool, seed: int):
+    """Two 16-row windows over 160 source columns (20 tiles): the first holds
+    nnz_first entries (a row repeats a source when dup), the second is the
+    same pattern over columns shifted by 8; then 160 empty rows."""
+    rng = np.random.default_rng(seed)
+    n = 192
+    rows = [[] for _ in range(n)]
+    for w in (0, 1):
+        cols = np.arange(160) + 8 * w  # every column used at least once
+        per = [nnz_first // 16 + (1 if r < nnz_first % 16 else 0) for r in range(16)]
+        pool = list(cols)
+        rng.shuffle(pool)
+        k = 0
+        for r in range(16):
+            take = [pool[(k + j) % 160] for j in range(per[r])]
+            k += per[r]
+            rows[16 * w + r] = sorted(set(take))
+        if dup and w == 0:
+            rows[3] = sorted(rows[3] + [rows[3][0]])
+    deg = np.array([len(x) for x in rows])
+    rp = np.zeros(n + 1, np.int32)
+    rp[1:] = np.cumsum(deg)
+    col = np.concatenate([np.asarray(x, np.int64) for x in rows if x]).astype(np.int32)
+    return graphgen.Graph(rp, col)
+
+
+@pytest.mark.parametrize("nnz,dup,split", [(640, False, True), (639, False, False), (800, True, False)],
+                         ids=["at_threshold", "one_below", "repeated_pair"])
+def test_split_density_boundary_and_repeated_pairs(nnz, dup, split):
+    """A 20-tile window whose density is exactly 0.25 (640 entries) splits,
+    one entry fewer does not, and a dense window holding a repeated (row,
+    source) pair never does (it runs on CUDA cores); the device planner
+    matches the reference planner and O matches the oracle."""
+    from oracle import planner as ref_planner
+    g = _wide_window_graph(nnz, dup, seed=41)
+    b = ref_planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
+    assert int(np.diff(b["win_tile_ptr"])[0]) == 20 and int(b["win_nnz"][0]) == nnz + (1 if dup else 0)
+    plan, _, _ = _run(g, 2, "bf16", dict(tile_path=1, heavy_threshold=512))
+    flags = plan.export("win_flags")
+    assert bool(flags[0] & 8) == split and bool(flags[0] & 1) == dup
+    sel = ref_planner.tile_selection(g.row_ptr, b, True, heavy_threshold=512, max_tiles=16, density_milli=100,
+                                     pool_milli=180, split_milli=250)
+    assert np.array_equal(flags, sel["win_flags"])
