@@ -617,6 +617,8 @@ template <typename T, typename OutT, bool kChains>
 cudaError_t launch_flavour(const TileParams& p, cudaStream_t st) {
     const long long work = (p.n_single_items + p.n_chains) * p.H;
     if (work <= 0) return cudaSuccess;
+    // work indices are 32-bit (one counter, every CTA taking a few past the end)
+    if (work > (1ll << 30)) return cudaErrorInvalidValue;
     const size_t smem = sizeof(TileSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT, kChains>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
