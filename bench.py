@@ -497,6 +497,9 @@ def parse_args():
     ap.add_argument("--workload", default="lognormal_local", choices=list(graphgen.WORKLOADS))
     ap.add_argument("--size", default="full", choices=["full", "small"])
     ap.add_argument("--nodes", type=int, default=None, help="override the workload's node count (profiling)")
+    ap.add_argument("--local-frac", type=float, default=None,
+                    help="lognormal_local only: override the share of sources within +-4096 rows (default 0.6; "
+                         "1.0 and 0.0 separate the L2-served gathers from the HBM-served ones)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle work for the cpu_baseline sample")
     ap.add_argument("--tile-path", type=int, default=-1, choices=[-1, 0, 1],
                     help="tensor-core tile path: -1 automatic (default), 0 off, 1 on")
@@ -708,6 +711,10 @@ def main():
     torch.cuda.set_device(dev)
 
     over = {} if args.nodes is None else {"num_nodes": args.nodes}
+    if args.local_frac is not None:
+        if args.workload != "lognormal_local":
+            raise SystemExit("--local-frac applies to the lognormal_local workload")
+        over["local_frac"] = args.local_frac
     g, vals, w = graphgen.make_workload(args.workload, args.size, **over)
     t = {k: graphgen.to_dtype(v, w.dtype) for k, v in vals.items()}
     rp = torch.from_numpy(g.row_ptr).to(dev)
