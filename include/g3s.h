@@ -114,23 +114,29 @@ typedef enum g3s_variant {
  *                  the M side of the kernel's tcgen05 product)
  *  tile_split_density_milli  windows wider than 16 tiles (128 source
  *                  columns) whose density reaches tile_split_density_milli /
- *                  1000 take the tile path as split windows: each 128-column
- *                  slice is a work item of its own, written as a partial
- *                  softmax state (row max, row sum, unnormalised output) and
- *                  merged per row after the kernels, the way heavy-row chunks
- *                  are (the edge-parallel form of the Fused3S page's Figure 2
- *                  caption, with the columns split as in its Figure 3 caption).
- *                  Heavy rows inside a split window are computed there, not
- *                  as chunks.  Decided per window, outside the pooled rule.
- *                  0 turns split windows off; otherwise 100..1000 (default
- *                  250).  The partial states take workspace: up to
- *                  2000 * E / (128 * tile_split_density_milli) rows of
- *                  4 * H * (d + 2) bytes when the tile path is on.  Measured on
- *                  one GB300 (windows whose 16 rows each draw 1024 sources from
- *                  a pool shared by the window, 4.2 M entries, 8 x 64 bf16, ms
- *                  per forward, CUDA-core chunks against split windows before
- *                  the merge): density 1 0.87 against 0.11, 0.5 0.85 against
- *                  0.21, 0.25 0.85 against 0.40
+ *                  1000 take the tile path as split windows, cut into
+ *                  128-column slices (the columns split as in the Fused3S
+ *                  page's Figure 3 caption); heavy rows inside a split window
+ *                  are computed there, not as chunks.  Decided per window,
+ *                  outside the pooled rule.  0 turns split windows off;
+ *                  otherwise 100..1000 (default 250).
+ *  tile_split_parallel  how split windows run (the node- and edge-parallel
+ *                  blocks of the Fused3S page's Figure 2 caption): 0 (default)
+ *                  node-parallel, one CTA takes all slices of a window and head,
+ *                  O accumulating in tensor memory with the row maxima carried
+ *                  over the slices; 1 edge-parallel, every slice a work item of
+ *                  its own that writes a partial softmax state per row (row
+ *                  max, row sum, unnormalised output), merged per row after the
+ *                  kernels the way heavy-row chunks are.  Edge-parallel partial
+ *                  states take workspace: up to 2000 * E / (128 *
+ *                  tile_split_density_milli) rows of 4 * H * (d + 2) bytes.
+ *                  Measured on one GB300 (1024 windows whose rows share
+ *                  2048-node pools, 12.6 M entries, 8 x 64 bf16, ms per
+ *                  forward): CUDA-core path 1.86, node-parallel 0.86,
+ *                  edge-parallel 1.29; windows whose 16 rows each draw 1024 of
+ *                  a shared pool, 4.2 M entries, CUDA-core chunks against
+ *                  slices before the merge: density 1 0.87 against 0.11, 0.5
+ *                  0.85 against 0.21, 0.25 0.85 against 0.40
  *  bsb_smem_edges  windows with more CSR entries than this are compacted by
  *                  the global-bitmap planner kernel instead of the shared-
  *                  memory sort (default 2048; a testing knob)
