@@ -119,7 +119,8 @@ typedef enum g3s_variant {
  *                  page's Figure 3 caption); heavy rows inside a split window
  *                  are computed there, not as chunks.  Decided per window,
  *                  outside the pooled rule.  0 turns split windows off;
- *                  otherwise 100..1000 (default 250).
+ *                  otherwise 100..1000 (default 150: node-parallel slices beat
+ *                  the CUDA-core path from a density between 0.125 and 0.17).
  *  tile_split_parallel  how split windows run (the node- and edge-parallel
  *                  blocks of the Fused3S page's Figure 2 caption): 0 (default)
  *                  node-parallel, one CTA takes all slices of a window and head,
@@ -132,7 +133,7 @@ typedef enum g3s_variant {
  *                  tile_split_density_milli) rows of 4 * H * (d + 2) bytes.
  *                  Measured on one GB300 (1024 windows whose rows share
  *                  2048-node pools, 12.6 M entries, 8 x 64 bf16, ms per
- *                  forward): CUDA-core path 1.86, node-parallel 0.86,
+ *                  forward): CUDA-core path 1.86, node-parallel 0.80,
  *                  edge-parallel 1.29; windows whose 16 rows each draw 1024 of
  *                  a shared pool, 4.2 M entries, CUDA-core chunks against
  *                  slices before the merge: density 1 0.87 against 0.11, 0.5

@@ -75,7 +75,7 @@ void default_options(g3s_plan_options* o) {
     o->pack_rows = -1;
     o->degree_buckets = 0;
     o->small_graph_rows = kSmallGraphRows;
-    o->tile_split_density_milli = 250;
+    o->tile_split_density_milli = 150;
     o->tile_split_parallel = 0;
 }
 

@@ -72,7 +72,7 @@ def test_default_options(lib):
         and o.out_dtype == 0
     assert abs(o.rtm_epsilon - 1e-6) < 1e-12 and o.rtm_elementwise_clamp == 1
     assert o.pack_rows == -1 and o.degree_buckets == 0 and o.small_graph_rows == 1024
-    assert o.tile_split_density_milli == 250 and o.tile_split_parallel == 0
+    assert o.tile_split_density_milli == 150 and o.tile_split_parallel == 0
 
 
 @pytest.mark.parametrize("args,status", [
@@ -119,7 +119,7 @@ def test_workspace_of_split_windows(lib):
     edge = g3s.workspace_size(*args, tile_split_parallel=1)
     dense = g3s.workspace_size(*args, tile_split_parallel=1, tile_split_density_milli=1000)
     node = g3s.workspace_size(*args)
-    rows = 2000 * 500_000 // (128 * 250) + 16
+    rows = 2000 * 500_000 // (128 * 150) + 16
     assert edge - off >= rows * 4 * 8 * 66 and edge > dense > off
     assert off < node < off + rows * 4 * 8 * 66 // 10
     assert g3s.workspace_size(10_000, 500_000, 4, 32, "bf16") == \
