@@ -36,15 +36,18 @@
 // second half reading the same rows again (atom stride 0), so TMEM lanes
 // 64-127 repeat lanes 0-63 and all four warps store rows.
 //
-// Pipeline: one item in flight per CTA and four CTAs per SM (shared memory
-// for one stage of K, V, Q and P^T: about 43 KB), so the SM, not the CTA,
+// Pipeline: one item in flight per CTA and five CTAs per SM (shared memory
+// for one stage of K, V, Q and P^T: about 44 KB), so the SM, not the CTA,
 // hides the gathers' latency.  At the start of item i (S^T of item i and
 // O^T of item i-1 complete) the CTA requests item i+1's K, Q and bitmaps and
 // item i's V rows, stores item i-1's rows, and turns item i's logits into
 // row maxima; S^T of item i+1 is issued as soon as its K and Q have landed,
 // and runs while item i forms P; O^T of item i follows once its V rows are
 // in.  Work indices come from one counter; one thread keeps the descriptors
-// of the next three items in a shared-memory ring.
+// of the next three items in a shared-memory ring.  The serial roles are
+// spread over the four warps (mbarrier polling and the row-max combine in
+// warp 0, S^T issued from warp 1, O^T from warp 2, the row-sum combine and
+// the descriptor fetch in warp 3), so no warp holds the others at a barrier.
 //
 // Windows wider than 128 columns (split windows) are cut into 128-column
 // slices, taken either edge-parallel (each slice an item of its own that
@@ -622,7 +625,7 @@ cudaError_t launch_flavour(const TileParams& p, cudaStream_t st) {
     const size_t smem = sizeof(TileSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, OutT, kChains>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // all of the SM's unified L1/shared storage as shared memory, so four CTAs fit
+    // all of the SM's unified L1/shared storage as shared memory, so five CTAs fit
     e = cudaFuncSetAttribute(tile_kernel<T, OutT, kChains>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
