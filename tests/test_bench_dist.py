@@ -81,3 +81,24 @@ def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_sources_hash() != h0
     f.write_text('__global__ void k(int* p) { p[0] = 1; }\nconst char* s = "a//c";\n')
     assert bench.kernel_sources_hash() != h0
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    """Under torchrun the reference arm (the oracle on the host cores) runs
+    and prints on rank 0 alone; another rank exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_poisson", "--size", "small",
+           "--steps", "2", "--warmup", "1"]
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip() == "", r.stderr
+    env.update(RANK="0", LOCAL_RANK="0")
+    r = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "tiny_poisson"
