@@ -235,12 +235,15 @@ typedef enum g3s_plan_array {
                                     windows of at most 16 tiles */
     G3S_ARR_CORE_WINDOWS = 11,   /* [windows - tile_windows] ascending: the windows whose rows the
                                     CUDA-core kernel takes (every window without bit 1) */
-    G3S_ARR_TILE_ITEMS = 12,     /* [tile_items][8]: the tile kernel's items.  First the pairs:
-                                    tile-path list entries 2k and 2k+1 share an item when
-                                    ceil(T/2) of both (16-column units of T tiles) sum to <= 8;
-                                    per item (w0, first tile of w0, T0, nwin | units0 << 8,
-                                    w1, first tile of w1, T1, 0), the second window zero when
-                                    nwin = 1.  Then the split windows in ascending order, one
+    G3S_ARR_TILE_ITEMS = 12,     /* [tile_items][8]: the tile kernel's items.  First the windows
+                                    of the tile-path list, one or two per item: a window of T
+                                    tiles takes u = ceil(T/2) units of 16 columns; the list sorted
+                                    by (u, id) is matched from both ends, the widest remaining
+                                    window taking the narrowest remaining one when their units
+                                    sum to <= 8, else alone; per item (w0, first tile of w0, T0,
+                                    nwin | u0 << 8, w1, first tile of w1, T1, 0), window 0 the
+                                    narrower of a pair, the second window zero when nwin = 1.
+                                    Then the split windows in ascending order, one
                                     item per 128-column slice s of S = ceil(T/16):
                                     (w, first tile + 16 s, its tiles, 1 | units << 8 | 1 << 16,
                                      chunks + B_w + s, S, 0, 0), where B_w = 16 x (the slices of

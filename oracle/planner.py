@@ -193,36 +193,38 @@ def tile_selection(row_ptr: np.ndarray, b: dict, enabled: bool, heavy_threshold:
 
 def tile_items(row_ptr: np.ndarray, b: dict, tile_windows: np.ndarray, split_windows=(), n_chunks: int = 0,
                edge_parallel: bool = False) -> np.ndarray:
-    """Work items of the tile kernel, (n_items, 8) int32.  Entries 2k and
-    2k+1 of the tile-path list share an item when ceil(T/2) of each (T = the
-    window's tile count, so 16-column units) sum to at most 8; otherwise each
-    is an item of its own, as is a last unpaired entry.  Per item:
-    (w0, first tile of w0, T0, nwin | units0 << 8, w1, first tile of w1, T1, 0),
-    the second half zero when nwin = 1.  Then one item per slice s of each
-    split window w (point 4 above): (w, first tile + 16 s, its tiles t_s,
-    1 | ceil(t_s/2) << 8 | 1 << 16, n_chunks + 16 B_w + s, S_w, 0, 0)
-    edge-parallel, (w, first tile + 16 s, t_s, 1 | ceil(t_s/2) << 8 | 1 << 17,
-    s, S_w, 0, 0) node-parallel."""
+    """Work items of the tile kernel, (n_items, 8) int32.  A window of T
+    tiles takes u = ceil(T/2) units of 16 columns (1..8); two windows share an
+    item when their units sum to at most 8.  The tile-path list is sorted by
+    (u, position in the list) and matched from both ends: the widest
+    remaining window takes the narrowest remaining one when the two fit,
+    else it is an item on its own; items come in that order.  Per item:
+    (w0, first tile of w0, T0, nwin | u0 << 8, w1, first tile of w1, T1, 0)
+    with window 0 the narrower of a pair, the second half zero when nwin = 1.
+    Then one item per slice s of each split window w (point 4 above): (w,
+    first tile + 16 s, its tiles t_s, 1 | ceil(t_s/2) << 8 | 1 << 16,
+    n_chunks + 16 B_w + s, S_w, 0, 0) edge-parallel, (w, first tile + 16 s,
+    t_s, 1 | ceil(t_s/2) << 8 | 1 << 17, s, S_w, 0, 0) node-parallel."""
     ptr = b["win_tile_ptr"].astype(np.int64)
     out = []
 
-    def entry(i):
-        w = int(tile_windows[i])
+    def entry(w):
+        w = int(w)
         return w, int(ptr[w]), int(ptr[w + 1] - ptr[w])
 
-    n = len(tile_windows)
-    for i0 in range(0, n, 2):
-        w0, f0, t0 = entry(i0)
-        u0 = (t0 + 1) // 2
-        if i0 + 1 < n:
-            w1, f1, t1 = entry(i0 + 1)
-            if u0 + (t1 + 1) // 2 <= 8:
-                out.append([w0, f0, t0, 2 | (u0 << 8), w1, f1, t1, 0])
-            else:
-                out.append([w0, f0, t0, 1 | (u0 << 8), 0, 0, 0, 0])
-                out.append([w1, f1, t1, 1 | (((t1 + 1) // 2) << 8), 0, 0, 0, 0])
+    units = [(int(ptr[w + 1] - ptr[w]) + 1) // 2 for w in tile_windows]
+    order = sorted(range(len(tile_windows)), key=lambda i: (units[i], i))
+    lo, hi = 0, len(order) - 1
+    while lo <= hi:
+        wh, fh, th = entry(tile_windows[order[hi]])
+        uh = units[order[hi]]
+        if lo < hi and units[order[lo]] + uh <= 8:
+            wl, fl, tl = entry(tile_windows[order[lo]])
+            out.append([wl, fl, tl, 2 | (units[order[lo]] << 8), wh, fh, th, 0])
+            lo += 1
         else:
-            out.append([w0, f0, t0, 1 | (u0 << 8), 0, 0, 0, 0])
+            out.append([wh, fh, th, 1 | (uh << 8), 0, 0, 0, 0])
+        hi -= 1
     slices_before = 0
     for w in split_windows:
         w = int(w)

@@ -206,6 +206,8 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->win_flags = c.take<uint8_t>(s.W);
         a->tile_windows = c.take<int32_t>(s.W);
         a->tile_items = c.take<int4>(2 * (s.W + s.max_split_items));
+        a->tile_sorted = c.take<int32_t>(s.W);
+        a->tile_runs = c.take<int4>(32);
         a->core_windows = c.take<int32_t>(s.W);
         a->large_windows = c.take<int32_t>(s.W);
         a->tile_cols = c.take<int32_t>(s.max_tiles * kTileCols);
@@ -217,8 +219,9 @@ size_t carve(const PlanShape& s, PlanArrays* a, void* base) {
         a->merge_range = split ? c.take<int2>(s.N) : nullptr;
         a->chains = split && !s.split_edge_parallel ? c.take<int2>(s.W) : nullptr;
     } else {
-        a->win_split_base = a->merge_rows = nullptr;
+        a->win_split_base = a->merge_rows = a->tile_sorted = nullptr;
         a->merge_range = a->chains = nullptr;
+        a->tile_runs = nullptr;
         a->win_tile_ptr = a->win_ucount = a->win_nnz = a->tile_windows = a->large_windows = a->tile_cols = nullptr;
         a->core_windows = nullptr;
         a->tile_items = nullptr;

@@ -28,10 +28,10 @@ enum : int32_t {
 };
 
 constexpr int kTileMaxTilesPerWindow = 16;  // tile-path windows have at most this many 16x8 tiles (128 columns)
-// A tile-kernel item holds one or two consecutive tile-path windows (in list
-// order), each starting at a 16-column boundary of the item, together at most
-// 128 columns: a window of T tiles takes ceil(T/2) units of 16 columns, and a
-// pair is formed from list entries (2k, 2k+1) when their units sum to <= 8.
+// A tile-kernel item holds one or two tile-path windows, each starting at a
+// 16-column boundary of the item, together at most 128 columns: a window of T
+// tiles takes ceil(T/2) units of 16 columns, and two windows pair when their
+// units sum to <= 8 (matched over the whole list, g3s_planner.cu).
 // Stored as two int4: (w0, first tile of w0, T0, nwin | units0 << 8) and
 // (w1, first tile of w1, T1, 0).  A slice s of the S slices of a split window
 // w (one item per 16 tiles) is (w, first tile + 16 s, its tiles, 1 | units <<
@@ -61,6 +61,8 @@ struct PlanCounts {
     int32_t n_split_items;    // their slices (tile items after the n_tile_items pairs)
     int32_t n_merge;          // rows a forward merges (with split windows; else the heavy rows)
     long long split_nnz;      // CSR entries of the split windows
+    int32_t unit_count[kTileItemUnits + 1];  // tile-path windows by 16-column units (index 1..8)
+    int32_t n_match_runs;     // runs of the item matching (planner scratch)
 };
 
 // Device views the planner writes into (all inside the caller's workspace).
@@ -81,6 +83,8 @@ struct PlanArrays {
     uint8_t* win_flags;        // [W]
     int32_t* tile_windows;     // [W]
     int4* tile_items;          // [2 (W + max_split_items)] tile kernel items: two int4 per item (kTileItemUnits)
+    int32_t* tile_sorted;      // [W] tile-path windows sorted by (units, id) (planner scratch)
+    int4* tile_runs;           // [32] runs of the item matching (planner scratch)
     int32_t* win_split_base;   // [W] split windows: slices of the split windows before this one
     int32_t* merge_rows;       // [N] rows a forward merges when the plan has split windows
     int2* merge_range;         // [N] their partial index ranges

@@ -599,48 +599,90 @@ __global__ void k_tile_pool(long long W, uint8_t* win_flags, int pool_milli, Pla
     if (blockIdx.x == 0 && threadIdx.x == 0) c->tile_window_nnz = take ? (long long)nnz : 0;
 }
 
-// Tile-kernel items: list entries (2k, 2k+1) share an item when their
-// 16-column units (ceil(T/2) each) sum to at most kTileItemUnits.
-struct TilePair {
+// Tile-kernel items.  A tile-path window of T tiles takes u = ceil(T/2)
+// units of 16 columns (1..8); two windows share an item when their units sum
+// to at most kTileItemUnits.  The list is sorted by (u, window id) -- eight
+// stable scans put each unit bucket in place -- and matched from both ends:
+// the widest remaining window takes the narrowest remaining one when the two
+// fit, else it is an item on its own (the fewest items any pairing reaches).
+// The walk runs over the eight bucket counts in one thread as at most 17
+// runs of identical steps; a parallel kernel then writes the items.
+constexpr int kMaxMatchRuns = 32;
+__device__ __forceinline__ int window_units(const int32_t* win_tile_ptr, int w) {
+    return (win_tile_ptr[w + 1] - win_tile_ptr[w] + 1) / 2;
+}
+struct UnitFlag {
     const int32_t* tile_windows;
     const int32_t* win_tile_ptr;
     const PlanCounts* c;
-    __device__ int ntiles(long long i) const {
-        const int w = tile_windows[i];
-        return win_tile_ptr[w + 1] - win_tile_ptr[w];
-    }
-    __device__ int operator()(long long pair) const {
-        const long long n = c->n_tile_windows, i0 = 2 * pair;
-        if (i0 >= n) return 0;
-        if (i0 + 1 >= n) return 1;
-        return (ntiles(i0) + 1) / 2 + (ntiles(i0 + 1) + 1) / 2 <= kTileItemUnits ? 1 : 2;
+    int u;
+    __device__ int operator()(long long i) const {
+        return i < c->n_tile_windows && window_units(win_tile_ptr, tile_windows[i]) == u ? 1 : 0;
     }
 };
-struct TilePairOut {
-    TilePair pr;
-    int4* items;
-    __device__ int4 single(long long i, int nwin, int units0) const {
-        const int w = pr.tile_windows[i];
-        const int t0 = pr.win_tile_ptr[w];
-        return make_int4(w, t0, pr.win_tile_ptr[w + 1] - t0, nwin | (units0 << 8));
+struct UnitOut {
+    const int32_t* tile_windows;
+    const PlanCounts* c;
+    int32_t* sorted;
+    int u;
+    __device__ void operator()(long long i, int p, int v) const {
+        if (!v) return;
+        int base = 0;
+        for (int b = 1; b < u; ++b) base += c->unit_count[b];
+        sorted[base + p] = tile_windows[i];
     }
-    __device__ void operator()(long long pair, int p, int v) const {
-        const long long i0 = 2 * pair;
-        if (v == 1) {
-            const bool two = i0 + 1 < pr.c->n_tile_windows;
-            const int units0 = (pr.ntiles(i0) + 1) / 2;
-            items[2 * p] = single(i0, two ? 2 : 1, units0);
-            int4 b = two ? single(i0 + 1, 0, 0) : make_int4(0, 0, 0, 0);
-            b.w = 0;
-            items[2 * p + 1] = b;
-        } else if (v == 2) {
-            items[2 * p] = single(i0, 1, (pr.ntiles(i0) + 1) / 2);
-            items[2 * p + 1] = make_int4(0, 0, 0, 0);
-            items[2 * p + 2] = single(i0 + 1, 1, (pr.ntiles(i0 + 1) + 1) / 2);
-            items[2 * p + 3] = make_int4(0, 0, 0, 0);
+};
+// runs[r] = (count << 1 | pair, low position, high position, first item)
+__global__ void k_match_runs(PlanCounts* c, int4* runs) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int base[kTileItemUnits + 2];
+    base[1] = 0;
+    for (int b = 1; b <= kTileItemUnits; ++b) base[b + 1] = base[b] + c->unit_count[b];
+    auto bucket = [&](int pos) {
+        int b = 1;
+        while (b < kTileItemUnits && pos >= base[b + 1]) ++b;
+        return b;
+    };
+    int lo = 0, hi = base[kTileItemUnits + 1] - 1, nr = 0, items = 0;
+    while (lo <= hi && nr < kMaxMatchRuns) {
+        const int bl = bucket(lo), bh = bucket(hi);
+        const bool pair = lo < hi && bl + bh <= kTileItemUnits;
+        int k;
+        if (pair)
+            k = bl == bh ? (hi - lo + 1) / 2 : min(base[bl + 1] - lo, hi - base[bh] + 1);
+        else
+            k = hi - max(base[bh], lo) + 1;  // the rest of the high bucket, each on its own
+        runs[nr++] = make_int4(k << 1 | (pair ? 1 : 0), lo, hi, items);
+        items += k;
+        if (pair) lo += k;
+        hi -= k;
+    }
+    c->n_tile_items = items;
+    c->n_match_runs = nr;
+}
+__global__ void k_match_items(const PlanCounts* c, const int4* runs, const int32_t* sorted,
+                              const int32_t* win_tile_ptr, int4* items, long long W) {
+    const int n = c->n_tile_items, nr = c->n_match_runs;
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
+        int r = 0;
+        while (r + 1 < nr && runs[r + 1].w <= k) ++r;
+        const int4 R = runs[r];
+        const int j = (int)k - R.w;
+        const int wh = sorted[R.z - j];
+        const int th = win_tile_ptr[wh];
+        const int4 high = make_int4(wh, th, win_tile_ptr[wh + 1] - th, 0);
+        if (R.x & 1) {
+            const int wl = sorted[R.y + j];
+            const int tl = win_tile_ptr[wl];
+            items[2 * k] = make_int4(wl, tl, win_tile_ptr[wl + 1] - tl, 2 | (window_units(win_tile_ptr, wl) << 8));
+            items[2 * k + 1] = high;
+        } else {
+            items[2 * k] = make_int4(wh, th, high.z, 1 | (window_units(win_tile_ptr, wh) << 8));
+            items[2 * k + 1] = make_int4(0, 0, 0, 0);
         }
     }
-};
+    (void)W;
+}
 
 struct TileFlag {  // tile-path windows of at most 16 tiles (the pairs' list)
     const uint8_t* win_flags;
@@ -850,9 +892,14 @@ cudaError_t plan_build(const int32_t* row_ptr, const int32_t* col_idx, const Pla
         G3S_TRY(cudaGetLastError());
     }
     G3S_TRY(scan(TileFlag{a.win_flags}, ListOut{a.tile_windows}, W, a.scan_blocks, &c->n_tile_windows, st));
-    if (s.tile_enabled) {
-        const TilePair pr{a.tile_windows, a.win_tile_ptr, c};
-        G3S_TRY(scan(pr, TilePairOut{pr, a.tile_items}, (W + 1) / 2, a.scan_blocks, &c->n_tile_items, st));
+    if (s.tile_enabled && W > 0) {
+        for (int u = 1; u <= kTileItemUnits; ++u)
+            G3S_TRY(scan(UnitFlag{a.tile_windows, a.win_tile_ptr, c, u}, UnitOut{a.tile_windows, c, a.tile_sorted, u}, W,
+                         a.scan_blocks, &c->unit_count[u], st));
+        k_match_runs<<<1, 32, 0, st>>>(c, a.tile_runs);
+        G3S_TRY(cudaGetLastError());
+        k_match_items<<<grid_for(W, 256), 256, 0, st>>>(c, a.tile_runs, a.tile_sorted, a.win_tile_ptr, a.tile_items, W);
+        G3S_TRY(cudaGetLastError());
     }
     if (s.max_split_items > 0) {
         G3S_TRY(scan(SplitCount{a.win_flags, a.win_tile_ptr},

@@ -149,36 +149,57 @@ def test_tile_selection_brute_force():
 
 
 def test_tile_items_pairing():
-    """Every tile-path window sits in exactly one item, in list order; two
-    share an item only as list entries 2k and 2k+1 and only when their
-    16-column units (ceil(T/2)) fit the 8 units of an item; an item of two
-    starts its second window at 16 * units0 columns."""
+    """Every tile-path window sits in exactly one item; two windows share an
+    item only when their 16-column units (ceil(T/2)) fit the 8 of an item,
+    the narrower first; no two single windows could have shared one; and on
+    small random unit mixes the number of items equals the fewest any pairing
+    reaches (brute force over all pairings)."""
+    from functools import lru_cache
     g = graphgen.batched_dense(num_graphs=60, seed=12)
     b = planner.bsb(g.row_ptr, g.col_idx, g.num_nodes)
     sel = planner.tile_selection(g.row_ptr, b, True, heavy_threshold=100, max_tiles=16, density_milli=0)
     tw = sel["tile_windows"]
     items = planner.tile_items(g.row_ptr, b, tw)
     ptr = b["win_tile_ptr"]
-    seen = []
+    units = lambda w: (ptr[w + 1] - ptr[w] + 1) // 2  # noqa: E731
+    seen, singles = [], []
     for it in items:
         nwin, u0 = it[3] & 0xFF, it[3] >> 8
         assert nwin in (1, 2)
         wins = [it[0]] + ([it[4]] if nwin == 2 else [])
         for w, first, t in zip(wins, (it[1], it[5]), (it[2], it[6])):
             assert first == ptr[w] and t == ptr[w + 1] - ptr[w]
-        assert u0 == (it[2] + 1) // 2
+        assert u0 == units(it[0])
         if nwin == 2:
-            assert u0 + (it[6] + 1) // 2 <= 8
-            assert len(seen) % 2 == 0  # a pair starts at an even list position
+            assert units(it[0]) <= units(it[4]) and units(it[0]) + units(it[4]) <= 8
         else:
             assert not np.any(it[4:])
+            singles.append(units(it[0]))
         seen += wins
-    assert seen == list(tw)
-    # an unpaired even entry: its partner did not fit
-    units = [(ptr[w + 1] - ptr[w] + 1) // 2 for w in tw]
-    pairs = sum(1 for it in items if (it[3] & 0xFF) == 2)
-    want_pairs = sum(1 for k in range(0, len(tw) - 1, 2) if units[k] + units[k + 1] <= 8)
-    assert pairs == want_pairs and 0 < pairs < len(tw) // 2 + 1
+    assert sorted(seen) == sorted(tw)
+    singles.sort()
+    assert len(singles) < 2 or singles[0] + singles[1] > 8
+    assert len(items) < 0.6 * len(tw)
+
+    rng = np.random.default_rng(13)
+    for _ in range(60):
+        n = int(rng.integers(1, 10))
+        T = rng.integers(1, 17, n)
+        fake = {"win_tile_ptr": np.concatenate([[0], np.cumsum(T)]).astype(np.int64)}
+        got = planner.tile_items(None, fake, np.arange(n))
+        u = [(int(t) + 1) // 2 for t in T]
+
+        @lru_cache(maxsize=None)
+        def fewest(mask):
+            if mask == (1 << n) - 1:
+                return 0
+            i = next(k for k in range(n) if not mask >> k & 1)
+            best = 1 + fewest(mask | 1 << i)
+            for j in range(i + 1, n):
+                if not mask >> j & 1 and u[i] + u[j] <= 8:
+                    best = min(best, 1 + fewest(mask | 1 << i | 1 << j))
+            return best
+        assert got.shape[0] == fewest(0), (u, got)
 
 
 def _split_graph():
