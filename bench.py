@@ -333,7 +333,12 @@ def tile_mma_flops(plan, heads: int, head_dim: int) -> int:
     over its 16-column units."""
     if not plan.stats()["tile_items"]:
         return 0
-    items = plan.export("tile_items").astype(np.int64)
+    return items_mma_flops(plan.export("tile_items"), heads, head_dim)
+
+
+def items_mma_flops(items, heads: int, head_dim: int) -> int:
+    """The same count from an (n, 8) tile-item array."""
+    items = np.asarray(items, np.int64).reshape(-1, 8)
     nwin = items[:, 3] & 0xFF
     units0 = (items[:, 3] >> 8) & 0xFF
     units1 = np.where(nwin == 2, (np.minimum(items[:, 6], 16) + 1) // 2, 0)

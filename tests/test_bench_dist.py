@@ -102,3 +102,21 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "tiny_poisson"
+
+
+def test_tile_item_flop_count():
+    """Issued tensor FLOPs of tile items, counted by hand: a pair of windows of
+    5 and 3 tiles (units 3 and 2) is S^T = 128 x 32 x d and O^T = 128 x 16 x 16
+    per unit of each window; a single window of 16 tiles (8 units) is
+    128 x 16 x d and 8 units; a split-window slice (flag bit 16 or 17) counts
+    as a single window of its tiles."""
+    d, H = 64, 8
+    pair = [10, 0, 5, 2 | (3 << 8), 11, 5, 3, 0]
+    single = [12, 8, 16, 1 | (8 << 8), 0, 0, 0, 0]
+    slice_ = [13, 24, 7, 1 | (4 << 8) | (1 << 17), 0, 3, 0, 0]
+    want_pair = 2 * 128 * 32 * d + 2 * 128 * 16 * 16 * (3 + 2)
+    want_single = 2 * 128 * 16 * d + 2 * 128 * 16 * 16 * 8
+    want_slice = 2 * 128 * 16 * d + 2 * 128 * 16 * 16 * 4
+    assert bench.items_mma_flops([pair], H, d) == H * want_pair
+    assert bench.items_mma_flops([pair, single, slice_], H, d) == H * (want_pair + want_single + want_slice)
+    assert bench.items_mma_flops([], H, d) == 0
