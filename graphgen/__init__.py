@@ -18,8 +18,7 @@ round-to-nearest-even (torch ``.to``) when the workload is a 16-bit one.
 from __future__ import annotations
 
 import dataclasses
-import math
-from typing import Callable, Dict, Optional
+from typing import Callable, Dict
 
 import numpy as np
 
